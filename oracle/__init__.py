@@ -1,0 +1,13 @@
+"""CPU oracle for TurboQuant_prod attention scores (TEST INFRASTRUCTURE).
+
+Plain, slow, float64 NumPy code that states what the GPU path must compute.
+It is used only by ``tests/``, by ``__graft_entry__.smoke()`` and by the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py``.  The product
+library never imports, links or calls anything here, and this package never
+imports the product.  Both sides take their raw random draws from ``synth``.
+
+Every function is pinned by a ``-m "not gpu"`` test against something other
+than itself (see ``tests/test_oracle_pins.py``).  No function here is
+"parity unpinned".
+"""
+from .tq_oracle import *  # noqa: F401,F403

@@ -1,0 +1,265 @@
+"""Float64 reference implementation of TurboQuant_prod compression and scoring.
+
+TEST INFRASTRUCTURE ONLY: used by tests, the smoke check and the CPU baseline
+of the benchmark; never by the product path.
+
+Sources (page title, then section):
+
+* [RY] "TurboQuant Attention in CUDA: Transform the Query, Reuse the Work"
+  (riteshyadav.xyz): "Move the transforms to the query", "A tiny example
+  before CUDA", "Two kernels, two jobs", "Full CUDA solution".
+* [KB] "TurboQuant: Rotate-then-Quantize KV Caches at 3 Bits" (kanthi.in):
+  §2 mental model, §3 "The quantizer in NumPy", §4 "Check the codebook
+  against the paper", §6 "The trap: unbiased is not the same as better",
+  §8 "Kernel view: never un-rotate a key".
+* [ZT] "Implementing TurboQuant on NVIDIA's AGX Thor" (zededa.com):
+  "Theorem 2: Unbiased Inner Products", v6 tile scorer.
+
+Where the pages are silent or garbled, the reading taken is stated in the
+docstring of the function concerned: tie-breaks, sign(0), the float32
+storage of Π, S_mat and the codebook, and the bit-packing format.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+__all__ = [
+    "SQRT_HALF_PI",
+    "kappa",
+    "haar_rotation",
+    "lloyd_max_sphere",
+    "nearest_cell",
+    "compress_prod",
+    "prepare_queries",
+    "scores",
+    "scores_from_queries",
+    "scores_sampled",
+    "pack_indices",
+    "unpack_indices",
+    "pack_signs",
+    "unpack_signs",
+    "f16_round",
+]
+
+SQRT_HALF_PI = math.sqrt(math.pi / 2.0)
+
+
+def kappa(D: int) -> float:
+    """QJL scale sqrt(pi/2)/D ([KB] §3 TurboQuantProd; [ZT] Theorem 2 item 1)."""
+    return SQRT_HALF_PI / D
+
+
+# ---------------------------------------------------------------------------
+# Rotation and codebook (inputs of the scorer, produced on the CPU)
+# ---------------------------------------------------------------------------
+
+def haar_rotation(G: np.ndarray) -> np.ndarray:
+    """Uniformly random orthogonal Π from a Gaussian matrix G ([KB] §3, HaarRotation).
+
+    G = Q R (Householder QR, LAPACK).  Each column j of Q is multiplied by the
+    sign of R[j, j] so that G = Π R' with R' upper triangular and a positive
+    diagonal; a zero diagonal entry keeps its column (sign taken as +1).  The
+    rotation acts on column vectors: y = Π k.
+    """
+    Q, R = np.linalg.qr(np.asarray(G, dtype=np.float64))
+    col_sign = np.where(np.diag(R) < 0.0, -1.0, 1.0)
+    return Q * col_sign[np.newaxis, :]
+
+
+def nearest_cell(values: np.ndarray, edges: np.ndarray) -> np.ndarray:
+    """Index of the codebook cell of each value: the number of edges strictly below it.
+
+    With sorted centroids the nearest-centroid rule is a search over the
+    midpoints ([KB] §3 "Indices are searched against midpoints").  A value
+    exactly on a midpoint goes to the lower cell (left-sided search).
+    """
+    v = np.asarray(values, dtype=np.float64)
+    out = np.zeros(v.shape, dtype=np.int64)
+    for e in np.asarray(edges, dtype=np.float64):
+        out += v > e
+    return out
+
+
+def lloyd_max_sphere(d: int, mse_bits: int, grid: int = 400_001, iters: int = 300):
+    """Lloyd-Max codebook for one coordinate of a uniform unit vector in R^d ([KB] §3-§4).
+
+    The coordinate has density proportional to (1 - x^2)^((d-3)/2) on [-1, 1]
+    ([KB] §2 fact 1).  The density is sampled on ``grid`` evenly spaced points
+    and normalised to unit mass; the 2^b centroids start evenly spaced on
+    [-2/sqrt(d), 2/sqrt(d)]; each of ``iters`` rounds sets the cell edges to
+    the midpoints of the current centroids and then every centroid to the
+    mean of its cell under the density.
+
+    Returns ``(centroids, edges, d_mse)`` in float64, where ``d_mse`` is
+    d * E[(x - Q(x))^2], the expected squared error of a unit vector.
+    """
+    if d < 3:
+        raise ValueError("the sphere-coordinate density needs d >= 3")
+    C = 1 << mse_bits
+    x = np.linspace(-1.0, 1.0, grid)
+    dens = np.clip(1.0 - x * x, 0.0, None) ** ((d - 3) / 2.0)
+    dens = dens / dens.sum()
+    centroids = np.linspace(-2.0, 2.0, C) / math.sqrt(d)
+    for _ in range(iters):
+        edges = 0.5 * (centroids[1:] + centroids[:-1])
+        cell = nearest_cell(x, edges)
+        new = np.empty(C)
+        for k in range(C):
+            member = cell == k
+            mass = dens[member].sum()
+            new[k] = (dens[member] * x[member]).sum() / mass
+        centroids = new
+    edges = 0.5 * (centroids[1:] + centroids[:-1])
+    err = x - centroids[nearest_cell(x, edges)]
+    d_mse = d * float(np.sum(dens * err * err))
+    return centroids, edges, d_mse
+
+
+# ---------------------------------------------------------------------------
+# Compressor: TurboQuant_prod on unit-norm keys
+# ---------------------------------------------------------------------------
+
+def f16_round(x: np.ndarray) -> np.ndarray:
+    """IEEE binary16 round-to-nearest-even of float64 values, returned as float64."""
+    return np.asarray(x, dtype=np.float64).astype(np.float16).astype(np.float64)
+
+
+def compress_prod(keys: np.ndarray, Pi: np.ndarray, S_mat: np.ndarray, codebook: np.ndarray,
+                  gamma_dtype: str = "f32"):
+    """TurboQuant_prod compression of unit-norm keys ([KB] §3 TurboQuantProd; [ZT] Theorem 2).
+
+    Steps, in the pages' order, for each key k (a row of ``keys``):
+
+    1. y = Π k (rotate; keys are unit length, so the stored norm is 1 and is
+       not kept -- the score has no norm term, [RY] "Move the transforms").
+    2. idx_d = nearest centroid of y_d (search over midpoints, ties to the
+       lower index).
+    3. r = k - Πᵀ c[idx] (residual of the MSE stage).
+    4. σ = sign(S_mat r) with sign(0) = +1 (the scorer needs ±1, [RY]).
+    5. γ = ‖r‖₂, stored as float32 or float16.
+
+    Π, S_mat and the codebook are used exactly as stored (float32 values
+    widened to float64), so the residual is taken against the keys the scorer
+    can reconstruct.  Returns ``(idx uint8 [S,D], signs int8 [S,D], gamma)``
+    with gamma float32 or float16.
+    """
+    k = np.asarray(keys, dtype=np.float64)
+    P = np.asarray(Pi, dtype=np.float64)
+    Sm = np.asarray(S_mat, dtype=np.float64)
+    c = np.asarray(codebook, dtype=np.float64)
+    y = k @ P.T
+    edges = 0.5 * (c[1:] + c[:-1])
+    idx = nearest_cell(y, edges)
+    r = k - c[idx] @ P
+    z = r @ Sm.T
+    signs = np.where(z >= 0.0, 1, -1).astype(np.int8)
+    g = np.sqrt(np.sum(r * r, axis=1))
+    if gamma_dtype == "f32":
+        gamma = g.astype(np.float32)
+    elif gamma_dtype == "f16":
+        gamma = g.astype(np.float16)
+    else:
+        raise ValueError(gamma_dtype)
+    return idx.astype(np.uint8), signs, gamma
+
+
+# ---------------------------------------------------------------------------
+# Scorer
+# ---------------------------------------------------------------------------
+
+def prepare_queries(Q: np.ndarray, Pi: np.ndarray, S_mat: np.ndarray):
+    """A_b = Π q_b and T_b = S_mat q_b for every query row ([RY] "Two kernels, two jobs").
+
+    A[b, d] = sum_j Π[d, j] q[b, j]; T[b, d] = sum_j S_mat[d, j] q[b, j].
+    """
+    q = np.asarray(Q, dtype=np.float64)
+    return q @ np.asarray(Pi, dtype=np.float64).T, q @ np.asarray(S_mat, dtype=np.float64).T
+
+
+def scores(A: np.ndarray, T: np.ndarray, idx: np.ndarray, signs: np.ndarray, gamma: np.ndarray,
+           codebook: np.ndarray) -> np.ndarray:
+    """Raw TurboQuant_prod scores from the transformed queries ([RY]; [ZT] Theorem 2).
+
+    score[b, s] = sum_d A[b,d] c[idx[s,d]] + sqrt(pi/2)/D * gamma[s] * sum_d T[b,d] sigma[s,d]
+
+    with no softmax, no value read and no 1/sqrt(D).  float64 throughout,
+    from the stored inputs widened exactly.
+    """
+    A = np.asarray(A, dtype=np.float64)
+    T = np.asarray(T, dtype=np.float64)
+    D = A.shape[1]
+    cvals = np.asarray(codebook, dtype=np.float64)[np.asarray(idx, dtype=np.int64)]
+    mse = A @ cvals.T
+    res = T @ np.asarray(signs, dtype=np.float64).T
+    return mse + kappa(D) * np.asarray(gamma, dtype=np.float64)[np.newaxis, :] * res
+
+
+def scores_from_queries(Q, Pi, S_mat, idx, signs, gamma, codebook) -> np.ndarray:
+    """Query transform followed by the scorer (the whole path, [RY] solve)."""
+    A, T = prepare_queries(Q, Pi, S_mat)
+    return scores(A, T, idx, signs, gamma, codebook)
+
+
+def scores_sampled(A, T, idx_rows, sign_rows, gamma_vals, codebook, b_index) -> np.ndarray:
+    """Scores of selected (query, key) pairs, one at a time.
+
+    ``idx_rows``/``sign_rows``/``gamma_vals`` hold the keys of the pairs and
+    ``b_index`` their query rows; used to check outputs of workloads too large
+    to score in full.
+    """
+    A = np.asarray(A, dtype=np.float64)
+    T = np.asarray(T, dtype=np.float64)
+    D = A.shape[1]
+    c = np.asarray(codebook, dtype=np.float64)
+    out = np.empty(len(b_index))
+    for n, b in enumerate(b_index):
+        mse = float(np.dot(A[b], c[np.asarray(idx_rows[n], dtype=np.int64)]))
+        res = float(np.dot(T[b], np.asarray(sign_rows[n], dtype=np.float64)))
+        out[n] = mse + kappa(D) * float(gamma_vals[n]) * res
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Bit packing (the library's storage format)
+# ---------------------------------------------------------------------------
+
+def pack_indices(idx: np.ndarray, bits: int) -> np.ndarray:
+    """Pack b-bit indices of each key into a little-endian bit stream.
+
+    Bit t of coordinate d is stream bit bits*d + t; stream bit i is bit
+    (i mod 8) of byte i // 8.  A key of D coordinates takes D*bits/8 bytes
+    (a 128-dim 2-bit key is 32 bytes, a 3-bit key 48 bytes: [KB] §8).
+    """
+    idx = np.asarray(idx, dtype=np.int64)
+    S, D = idx.shape
+    if (D * bits) % 8:
+        raise ValueError("D*bits must be a whole number of bytes")
+    stream = np.zeros((S, D * bits), dtype=np.uint8)
+    for t in range(bits):
+        stream[:, t::bits] = (idx >> t) & 1
+    return np.packbits(stream.reshape(S, -1, 8), axis=2, bitorder="little").reshape(S, -1)
+
+
+def unpack_indices(plane: np.ndarray, bits: int, D: int) -> np.ndarray:
+    """Inverse of :func:`pack_indices`."""
+    plane = np.asarray(plane, dtype=np.uint8)
+    S = plane.shape[0]
+    stream = np.unpackbits(plane, axis=1, bitorder="little")[:, :D * bits].astype(np.int64)
+    idx = np.zeros((S, D), dtype=np.int64)
+    for t in range(bits):
+        idx |= stream[:, t::bits] << t
+    return idx.astype(np.uint8)
+
+
+def pack_signs(signs: np.ndarray) -> np.ndarray:
+    """One bit per coordinate, little-endian: bit d is 1 exactly when sigma_d = +1."""
+    s = np.asarray(signs)
+    return np.packbits((s > 0).astype(np.uint8), axis=1, bitorder="little")
+
+
+def unpack_signs(plane: np.ndarray, D: int) -> np.ndarray:
+    """Inverse of :func:`pack_signs`: int8 +1 / -1."""
+    bits = np.unpackbits(np.asarray(plane, dtype=np.uint8), axis=1, bitorder="little")[:, :D]
+    return np.where(bits == 1, 1, -1).astype(np.int8)

@@ -1,0 +1,327 @@
+"""Pins for the CPU oracle: each check ties it to something other than itself.
+
+* the worked example printed on the riteshyadav.xyz page (intermediates and output);
+* brute-force key reconstruction followed by a plain dot product (pure Python loops);
+* closed forms and tables of the Lloyd-Max codebook from the kanthi.in chapter, the
+  exact 1-bit centroid from the Gamma function, and the centroid fixed point checked by
+  adaptive quadrature of the exact density;
+* the defining property of the sign-fixed QR rotation;
+* nearest-centroid / sign / norm properties of the compressor on brute force;
+* the unbiasedness of the estimator (zededa.com Theorem 2) and the slope table of the
+  kanthi.in chapter, section 6;
+* hand-worked bytes of the packed format.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from conftest import codebook, golden
+
+
+# ---------------------------------------------------------------------------
+# Scorer
+# ---------------------------------------------------------------------------
+
+def test_worked_example_matches_page():
+    g = golden("worked_example.json")
+    A, T = oracle.prepare_queries(np.array(g["Q"]), np.array(g["Pi"]), np.array(g["S_mat"]))
+    np.testing.assert_array_equal(A, np.array(g["A"]))
+    np.testing.assert_array_equal(T, np.array(g["T"]))
+    gamma = np.array(g["gamma"], dtype=np.float32)
+    out = oracle.scores(A, T, np.array(g["K_idx"], dtype=np.uint8), np.array(g["signs"], dtype=np.int8),
+                        gamma, np.array(g["codebook"], dtype=np.float32))
+    assert np.round(out, g["decimals"]).tolist() == g["scores"]
+    # the two parts the page spells out for token 0 and token 1
+    no_corr = oracle.scores(A, T, np.array(g["K_idx"], dtype=np.uint8), np.array(g["signs"], dtype=np.int8),
+                            np.zeros(2, dtype=np.float32), np.array(g["codebook"], dtype=np.float32))
+    np.testing.assert_allclose(no_corr, g["centroid_score"], rtol=0, atol=1e-15)
+    corr0 = out[0, 0] - no_corr[0, 0]
+    assert round(corr0, 6) == g["correction_token0"]
+    assert corr0 / (oracle.kappa(2) * float(gamma[0])) == pytest.approx(g["residual_dot"][0][0], rel=1e-12)
+
+
+def _bruteforce_scores(Q, Pi, Smat, idx, signs, gamma, cb):
+    """Reconstruct every key as Pi^T c[idx] + sqrt(pi/2)/D * gamma * S_mat^T sigma and dot it
+    with the query, all in plain Python floats (kanthi.in §3, TurboQuantProd.dequantize)."""
+    B, D = len(Q), len(Q[0])
+    S = len(idx)
+    k = math.sqrt(math.pi / 2.0) / D
+    out = [[0.0] * S for _ in range(B)]
+    for s in range(S):
+        key = [0.0] * D
+        for j in range(D):
+            acc = 0.0
+            for d in range(D):
+                acc += float(Pi[d][j]) * float(cb[int(idx[s][d])])
+                acc += k * float(gamma[s]) * float(Smat[d][j]) * float(signs[s][d])
+            key[j] = acc
+        for b in range(B):
+            out[b][s] = sum(float(Q[b][j]) * key[j] for j in range(D))
+    return np.array(out)
+
+
+@pytest.mark.parametrize("D,C,B,S", [(2, 4, 1, 3), (4, 2, 2, 5), (8, 8, 3, 16), (5, 16, 2, 7)])
+def test_scores_equal_bruteforce_reconstruction(D, C, B, S):
+    rng = np.random.default_rng(100 + D * 7 + C)
+    Pi = rng.standard_normal((D, D)).astype(np.float32)      # deliberately not orthogonal or symmetric
+    Smat = rng.standard_normal((D, D)).astype(np.float32)
+    cb = np.sort(rng.standard_normal(C)).astype(np.float32)
+    Q = rng.standard_normal((B, D)).astype(np.float32)
+    idx = rng.integers(0, C, (S, D)).astype(np.uint8)
+    signs = np.where(rng.random((S, D)) < 0.5, 1, -1).astype(np.int8)
+    gamma = rng.random(S).astype(np.float32)
+    got = oracle.scores_from_queries(Q, Pi, Smat, idx, signs, gamma, cb)
+    want = _bruteforce_scores(Q, Pi, Smat, idx, signs, gamma, cb)
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
+    # gamma = 0: the rotated-domain identity <Pi q, c[idx]> = <q, Pi^T c[idx]> (kanthi.in §8)
+    got0 = oracle.scores_from_queries(Q, Pi, Smat, idx, signs, np.zeros(S, np.float32), cb)
+    want0 = _bruteforce_scores(Q, Pi, Smat, idx, signs, np.zeros(S), cb)
+    np.testing.assert_allclose(got0, want0, rtol=1e-12, atol=1e-12)
+    # sampled one-by-one scorer agrees with the full scorer
+    A, T = oracle.prepare_queries(Q, Pi, Smat)
+    bs = np.arange(B).repeat(S)
+    ss = np.tile(np.arange(S), B)
+    one = oracle.scores_sampled(A, T, idx[ss], signs[ss], gamma[ss], cb, bs)
+    np.testing.assert_allclose(one, got[bs, ss], rtol=1e-13, atol=1e-13)
+
+
+def test_exact_binary_case():
+    """Pi = S_mat = I, integer codebook, kappa*gamma = 1/8: every term is exact in binary."""
+    D = 4
+    gamma = np.float32(0.125 / oracle.kappa(D))       # kappa*gamma rounds back to 1/8 within 1e-8
+    cb = np.array([-3.0, -1.0, 1.0, 3.0], dtype=np.float32)
+    Q = np.array([[1.0, 2.0, -4.0, 8.0]], dtype=np.float32)
+    idx = np.array([[0, 1, 2, 3]], dtype=np.uint8)
+    sg = np.array([[1, -1, -1, 1]], dtype=np.int8)
+    out = oracle.scores_from_queries(Q, np.eye(D), np.eye(D), idx, sg, np.array([gamma]), cb)
+    # centroid part: 1*-3 + 2*-1 + -4*1 + 8*3 = 15 ; sign part: 1 - 2 + 4 + 8 = 11 ; 15 + 11/8
+    assert out[0, 0] == pytest.approx(15.0 + 11.0 / 8.0, abs=1e-6)
+
+
+# ---------------------------------------------------------------------------
+# Codebook
+# ---------------------------------------------------------------------------
+
+def test_codebook_matches_printed_table():
+    g = golden("codebook_d128.json")
+    d = g["d"]
+    for b, vals in g["centroids_times_sqrt_d"].items():
+        c, _, _ = codebook(d, int(b))
+        np.testing.assert_allclose(c * math.sqrt(d), vals, atol=0.5 * 10 ** -g["centroid_decimals"] + 1e-4)
+    for b, dm in g["d_mse"].items():
+        _, _, got = codebook(d, int(b))
+        assert abs(got - dm) <= 0.5 * 10 ** -g["d_mse_decimals"] + 1e-6, (b, got, dm)
+        lo, hi = 4.0 ** -int(b), math.sqrt(3) * math.pi / 2 * 4.0 ** -int(b)
+        assert lo < got < hi
+
+
+def test_codebook_gaussian_closed_forms():
+    g = golden("codebook_d128.json")["gaussian_closed_forms"]
+    d = 128
+    c1, _, _ = codebook(d, 1)
+    c2, _, _ = codebook(d, 2)
+    tol = g["abs_tolerance_times_sqrt_d"]
+    assert abs(c1[1] * math.sqrt(d) - g["1"][0]) < tol
+    np.testing.assert_allclose(np.abs(c2[2:]) * math.sqrt(d), g["2"], atol=tol)
+
+
+def test_one_bit_codebook_exact_closed_form():
+    """1 bit: the cell edge is 0 and each centroid is E|x| = Gamma(d/2) / (sqrt(pi) Gamma((d+1)/2));
+    the distortion is 1 - d c^2 because E[x^2] = 1/d on the sphere."""
+    for d in (16, 64, 128):
+        c, edges, dm = codebook(d, 1) if d == 128 else oracle.lloyd_max_sphere(d, 1, iters=60)
+        exact = math.exp(math.lgamma(d / 2) - math.lgamma((d + 1) / 2)) / math.sqrt(math.pi)
+        np.testing.assert_allclose([-c[0], c[1]], [exact, exact], rtol=1e-4)
+        # the grid point at exactly 0 joins the lower cell (left-sided search), so the
+        # edge can sit off 0 by at most about one grid step 2/(grid-1)
+        assert abs(edges[0]) < 2.0 / 400_000
+        assert dm == pytest.approx(1.0 - d * exact * exact, rel=2e-4)
+
+
+def test_codebook_is_a_lloyd_fixed_point_under_quadrature():
+    """Each centroid is the conditional mean of its cell under the exact density, checked with
+    adaptive quadrature (scipy) instead of the grid the oracle sums over."""
+    integrate = pytest.importorskip("scipy.integrate")
+    d = 128
+    for b in (2, 3):
+        c, edges, _ = codebook(d, b)
+        f = lambda x: (1.0 - x * x) ** ((d - 3) / 2.0)
+        lims = [-1.0] + list(edges) + [1.0]
+        for k in range(len(c)):
+            mass = integrate.quad(f, lims[k], lims[k + 1], epsabs=0, epsrel=1e-12, limit=200)[0]
+            mom = integrate.quad(lambda x: x * f(x), lims[k], lims[k + 1], epsabs=0, epsrel=1e-12, limit=200)[0]
+            # 300 Lloyd rounds leave ~3e-5 relative; a wrong density exponent moves centroids ~1e-2
+            assert c[k] == pytest.approx(mom / mass, rel=1e-4)
+        # symmetry of a symmetric density: c_k = -c_{C-1-k}
+        np.testing.assert_allclose(c, -c[::-1], atol=1e-5)
+
+
+# ---------------------------------------------------------------------------
+# Rotation
+# ---------------------------------------------------------------------------
+
+def test_haar_rotation_is_sign_fixed_qr_factor():
+    for D in (2, 7, 128):
+        G = synth.rotation_seed_matrix(5, 0, D)
+        Pi = oracle.haar_rotation(G)
+        assert np.abs(Pi @ Pi.T - np.eye(D)).max() < 1e-12
+        R = Pi.T @ G                       # G = Pi R with R upper triangular, positive diagonal
+        assert np.abs(np.tril(R, -1)).max() < 1e-11 * max(1.0, np.abs(R).max())
+        assert (np.diag(R) > 0).all()
+
+
+def test_haar_rotation_second_moment():
+    """Entries of a Haar matrix have E[Pi_ij^2] = 1/D."""
+    D = 16
+    acc = np.zeros((D, D))
+    n = 400
+    for seed in range(n):
+        acc += oracle.haar_rotation(np.random.default_rng(seed).standard_normal((D, D))) ** 2
+    assert np.abs(acc / n - 1.0 / D).max() < 6 * math.sqrt(2.0 / n) / D
+
+
+# ---------------------------------------------------------------------------
+# Compressor
+# ---------------------------------------------------------------------------
+
+def test_compressor_bruteforce_properties():
+    D, S = 16, 64
+    rng = np.random.default_rng(3)
+    keys = rng.standard_normal((S, D))
+    keys /= np.linalg.norm(keys, axis=1, keepdims=True)
+    Pi = oracle.haar_rotation(rng.standard_normal((D, D))).astype(np.float32)
+    Smat = rng.standard_normal((D, D)).astype(np.float32)
+    cb = (oracle.lloyd_max_sphere(D, 2, iters=60)[0]).astype(np.float32)
+    idx, sg, gamma = oracle.compress_prod(keys, Pi, Smat, cb, "f32")
+    P64, S64, c64 = Pi.astype(float), Smat.astype(float), cb.astype(float)
+    for s in range(S):
+        r = keys[s].copy()
+        for d in range(D):
+            y = sum(P64[d][j] * keys[s][j] for j in range(D))
+            dist = [abs(y - c64[k]) for k in range(len(cb))]
+            assert idx[s][d] == min(range(len(cb)), key=lambda k: (dist[k], k))
+            for j in range(D):
+                r[j] -= P64[d][j] * c64[idx[s][d]]
+        for d in range(D):
+            z = sum(S64[d][j] * r[j] for j in range(D))
+            assert sg[s][d] == (1 if z >= 0 else -1)
+        assert float(gamma[s]) == pytest.approx(math.sqrt(sum(v * v for v in r)), rel=1e-7)
+
+
+def test_compressor_ties_and_zero_sign():
+    """A coordinate on a cell edge takes the lower index; sign(0) is +1."""
+    D = 4
+    cb = np.array([-3.0, -1.0, 1.0, 3.0], dtype=np.float32) / 8   # edges -0.25, 0, 0.25
+    key = np.array([[0.0, 0.25, -0.25, math.sqrt(1 - 2 * 0.0625)]])
+    Smat = np.zeros((D, D), dtype=np.float32)
+    Smat[1, 0] = 1.0
+    idx, sg, gamma = oracle.compress_prod(key, np.eye(D, dtype=np.float32), Smat, cb, "f16")
+    assert idx[0].tolist() == [1, 2, 0, 3]
+    r0 = key[0, 0] - cb[1]
+    assert sg[0].tolist() == [1, 1 if r0 >= 0 else -1, 1, 1]
+    assert gamma.dtype == np.float16
+
+
+def _prod_estimates(mse_bits, n, seed, D=128):
+    """The kanthi.in §6 Part 1 protocol: unit keys, correlated unit queries, estimate <q, k>."""
+    rng = np.random.default_rng(seed)
+    k = rng.standard_normal((n, D))
+    k /= np.linalg.norm(k, axis=1, keepdims=True)
+    q = k + 0.6 * rng.standard_normal((n, D)) / math.sqrt(D)
+    q /= np.linalg.norm(q, axis=1, keepdims=True)
+    Pi = oracle.haar_rotation(rng.standard_normal((D, D))).astype(np.float32)
+    Smat = rng.standard_normal((D, D)).astype(np.float32)
+    cb = codebook(D, mse_bits)[0].astype(np.float32)
+    idx, sg, gamma = oracle.compress_prod(k, Pi, Smat, cb, "f32")
+    A, T = oracle.prepare_queries(q, Pi, Smat)
+    rows = np.arange(n)
+    est = oracle.scores_sampled(A, T, idx, sg, gamma, cb, rows)
+    return np.sum(q * k, axis=1), est
+
+
+def test_slope_table_of_mse_plus_qjl():
+    g = golden("prod_slope.json")
+    for name, row in g["rows"].items():
+        true, est = _prod_estimates(row["mse_bits"], 512, seed=11 + row["mse_bits"])
+        slope = float(est @ true / (true @ true))
+        resid = est - slope * true
+        se = float(np.std(resid) / math.sqrt(true @ true))
+        assert abs(slope - 1.0) < 5 * se + 1e-3, (name, slope, se)
+        assert abs(slope - row["slope"]) < 5 * se + 2e-3, (name, slope)
+        assert np.std(resid) == pytest.approx(row["resid_std"], rel=0.25), name
+        # zededa.com Theorem 3: no inner-product quantizer beats 1/(d 4^b) for unit queries
+        b_total = row["mse_bits"] + 1
+        assert np.mean((est - true) ** 2) > 1.0 / (128 * 4 ** b_total)
+
+
+def test_estimator_is_unbiased_over_rotations():
+    """zededa.com Theorem 2: E[<y, x~>] = <y, x> over the random rotation and projection.
+    Without the QJL term the estimate is visibly biased, so the test can fail."""
+    D, n_keys, reps = 128, 8, 96
+    rng = np.random.default_rng(21)
+    k = rng.standard_normal((n_keys, D))
+    k /= np.linalg.norm(k, axis=1, keepdims=True)
+    q = k + 0.6 * rng.standard_normal((n_keys, D)) / math.sqrt(D)
+    true = np.sum(q * k, axis=1)
+    cb = codebook(D, 2)[0].astype(np.float32)
+    err, err_mse_only = [], []
+    for rep in range(reps):
+        r2 = np.random.default_rng(1000 + rep)
+        Pi = oracle.haar_rotation(r2.standard_normal((D, D))).astype(np.float32)
+        Smat = r2.standard_normal((D, D)).astype(np.float32)
+        idx, sg, gamma = oracle.compress_prod(k, Pi, Smat, cb, "f32")
+        A, T = oracle.prepare_queries(q, Pi, Smat)
+        rows = np.arange(n_keys)
+        err.append(oracle.scores_sampled(A, T, idx, sg, gamma, cb, rows) - true)
+        err_mse_only.append(oracle.scores_sampled(A, T, idx, sg, np.zeros(n_keys), cb, rows) - true)
+    err = np.array(err)
+    mean, se = err.mean(), err.std() / math.sqrt(err.size)
+    assert abs(mean) < 4 * se, (mean, se)
+    e2 = np.array(err_mse_only)
+    assert abs(e2.mean()) > 4 * e2.std() / math.sqrt(e2.size)
+
+
+# ---------------------------------------------------------------------------
+# Packer
+# ---------------------------------------------------------------------------
+
+def test_pack_hand_worked_bytes():
+    for case in golden("pack_bytes.json")["cases"]:
+        if case["kind"] == "indices":
+            idx = np.array([case["idx"]], dtype=np.uint8)
+            plane = oracle.pack_indices(idx, case["bits"])
+            assert plane[0].tolist() == case["bytes"]
+            np.testing.assert_array_equal(oracle.unpack_indices(plane, case["bits"], case["D"]), idx)
+        else:
+            sg = -np.ones((1, case["D"]), dtype=np.int8)
+            sg[0, case["plus_at"]] = 1
+            plane = oracle.pack_signs(sg)
+            assert plane[0].tolist() == case["bytes"]
+            np.testing.assert_array_equal(oracle.unpack_signs(plane, case["D"]), sg)
+
+
+@pytest.mark.parametrize("bits", [1, 2, 3])
+@pytest.mark.parametrize("D", [32, 64, 96, 128, 256])
+def test_pack_round_trip(bits, D):
+    rng = np.random.default_rng(bits * 1000 + D)
+    idx = rng.integers(0, 1 << bits, (37, D)).astype(np.uint8)
+    plane = oracle.pack_indices(idx, bits)
+    assert plane.shape == (37, D * bits // 8)
+    np.testing.assert_array_equal(oracle.unpack_indices(plane, bits, D), idx)
+    sg = np.where(rng.random((37, D)) < 0.5, 1, -1).astype(np.int8)
+    sp = oracle.pack_signs(sg)
+    assert sp.shape == (37, D // 8)
+    np.testing.assert_array_equal(oracle.unpack_signs(sp, D), sg)
+
+
+def test_synth_keys_are_unit_and_reproducible():
+    a = synth.unit_keys(7, 0, 4090, 20, 128)
+    b = synth.unit_keys(7, 0, 4000, 200, 128)[90:110]
+    np.testing.assert_array_equal(a, b)
+    np.testing.assert_allclose(np.linalg.norm(a, axis=1), 1.0, atol=1e-14)
+    q, raw = synth.queries(7, 0, 4, 128, "bf16")
+    assert raw.dtype == np.uint16
+    assert np.abs(q - synth.queries(7, 0, 4, 128, "f32")[0]).max() <= 2.0 ** -8 * np.abs(q).max()

@@ -1,0 +1,237 @@
+// C ABI of libtq (declared in include/tq.h): argument validation and dispatch.
+// Every check runs on the host before any CUDA call, so an invalid call
+// returns its status without touching the device.
+#include <climits>
+
+#include "tq_internal.cuh"
+
+namespace {
+
+constexpr int kMaxGridYZ = 65535;
+
+bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+
+template <typename... Ptrs>
+tq_status check_ptrs(Ptrs... ptrs) {
+  const void* all[] = {static_cast<const void*>(ptrs)...};
+  for (const void* p : all)
+    if (p == nullptr) return TQ_ERR_INVALID_VALUE;
+  for (const void* p : all)
+    if (misaligned(p)) return TQ_ERR_MISALIGNED;
+  return TQ_OK;
+}
+
+tq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? TQ_OK : TQ_ERR_LAUNCH; }
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+size_t at_bytes(int P, int B, int D) {
+  return round_up(static_cast<size_t>(P) * B * D * sizeof(float), 256);
+}
+
+tq_status check_prepare_sizes(int P, int H, int B, int D, tq_qtype qtype) {
+  if (P < 1 || H < 1 || H > P || B < 1 || D < 1 || D > 256) return TQ_ERR_INVALID_VALUE;
+  if (P > kMaxGridYZ || (B + 7) / 8 > kMaxGridYZ) return TQ_ERR_INVALID_VALUE;
+  if (qtype != TQ_Q_F32 && qtype != TQ_Q_BF16) return TQ_ERR_INVALID_VALUE;
+  return TQ_OK;
+}
+
+tq_status check_score_sizes(int P, int B, int S, int D) {
+  if (P < 1 || B < 1 || S < 1 || D < 1 || D > 256) return TQ_ERR_INVALID_VALUE;
+  if (P > kMaxGridYZ || B > kMaxGridYZ || S > INT_MAX - 1024) return TQ_ERR_INVALID_VALUE;
+  return TQ_OK;
+}
+
+// Resolves AUTO and checks that the requested path exists for this shape.
+tq_status resolve_path(tq_path path, int B, int D, tq_path* out) {
+  if (path != TQ_PATH_AUTO && path != TQ_PATH_FP32 && path != TQ_PATH_BF16_MMA)
+    return TQ_ERR_INVALID_VALUE;
+  if (path == TQ_PATH_AUTO) path = tq_auto_path(B, D);
+  if (path == TQ_PATH_BF16_MMA && (D != 128 || !tq::mma_path_available()))
+    return TQ_ERR_UNSUPPORTED;
+  *out = path;
+  return TQ_OK;
+}
+
+tq_status check_unpacked(const float* A, const float* T, const uint8_t* K_idx, const int8_t* signs,
+                         const float* gamma, const float* codebook, float* scores, int P, int B,
+                         int S, int D, int C, tq_path path, tq_path* resolved) {
+  tq_status st = check_ptrs(A, T, K_idx, signs, gamma, codebook, scores);
+  if (st != TQ_OK) return st;
+  if ((st = check_score_sizes(P, B, S, D)) != TQ_OK) return st;
+  if (C < 1 || C > 256) return TQ_ERR_INVALID_VALUE;
+  return resolve_path(path, B, D, resolved);
+}
+
+tq_status check_packed(const float* A, const float* T, const uint8_t* idx_plane,
+                       const uint8_t* sign_plane, const uint16_t* gamma_f16,
+                       const float* codebook, float* scores, int P, int B, int S, int D,
+                       int idx_bits, tq_path path, tq_path* resolved) {
+  tq_status st = check_ptrs(A, T, idx_plane, sign_plane, gamma_f16, codebook, scores);
+  if (st != TQ_OK) return st;
+  if ((st = check_score_sizes(P, B, S, D)) != TQ_OK) return st;
+  if (idx_bits < 1 || idx_bits > 3) return TQ_ERR_INVALID_VALUE;
+  if (D % 32 != 0) return TQ_ERR_UNSUPPORTED;
+  return resolve_path(path, B, D, resolved);
+}
+
+tq_status run_unpacked(const float* A, const float* T, const uint8_t* K_idx, const int8_t* signs,
+                       const float* gamma, const float* codebook, float* scores, int P, int B,
+                       int S, int D, int C, tq_path path, cudaStream_t stream) {
+  if (path == TQ_PATH_BF16_MMA)
+    return from_cuda(tq::launch_scores_mma(A, T, K_idx, signs, gamma, codebook, scores, P, B, S,
+                                           C, 0, false, stream));
+  return from_cuda(tq::launch_scores_unpacked_fp32(A, T, K_idx, signs, gamma, codebook, scores,
+                                                   P, B, S, D, C, stream));
+}
+
+tq_status run_packed(const float* A, const float* T, const uint8_t* idx_plane,
+                     const uint8_t* sign_plane, const uint16_t* gamma_f16, const float* codebook,
+                     float* scores, int P, int B, int S, int D, int idx_bits, tq_path path,
+                     cudaStream_t stream) {
+  if (path == TQ_PATH_BF16_MMA)
+    return from_cuda(tq::launch_scores_mma(A, T, idx_plane, sign_plane, gamma_f16, codebook,
+                                           scores, P, B, S, 1 << idx_bits, idx_bits, true,
+                                           stream));
+  return from_cuda(tq::launch_scores_packed_fp32(A, T, idx_plane, sign_plane, gamma_f16, codebook,
+                                                 scores, P, B, S, D, idx_bits, stream));
+}
+
+tq_status check_pack_sizes(int64_t n_keys, int D, int bits) {
+  if (n_keys < 1 || D < 8 || D > 4096 || D % 8 != 0 || bits < 1 || bits > 8)
+    return TQ_ERR_INVALID_VALUE;
+  if (n_keys > (static_cast<int64_t>(1) << 40) / D) return TQ_ERR_INVALID_VALUE;
+  return TQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* tq_status_string(tq_status status) {
+  switch (status) {
+    case TQ_OK: return "TQ_OK";
+    case TQ_ERR_INVALID_VALUE: return "TQ_ERR_INVALID_VALUE: null pointer or size out of range";
+    case TQ_ERR_UNSUPPORTED: return "TQ_ERR_UNSUPPORTED: no kernel implements this combination";
+    case TQ_ERR_MISALIGNED: return "TQ_ERR_MISALIGNED: an array pointer is not 16-byte aligned";
+    case TQ_ERR_WORKSPACE: return "TQ_ERR_WORKSPACE: workspace null or too small";
+    case TQ_ERR_LAUNCH: return "TQ_ERR_LAUNCH: CUDA reported a launch error";
+  }
+  return "unknown tq_status";
+}
+
+tq_path tq_auto_path(int B, int D) {
+  return (B >= 16 && D == 128 && tq::mma_path_available()) ? TQ_PATH_BF16_MMA : TQ_PATH_FP32;
+}
+
+tq_status tq_prepare_queries(const void* Q, tq_qtype qtype, const float* Pi, const float* S_mat,
+                             float* A, float* T, int P, int H, int B, int D,
+                             cudaStream_t stream) {
+  tq_status st = check_ptrs(Q, Pi, S_mat, A, T);
+  if (st != TQ_OK) return st;
+  if ((st = check_prepare_sizes(P, H, B, D, qtype)) != TQ_OK) return st;
+  return from_cuda(tq::launch_prepare(Q, qtype, Pi, S_mat, A, T, P, H, B, D, stream));
+}
+
+tq_status tq_scores(const float* A, const float* T, const uint8_t* K_idx, const int8_t* signs,
+                    const float* gamma, const float* codebook, float* scores, int P, int B, int S,
+                    int D, int C, tq_path path, cudaStream_t stream) {
+  tq_path p;
+  tq_status st = check_unpacked(A, T, K_idx, signs, gamma, codebook, scores, P, B, S, D, C, path, &p);
+  if (st != TQ_OK) return st;
+  return run_unpacked(A, T, K_idx, signs, gamma, codebook, scores, P, B, S, D, C, p, stream);
+}
+
+tq_status tq_scores_packed(const float* A, const float* T, const uint8_t* idx_plane,
+                           const uint8_t* sign_plane, const uint16_t* gamma_f16,
+                           const float* codebook, float* scores, int P, int B, int S, int D,
+                           int idx_bits, tq_path path, cudaStream_t stream) {
+  tq_path p;
+  tq_status st = check_packed(A, T, idx_plane, sign_plane, gamma_f16, codebook, scores, P, B, S, D,
+                              idx_bits, path, &p);
+  if (st != TQ_OK) return st;
+  return run_packed(A, T, idx_plane, sign_plane, gamma_f16, codebook, scores, P, B, S, D, idx_bits,
+                    p, stream);
+}
+
+size_t tq_workspace_bytes(int P, int B, int D) {
+  if (P < 1 || B < 1 || D < 1) return 0;
+  return 2 * at_bytes(P, B, D);
+}
+
+tq_status tq_solve(const void* Q, tq_qtype qtype, const uint8_t* K_idx, const int8_t* signs,
+                   const float* gamma, const float* Pi, const float* S_mat, const float* codebook,
+                   float* scores, int P, int H, int B, int S, int D, int C, void* workspace,
+                   size_t workspace_bytes, tq_path path, cudaStream_t stream) {
+  tq_status st = check_ptrs(Q, Pi, S_mat);
+  if (st != TQ_OK) return st;
+  if ((st = check_prepare_sizes(P, H, B, D, qtype)) != TQ_OK) return st;
+  if (workspace == nullptr) return TQ_ERR_WORKSPACE;
+  if (misaligned(workspace)) return TQ_ERR_MISALIGNED;
+  if (workspace_bytes < tq_workspace_bytes(P, B, D)) return TQ_ERR_WORKSPACE;
+  float* A = static_cast<float*>(workspace);
+  float* T = reinterpret_cast<float*>(static_cast<char*>(workspace) + at_bytes(P, B, D));
+  tq_path p;
+  if ((st = check_unpacked(A, T, K_idx, signs, gamma, codebook, scores, P, B, S, D, C, path, &p)) != TQ_OK)
+    return st;
+  if ((st = from_cuda(tq::launch_prepare(Q, qtype, Pi, S_mat, A, T, P, H, B, D, stream))) != TQ_OK)
+    return st;
+  return run_unpacked(A, T, K_idx, signs, gamma, codebook, scores, P, B, S, D, C, p, stream);
+}
+
+tq_status tq_solve_packed(const void* Q, tq_qtype qtype, const uint8_t* idx_plane,
+                          const uint8_t* sign_plane, const uint16_t* gamma_f16, const float* Pi,
+                          const float* S_mat, const float* codebook, float* scores, int P, int H,
+                          int B, int S, int D, int idx_bits, void* workspace,
+                          size_t workspace_bytes, tq_path path, cudaStream_t stream) {
+  tq_status st = check_ptrs(Q, Pi, S_mat);
+  if (st != TQ_OK) return st;
+  if ((st = check_prepare_sizes(P, H, B, D, qtype)) != TQ_OK) return st;
+  if (workspace == nullptr) return TQ_ERR_WORKSPACE;
+  if (misaligned(workspace)) return TQ_ERR_MISALIGNED;
+  if (workspace_bytes < tq_workspace_bytes(P, B, D)) return TQ_ERR_WORKSPACE;
+  float* A = static_cast<float*>(workspace);
+  float* T = reinterpret_cast<float*>(static_cast<char*>(workspace) + at_bytes(P, B, D));
+  tq_path p;
+  if ((st = check_packed(A, T, idx_plane, sign_plane, gamma_f16, codebook, scores, P, B, S, D,
+                         idx_bits, path, &p)) != TQ_OK)
+    return st;
+  if ((st = from_cuda(tq::launch_prepare(Q, qtype, Pi, S_mat, A, T, P, H, B, D, stream))) != TQ_OK)
+    return st;
+  return run_packed(A, T, idx_plane, sign_plane, gamma_f16, codebook, scores, P, B, S, D, idx_bits,
+                    p, stream);
+}
+
+tq_status tq_pack_indices(const uint8_t* K_idx, uint8_t* idx_plane, int64_t n_keys, int D,
+                          int bits, cudaStream_t stream) {
+  tq_status st = check_ptrs(K_idx, idx_plane);
+  if (st != TQ_OK) return st;
+  if ((st = check_pack_sizes(n_keys, D, bits)) != TQ_OK) return st;
+  return from_cuda(tq::launch_pack_indices(K_idx, idx_plane, n_keys, D, bits, stream));
+}
+
+tq_status tq_unpack_indices(const uint8_t* idx_plane, uint8_t* K_idx, int64_t n_keys, int D,
+                            int bits, cudaStream_t stream) {
+  tq_status st = check_ptrs(idx_plane, K_idx);
+  if (st != TQ_OK) return st;
+  if ((st = check_pack_sizes(n_keys, D, bits)) != TQ_OK) return st;
+  return from_cuda(tq::launch_unpack_indices(idx_plane, K_idx, n_keys, D, bits, stream));
+}
+
+tq_status tq_pack_signs(const int8_t* signs, uint8_t* sign_plane, int64_t n_keys, int D,
+                        cudaStream_t stream) {
+  tq_status st = check_ptrs(signs, sign_plane);
+  if (st != TQ_OK) return st;
+  if ((st = check_pack_sizes(n_keys, D, 1)) != TQ_OK) return st;
+  return from_cuda(tq::launch_pack_signs(signs, sign_plane, n_keys, D, stream));
+}
+
+tq_status tq_unpack_signs(const uint8_t* sign_plane, int8_t* signs, int64_t n_keys, int D,
+                          cudaStream_t stream) {
+  tq_status st = check_ptrs(sign_plane, signs);
+  if (st != TQ_OK) return st;
+  if ((st = check_pack_sizes(n_keys, D, 1)) != TQ_OK) return st;
+  return from_cuda(tq::launch_unpack_signs(sign_plane, signs, n_keys, D, stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,53 @@
+// Internal declarations shared by the libtq translation units (not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "tq.h"
+
+namespace tq {
+
+// sqrt(pi/2) rounded to float32: the QJL scale numerator of the TurboQuant_prod
+// estimator (kanthi.in §3, TurboQuantProd.dequantize; riteshyadav.xyz epilogue).
+constexpr float kSqrtHalfPi = 1.25331413731550025f;
+
+inline float qjl_scale(int D) { return kSqrtHalfPi / static_cast<float>(D); }
+
+// ---- launchers (return the CUDA error of the launch, cudaSuccess otherwise) ----
+
+cudaError_t launch_prepare(const void* Q, tq_qtype qtype, const float* Pi, const float* S_mat,
+                           float* A, float* T, int P, int H, int B, int D, cudaStream_t st);
+
+cudaError_t launch_scores_unpacked_fp32(const float* A, const float* T, const uint8_t* K_idx,
+                                        const int8_t* signs, const float* gamma,
+                                        const float* codebook, float* scores, int P, int B,
+                                        int S, int D, int C, cudaStream_t st);
+
+cudaError_t launch_scores_packed_fp32(const float* A, const float* T, const uint8_t* idx_plane,
+                                      const uint8_t* sign_plane, const uint16_t* gamma_f16,
+                                      const float* codebook, float* scores, int P, int B, int S,
+                                      int D, int idx_bits, cudaStream_t st);
+
+// bf16 tensor-core path (D == 128). `packed` selects the cache layout; for the
+// unpacked layout idx_bits is ignored and C is the codebook size.
+bool mma_path_available();
+cudaError_t launch_scores_mma(const float* A, const float* T, const uint8_t* idx,
+                              const void* signs, const void* gamma, const float* codebook,
+                              float* scores, int P, int B, int S, int C, int idx_bits,
+                              bool packed, cudaStream_t st);
+
+cudaError_t launch_pack_indices(const uint8_t* K_idx, uint8_t* plane, int64_t n, int D, int bits,
+                                cudaStream_t st);
+cudaError_t launch_unpack_indices(const uint8_t* plane, uint8_t* K_idx, int64_t n, int D,
+                                  int bits, cudaStream_t st);
+cudaError_t launch_pack_signs(const int8_t* signs, uint8_t* plane, int64_t n, int D,
+                              cudaStream_t st);
+cudaError_t launch_unpack_signs(const uint8_t* plane, int8_t* signs, int64_t n, int D,
+                                cudaStream_t st);
+
+inline int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
+
+}  // namespace tq

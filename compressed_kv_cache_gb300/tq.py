@@ -1,0 +1,259 @@
+"""Thin Python binding of libtq (argument marshalling only).
+
+Every function takes torch tensors that already live on a CUDA device, checks
+their dtype, device, contiguity and shape, and passes raw device pointers and
+the current CUDA stream to the C ABI declared in ``include/tq.h``.  All work
+runs in libtq's kernels; there is no CPU fallback.  A missing libtq.so, a
+tensor on the CPU, or a non-OK status raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libtq.so")
+HEADER = os.path.join(os.path.dirname(_HERE), "include", "tq.h")
+
+TQ_OK = 0
+STATUS_NAMES = {0: "TQ_OK", 1: "TQ_ERR_INVALID_VALUE", 2: "TQ_ERR_UNSUPPORTED",
+                3: "TQ_ERR_MISALIGNED", 4: "TQ_ERR_WORKSPACE", 5: "TQ_ERR_LAUNCH"}
+QTYPE = {torch.float32: 0, torch.bfloat16: 1}
+PATHS = {"auto": 0, "fp32": 1, "bf16_mma": 2}
+PATH_NAMES = {v: k for k, v in PATHS.items()}
+
+_lib = None
+
+
+class TQError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} returned {status_string(status)}")
+
+
+_P, _I, _L, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+_SIGNATURES = {
+    "tq_status_string": ([_I], ctypes.c_char_p),
+    "tq_auto_path": ([_I, _I], _I),
+    "tq_prepare_queries": ([_P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _P], _I),
+    "tq_scores": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P], _I),
+    "tq_scores_packed": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P], _I),
+    "tq_workspace_bytes": ([_I, _I, _I], _Z),
+    "tq_solve": ([_P, _I, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _Z, _I, _P], _I),
+    "tq_solve_packed": ([_P, _I, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _Z, _I, _P], _I),
+    "tq_pack_indices": ([_P, _P, _L, _I, _I, _P], _I),
+    "tq_unpack_indices": ([_P, _P, _L, _I, _I, _P], _I),
+    "tq_pack_signs": ([_P, _P, _L, _I, _P], _I),
+    "tq_unpack_signs": ([_P, _P, _L, _I, _P], _I),
+}
+
+
+def lib() -> ctypes.CDLL:
+    """Loads libtq.so once; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: build it with compressed_kv_cache_gb300.build.build()")
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, (args, res) in _SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = handle
+    return _lib
+
+
+def declared_functions() -> list[str]:
+    """Names of the functions include/tq.h declares."""
+    with open(HEADER) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(tq_[a-z0-9_]+)\s*\(",
+                                 text, flags=re.M)))
+
+
+def status_string(status: int) -> str:
+    return lib().tq_status_string(status).decode()
+
+
+def auto_path(B: int, D: int) -> str:
+    return PATH_NAMES[lib().tq_auto_path(B, D)]
+
+
+def _check(fn: str, status: int) -> None:
+    if status != TQ_OK:
+        raise TQError(fn, status)
+
+
+def _stream() -> int:
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _dev(t: torch.Tensor, name: str, dtypes) -> int:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (libtq has no CPU path)")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _as3(t: torch.Tensor) -> tuple[int, int, int]:
+    if t.dim() == 2:
+        return 1, t.shape[0], t.shape[1]
+    if t.dim() == 3:
+        return t.shape[0], t.shape[1], t.shape[2]
+    raise ValueError(f"expected a [B,D] or [P,B,D] tensor, got shape {tuple(t.shape)}")
+
+
+def prepare_queries(Q, Pi, S_mat, out=None):
+    """A = Pi q and T = S_mat q.  Q [P,B,D] (or [B,D]) fp32/bf16; Pi, S_mat [H,D,D] (or [D,D])."""
+    P, B, D = _as3(Q)
+    H = 1 if Pi.dim() == 2 else Pi.shape[0]
+    if tuple(Pi.shape[-2:]) != (D, D) or Pi.shape != S_mat.shape:
+        raise ValueError("Pi and S_mat must be [H,D,D] or [D,D]")
+    A, T = out if out is not None else (torch.empty((P, B, D), device=Q.device, dtype=torch.float32),
+                                         torch.empty((P, B, D), device=Q.device, dtype=torch.float32))
+    _check("tq_prepare_queries", lib().tq_prepare_queries(
+        _dev(Q, "Q", QTYPE), QTYPE[Q.dtype], _dev(Pi, "Pi", (torch.float32,)),
+        _dev(S_mat, "S_mat", (torch.float32,)), _dev(A, "A", (torch.float32,)),
+        _dev(T, "T", (torch.float32,)), P, H, B, D, _stream()))
+    if Q.dim() == 2:
+        return A.view(B, D), T.view(B, D)
+    return A, T
+
+
+def _keys3(t: torch.Tensor, P: int):
+    if t.dim() == 2 and P == 1:
+        return t.shape[0], t.shape[1]
+    if t.dim() == 3 and t.shape[0] == P:
+        return t.shape[1], t.shape[2]
+    raise ValueError(f"key tensor shape {tuple(t.shape)} does not match P={P}")
+
+
+def _scores_out(out, P, B, S, like):
+    if out is None:
+        out = torch.empty((P, B, S), device=like.device, dtype=torch.float32)
+    if out.numel() != P * B * S:
+        raise ValueError("scores output has the wrong size")
+    return out
+
+
+def scores(A, T, K_idx, signs, gamma, codebook, path="auto", out=None):
+    """Scores from an unpacked cache: K_idx uint8 [P,S,D], signs int8 [P,S,D], gamma fp32 [P,S]."""
+    P, B, D = _as3(A)
+    S, Dk = _keys3(K_idx, P)
+    if Dk != D or signs.shape != K_idx.shape or gamma.numel() != P * S:
+        raise ValueError("inconsistent key shapes")
+    o = _scores_out(out, P, B, S, A)
+    _check("tq_scores", lib().tq_scores(
+        _dev(A, "A", (torch.float32,)), _dev(T, "T", (torch.float32,)),
+        _dev(K_idx, "K_idx", (torch.uint8,)), _dev(signs, "signs", (torch.int8,)),
+        _dev(gamma, "gamma", (torch.float32,)), _dev(codebook, "codebook", (torch.float32,)),
+        _dev(o, "scores", (torch.float32,)), P, B, S, D, codebook.numel(), PATHS[path], _stream()))
+    return o if (out is not None or A.dim() == 3) else o.view(B, S)
+
+
+def scores_packed(A, T, idx_plane, sign_plane, gamma_f16, codebook, idx_bits, path="auto", out=None):
+    """Scores from a bit-packed cache: idx_plane uint8 [P,S,D*bits/8], sign_plane uint8
+    [P,S,D/8], gamma_f16 float16 [P,S]."""
+    P, B, D = _as3(A)
+    S, row = _keys3(idx_plane, P)
+    if row * 8 != D * idx_bits or sign_plane.shape[-1] * 8 != D or gamma_f16.numel() != P * S:
+        raise ValueError("inconsistent packed key shapes")
+    o = _scores_out(out, P, B, S, A)
+    _check("tq_scores_packed", lib().tq_scores_packed(
+        _dev(A, "A", (torch.float32,)), _dev(T, "T", (torch.float32,)),
+        _dev(idx_plane, "idx_plane", (torch.uint8,)), _dev(sign_plane, "sign_plane", (torch.uint8,)),
+        _dev(gamma_f16, "gamma_f16", (torch.float16,)), _dev(codebook, "codebook", (torch.float32,)),
+        _dev(o, "scores", (torch.float32,)), P, B, S, D, idx_bits, PATHS[path], _stream()))
+    return o if (out is not None or A.dim() == 3) else o.view(B, S)
+
+
+def workspace_bytes(P: int, B: int, D: int) -> int:
+    return int(lib().tq_workspace_bytes(P, B, D))
+
+
+def _workspace(ws, P, B, D, like):
+    need = workspace_bytes(P, B, D)
+    if ws is None:
+        ws = torch.empty(need, device=like.device, dtype=torch.uint8)
+    return ws
+
+
+def solve(Q, K_idx, signs, gamma, Pi, S_mat, codebook, path="auto", workspace=None, out=None):
+    """Fused query transform + scoring over an unpacked cache."""
+    P, B, D = _as3(Q)
+    H = 1 if Pi.dim() == 2 else Pi.shape[0]
+    S, Dk = _keys3(K_idx, P)
+    if Dk != D:
+        raise ValueError("inconsistent key shapes")
+    ws = _workspace(workspace, P, B, D, Q)
+    o = _scores_out(out, P, B, S, Q)
+    _check("tq_solve", lib().tq_solve(
+        _dev(Q, "Q", QTYPE), QTYPE[Q.dtype], _dev(K_idx, "K_idx", (torch.uint8,)),
+        _dev(signs, "signs", (torch.int8,)), _dev(gamma, "gamma", (torch.float32,)),
+        _dev(Pi, "Pi", (torch.float32,)), _dev(S_mat, "S_mat", (torch.float32,)),
+        _dev(codebook, "codebook", (torch.float32,)), _dev(o, "scores", (torch.float32,)),
+        P, H, B, S, D, codebook.numel(), _dev(ws, "workspace", (torch.uint8,)), ws.numel(),
+        PATHS[path], _stream()))
+    return o if (out is not None or Q.dim() == 3) else o.view(B, S)
+
+
+def solve_packed(Q, idx_plane, sign_plane, gamma_f16, Pi, S_mat, codebook, idx_bits, path="auto",
+                 workspace=None, out=None):
+    """Fused query transform + scoring over a bit-packed cache."""
+    P, B, D = _as3(Q)
+    H = 1 if Pi.dim() == 2 else Pi.shape[0]
+    S, _ = _keys3(idx_plane, P)
+    ws = _workspace(workspace, P, B, D, Q)
+    o = _scores_out(out, P, B, S, Q)
+    _check("tq_solve_packed", lib().tq_solve_packed(
+        _dev(Q, "Q", QTYPE), QTYPE[Q.dtype], _dev(idx_plane, "idx_plane", (torch.uint8,)),
+        _dev(sign_plane, "sign_plane", (torch.uint8,)), _dev(gamma_f16, "gamma_f16", (torch.float16,)),
+        _dev(Pi, "Pi", (torch.float32,)), _dev(S_mat, "S_mat", (torch.float32,)),
+        _dev(codebook, "codebook", (torch.float32,)), _dev(o, "scores", (torch.float32,)),
+        P, H, B, S, D, idx_bits, _dev(ws, "workspace", (torch.uint8,)), ws.numel(),
+        PATHS[path], _stream()))
+    return o if (out is not None or Q.dim() == 3) else o.view(B, S)
+
+
+def pack_indices(K_idx, bits, out=None):
+    """uint8 codes [..., D] -> packed plane [..., D*bits/8]."""
+    D = K_idx.shape[-1]
+    n = K_idx.numel() // D
+    o = out if out is not None else torch.empty((*K_idx.shape[:-1], D * bits // 8), device=K_idx.device, dtype=torch.uint8)
+    _check("tq_pack_indices", lib().tq_pack_indices(
+        _dev(K_idx, "K_idx", (torch.uint8,)), _dev(o, "idx_plane", (torch.uint8,)), n, D, bits, _stream()))
+    return o
+
+
+def unpack_indices(plane, D, bits, out=None):
+    n = plane.numel() // (D * bits // 8)
+    o = out if out is not None else torch.empty((*plane.shape[:-1], D), device=plane.device, dtype=torch.uint8)
+    _check("tq_unpack_indices", lib().tq_unpack_indices(
+        _dev(plane, "idx_plane", (torch.uint8,)), _dev(o, "K_idx", (torch.uint8,)), n, D, bits, _stream()))
+    return o
+
+
+def pack_signs(signs, out=None):
+    D = signs.shape[-1]
+    n = signs.numel() // D
+    o = out if out is not None else torch.empty((*signs.shape[:-1], D // 8), device=signs.device, dtype=torch.uint8)
+    _check("tq_pack_signs", lib().tq_pack_signs(
+        _dev(signs, "signs", (torch.int8,)), _dev(o, "sign_plane", (torch.uint8,)), n, D, _stream()))
+    return o
+
+
+def unpack_signs(plane, D, out=None):
+    n = plane.numel() // (D // 8)
+    o = out if out is not None else torch.empty((*plane.shape[:-1], D), device=plane.device, dtype=torch.int8)
+    _check("tq_unpack_signs", lib().tq_unpack_signs(
+        _dev(plane, "sign_plane", (torch.uint8,)), _dev(o, "signs", (torch.int8,)), n, D, _stream()))
+    return o

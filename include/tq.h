@@ -1,0 +1,167 @@
+/*
+ * tq.h -- C ABI of libtq: raw TurboQuant_prod attention scores read straight
+ * from a compressed key cache, on one NVIDIA Blackwell GPU (sm_103a).
+ *
+ * For query b and cached key s of a problem, the library computes
+ *
+ *   score[b,s] = <A_b, codebook[K_idx[s,:]]> + (sqrt(pi/2)/D) * gamma[s] * <T_b, sign[s,:]>
+ *   with A_b = Pi q_b and T_b = S_mat q_b,
+ *
+ * with no softmax, no value read and no 1/sqrt(D) scale.  The query-side
+ * transform is the identity of "TurboQuant Attention in CUDA: Transform the
+ * Query, Reuse the Work" (riteshyadav.xyz), section "Move the transforms to
+ * the query"; the estimator is TurboQuant_prod ("Implementing TurboQuant on
+ * NVIDIA's AGX Thor", zededa.com, "Theorem 2: Unbiased Inner Products";
+ * "TurboQuant: Rotate-then-Quantize KV Caches at 3 Bits", kanthi.in, §3,
+ * TurboQuantProd).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Memory: unless stated otherwise every pointer is a DEVICE pointer owned by
+ *   the caller.  The library allocates no memory and keeps no mutable global
+ *   state; concurrent calls on different streams are safe as long as their
+ *   output and workspace buffers do not overlap.
+ * - Streams: every call is asynchronous on `stream` (0 = legacy default
+ *   stream).  Outputs are valid once the stream reaches the call.
+ * - Errors: argument errors are reported synchronously, before anything is
+ *   launched (nothing is written).  A launch error reported by CUDA maps to
+ *   TQ_ERR_LAUNCH.  Faults during execution surface at the caller's next
+ *   synchronisation, as for any CUDA library.  Nothing is printed and no C++
+ *   exception crosses the ABI.
+ * - Layouts are dense and row-major.  P independent problems are laid out
+ *   back to back: queries [P,B,D], keys [P,S,...], scores [P,B,S].  Problem p
+ *   uses rotation and projection head p % H (grouped-query attention: all
+ *   problems of one KV head share its Pi and S_mat).  The codebook is shared.
+ * - Alignment: every array pointer must be 16-byte aligned
+ *   (TQ_ERR_MISALIGNED otherwise).  Row pitches need no alignment.
+ * - Indices: every code must be < C (unpacked) or < 2^idx_bits (packed); this
+ *   is the caller's contract and is not checked on the device.
+ */
+#ifndef TQ_H
+#define TQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TQ_OK = 0,
+  TQ_ERR_INVALID_VALUE = 1, /* null pointer, size <= 0 or out of range               */
+  TQ_ERR_UNSUPPORTED = 2,   /* valid arguments no kernel of this library implements     */
+  TQ_ERR_MISALIGNED = 3,    /* an array pointer is not 16-byte aligned                  */
+  TQ_ERR_WORKSPACE = 4,     /* workspace null or smaller than tq_workspace_bytes()      */
+  TQ_ERR_LAUNCH = 5         /* CUDA reported an error when the kernels were launched    */
+} tq_status;
+
+/* Element type of the queries Q. */
+typedef enum { TQ_Q_F32 = 0, TQ_Q_BF16 = 1 } tq_qtype;
+
+/* Arithmetic path of a scoring call.
+ * TQ_PATH_FP32: CUDA-core fp32 throughout; max |err| <= 1e-5 (1 + |score|) against
+ *   the float64 definition.
+ * TQ_PATH_BF16_MMA: A and T rounded to bf16, centroids rounded to bf16, signs exact,
+ *   products summed by the tensor cores in fp32; max |err| <= 2e-3 ||q_b||_2.
+ *   Requires D == 128.
+ * TQ_PATH_AUTO: the path tq_auto_path(B, D) names. */
+typedef enum { TQ_PATH_AUTO = 0, TQ_PATH_FP32 = 1, TQ_PATH_BF16_MMA = 2 } tq_path;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* tq_status_string(tq_status status);
+
+/* The path TQ_PATH_AUTO resolves to for B queries of length D per problem. */
+tq_path tq_auto_path(int B, int D);
+
+/* ------------------------------------------------------------------------
+ * Query transform (riteshyadav.xyz, "Two kernels, two jobs", first kernel;
+ * zededa.com v3 "Combined Transform": one [Pi | S_mat] product per query).
+ *
+ *   A[p,b,d] = sum_j Pi[h,d,j]    * Q[p,b,j]
+ *   T[p,b,d] = sum_j S_mat[h,d,j] * Q[p,b,j]      h = p % H
+ *
+ * Q: [P,B,D] of `qtype` (bf16 values are widened exactly).  Pi, S_mat: [H,D,D]
+ * fp32.  A, T: [P,B,D] fp32 outputs.  1 <= D <= 256, 1 <= H <= P.
+ * ---------------------------------------------------------------------- */
+tq_status tq_prepare_queries(const void* Q, tq_qtype qtype, const float* Pi, const float* S_mat,
+                             float* A, float* T, int P, int H, int B, int D, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Scores from an UNPACKED cache (riteshyadav.xyz, "Two kernels, two jobs",
+ * second kernel, and "Full CUDA solution"): one byte per index and per sign.
+ *
+ * A, T: [P,B,D] fp32 (from tq_prepare_queries).  K_idx: [P,S,D] uint8 codes < C.
+ * signs: [P,S,D] int8, each +1 or -1.  gamma: [P,S] fp32 residual norms.
+ * codebook: [C] fp32.  scores: [P,B,S] fp32 output.
+ * 1 <= D <= 256, 1 <= C <= 256.  TQ_PATH_BF16_MMA needs D == 128.
+ * ---------------------------------------------------------------------- */
+tq_status tq_scores(const float* A, const float* T, const uint8_t* K_idx, const int8_t* signs,
+                    const float* gamma, const float* codebook, float* scores,
+                    int P, int B, int S, int D, int C, tq_path path, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Scores from a BIT-PACKED cache: two bit planes per key plus an fp16 norm
+ * (kanthi.in §8 "Kernel view", packed slot sizes; zededa.com v6 tile scorer,
+ * (packed >> sub*BITS) & MASK).
+ *
+ * idx_plane: [P,S,D*idx_bits/8] bytes.  Within a key, bit t of coordinate d is
+ *   stream bit idx_bits*d + t, and stream bit i is bit (i mod 8) of byte i/8
+ *   (little-endian; 3-bit fields straddle bytes).
+ * sign_plane: [P,S,D/8] bytes; bit d (same numbering) is 1 exactly when sigma_d = +1.
+ * gamma_f16: [P,S] IEEE binary16 residual norms (raw 16-bit patterns).
+ * codebook: [2^idx_bits] fp32.  A, T, scores as for tq_scores.
+ * D % 32 == 0, 32 <= D <= 256, idx_bits in {1,2,3}.
+ * ---------------------------------------------------------------------- */
+tq_status tq_scores_packed(const float* A, const float* T, const uint8_t* idx_plane,
+                           const uint8_t* sign_plane, const uint16_t* gamma_f16,
+                           const float* codebook, float* scores, int P, int B, int S, int D,
+                           int idx_bits, tq_path path, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Fused query transform + scoring: the challenge's `solve` without its
+ * per-call cudaMalloc/cudaFree (riteshyadav.xyz, "What the rearrangement
+ * saves": its solve "allocates temporary arrays on every call").  The caller
+ * passes `workspace`, a device buffer of at least tq_workspace_bytes(P, B, D)
+ * bytes that holds A and T between the two steps; it is scratch, its contents
+ * on return are unspecified, and calls that may run concurrently must not
+ * share it.
+ * ---------------------------------------------------------------------- */
+size_t tq_workspace_bytes(int P, int B, int D);
+
+tq_status tq_solve(const void* Q, tq_qtype qtype, const uint8_t* K_idx, const int8_t* signs,
+                   const float* gamma, const float* Pi, const float* S_mat, const float* codebook,
+                   float* scores, int P, int H, int B, int S, int D, int C,
+                   void* workspace, size_t workspace_bytes, tq_path path, cudaStream_t stream);
+
+tq_status tq_solve_packed(const void* Q, tq_qtype qtype, const uint8_t* idx_plane,
+                          const uint8_t* sign_plane, const uint16_t* gamma_f16, const float* Pi,
+                          const float* S_mat, const float* codebook, float* scores,
+                          int P, int H, int B, int S, int D, int idx_bits,
+                          void* workspace, size_t workspace_bytes, tq_path path,
+                          cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Bit packing of the cache format above, bit-exact in both directions
+ * (kanthi.in §11 "Verification plan", item 4: pack then unpack is the
+ * identity for every slot size and head dimension).
+ *
+ * n_keys rows of D coordinates.  Packing ignores code bits at and above
+ * `bits`; packing signs stores 1 for every strictly positive int8.
+ * Unpacked signs are +1 / -1.  D % 8 == 0, 8 <= D <= 4096, bits in {1,...,8}.
+ * ---------------------------------------------------------------------- */
+tq_status tq_pack_indices(const uint8_t* K_idx, uint8_t* idx_plane, int64_t n_keys, int D,
+                          int bits, cudaStream_t stream);
+tq_status tq_unpack_indices(const uint8_t* idx_plane, uint8_t* K_idx, int64_t n_keys, int D,
+                            int bits, cudaStream_t stream);
+tq_status tq_pack_signs(const int8_t* signs, uint8_t* sign_plane, int64_t n_keys, int D,
+                        cudaStream_t stream);
+tq_status tq_unpack_signs(const uint8_t* sign_plane, int8_t* signs, int64_t n_keys, int D,
+                          cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TQ_H */

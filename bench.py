@@ -1,0 +1,445 @@
+#!/usr/bin/env python
+"""Throughput of the TurboQuant_prod score path (query transform + scoring) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config c1] [--path auto]
+    python bench.py --impl reference ...      # the CPU oracle on the host cores
+
+One step = one pass of the whole hot path over one workload: the query
+transform A = Pi q, T = S_mat q for every query, then every raw score read from
+the compressed cache.  Inputs are synthetic (the ``synth`` draws), compressed on
+the GPU by libtq's own compressor before timing starts; nothing on the timed
+path touches the CPU oracle.  Prints one JSON line (rank 0).
+
+Timing: each step is one replay of a CUDA graph holding the step's two kernels;
+steps rotate over enough independent input/output copies that their union is
+more than twice the L2, so every step reads its cache from HBM.  The scoring
+kernel's own duration is taken with CUDA events recorded inside those graphs
+on the launching stream.  Under torchrun every rank runs its own replica of the
+workload (weak scaling, no data-path collective); the timed region is bracketed
+by a barrier and the max over ranks is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "scores/sec and achieved HBM GB/s (fraction of ~8 TB/s) at 1 GB300"
+FALLBACK_HBM_GBS = 6800.0
+
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the scoring kernel, from
+# the ncu captures summarised under profiles/, keyed by (workload, path, kernel source
+# fingerprint).  A changed kernel source makes the figure stale and it is reported null.
+NCU_TRAFFIC = {}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", choices=sorted(synth.WORKLOADS), default="c1")
+    ap.add_argument("--path", choices=["auto", "fp32", "bf16_mma"], default="auto")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="approximate CPU time of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# accounting
+# ---------------------------------------------------------------------------
+
+def key_bytes(w) -> int:
+    if w.layout == "unpacked":
+        return 2 * w.D + (4 if w.gamma_dtype == "f32" else 2)
+    return w.D * w.mse_bits // 8 + w.D // 8 + (4 if w.gamma_dtype == "f32" else 2)
+
+
+def score_kernel_bytes(w) -> int:
+    """Algorithmic bytes of one scoring launch: the compressed cache once, the
+    scores once, A and T once, the codebook."""
+    return (w.P * w.S * key_bytes(w) + 4 * w.P * w.B * w.S + 2 * 4 * w.P * w.B * w.D + 4 * w.C)
+
+
+def step_input_bytes(w) -> int:
+    qbytes = w.P * w.B * w.D * (2 if w.q_dtype == "bf16" else 4)
+    return qbytes + w.P * w.S * key_bytes(w) + 2 * 4 * w.H * w.D * w.D + 4 * w.C
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_fingerprint() -> str:
+    import hashlib
+    h = hashlib.sha1()
+    for name in sorted(os.listdir(os.path.join(ROOT, "compressed_kv_cache_gb300", "csrc"))):
+        with open(os.path.join(ROOT, "compressed_kv_cache_gb300", "csrc", name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:12]
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.t0 = time.time()
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self, region):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = []
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[4:8]))
+            except ValueError:
+                continue
+        t_lo, t_hi = region
+        inside = [r for r in rows if t_lo - 1.0 <= r[0] <= t_hi + 1.0]
+        use = inside or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in use for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in use) if use else None,
+                "sm_max_mhz": max(r[2] for r in use) if use else None,
+                "reasons": reasons, "samples": len(use), "samples_in_region": len(inside)}
+
+
+# ---------------------------------------------------------------------------
+# workload on the device (product code only)
+# ---------------------------------------------------------------------------
+
+def build_device_workload(w, tq, torch, dev):
+    cb = torch.from_numpy(tq.lloyd_max_codebook(w.D, w.mse_bits)).to(dev)
+    Pi = torch.from_numpy(np.stack([tq.haar_rotation(synth.rotation_seed_matrix(w.seed, h, w.D))
+                                    for h in range(w.H)])).to(dev)
+    S_mat = torch.from_numpy(np.stack([synth.s_matrix(w.seed, h, w.D) for h in range(w.H)])).to(dev)
+    gdt = torch.float32 if w.gamma_dtype == "f32" else torch.float16
+    idx = torch.empty((w.P, w.S, w.D), dtype=torch.uint8, device=dev)
+    sg = torch.empty((w.P, w.S, w.D), dtype=torch.int8, device=dev)
+    gamma = torch.empty((w.P, w.S), dtype=gdt, device=dev)
+    for p in range(w.P):
+        keys = torch.from_numpy(synth.unit_keys(w.seed, p, 0, w.S, w.D).astype(np.float32)).to(dev)
+        i_, s_, g_ = tq.compress_keys(keys, Pi[p % w.H], S_mat[p % w.H], cb, gdt)
+        idx[p].copy_(i_)
+        sg[p].copy_(s_)
+        gamma[p].copy_(g_)
+    if w.q_dtype == "bf16":
+        Q = torch.from_numpy(np.stack([synth.queries(w.seed, p, w.B, w.D, "bf16")[1]
+                                       for p in range(w.P)]).view(np.int16)).to(dev).view(torch.bfloat16)
+    else:
+        Q = torch.from_numpy(np.stack([synth.queries(w.seed, p, w.B, w.D, "f32")[0]
+                                       for p in range(w.P)])).to(dev)
+    cache = {"gamma": gamma}
+    if w.layout == "unpacked":
+        cache["idx"], cache["signs"] = idx, sg
+    else:
+        cache["idx"] = tq.pack_indices(idx, w.mse_bits)
+        cache["signs"] = tq.pack_signs(sg)
+    torch.cuda.synchronize(dev)
+    return Q, Pi, S_mat, cb, cache
+
+
+def score_call(tq, w, path, A, T, cache, cb, out):
+    if w.layout == "unpacked":
+        return tq.scores(A, T, cache["idx"], cache["signs"], cache["gamma"], cb, path=path, out=out)
+    return tq.scores_packed(A, T, cache["idx"], cache["signs"], cache["gamma"], cb, w.mse_bits,
+                            path=path, out=out)
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (cpu_baseline leg and --impl reference only)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(w, n_keys):
+    import oracle
+    cb = oracle.lloyd_max_sphere(w.D, w.mse_bits)[0].astype(np.float32)
+    Pi = oracle.haar_rotation(synth.rotation_seed_matrix(w.seed, 0, w.D)).astype(np.float32)
+    S_mat = synth.s_matrix(w.seed, 0, w.D)
+    keys = synth.unit_keys(w.seed, 0, 0, n_keys, w.D)
+    idx, sg, gamma = oracle.compress_prod(keys, Pi, S_mat, cb, w.gamma_dtype)
+    Q = synth.queries(w.seed, 0, w.B, w.D, w.q_dtype)[0]
+    return oracle, (Q, Pi, S_mat, idx, sg, gamma, cb)
+
+
+def time_oracle(w, seconds, n_keys=None):
+    """Scores/s of the oracle (query transform + scoring of B queries over a key sample)."""
+    n_keys = n_keys or min(w.S, 4096)
+    oracle, args = oracle_sample(w, n_keys)
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        oracle.scores_from_queries(*args)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"value": reps * w.B * n_keys / el, "unit": "scores/s", "cores": cores, "kind": "oracle",
+            "sample": f"{reps} x (query transform + {w.B} queries x {n_keys} keys of problem 0), "
+                      f"{el:.1f} s, float64 NumPy (BLAS threads = host cores)"}
+
+
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    n_keys = min(w.S, 4096)
+    oracle, ins = oracle_sample(w, n_keys)
+    for _ in range(args.warmup):
+        oracle.scores_from_queries(*ins)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.scores_from_queries(*ins)
+    el = time.perf_counter() - t0
+    value = args.steps * w.B * n_keys / el
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "scores/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "sample_keys": n_keys, "B": w.B, "D": w.D},
+            "cpu_baseline": {"value": value, "unit": "scores/s", "cores": cores, "kind": "oracle",
+                             "sample": f"each step: query transform + {w.B} queries x {n_keys} keys "
+                                       f"(a bounded sample of the workload), float64 NumPy"},
+            "e2e": {"value": value, "unit": "scores/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def main():
+    args = parse_args()
+    w = synth.WORKLOADS[args.config]
+    if args.impl == "reference":
+        run_reference(args, w)
+        return
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+
+    import torch
+    from compressed_kv_cache_gb300 import tq
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    tq.lib()
+    path = args.path if args.path != "auto" else tq.auto_path(w.B, w.D)
+    Q0, Pi, S_mat, cb, cache0 = build_device_workload(w, tq, torch, dev)
+
+    # rotating copies: their union exceeds twice the L2 so that every step reads HBM
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    per_copy = score_kernel_bytes(w)
+    R = max(1, math.ceil(2.2 * l2 / per_copy))
+    R = min(R, max(1, int(40e9 // per_copy)))
+    copies = []
+    for r in range(R):
+        c = {k: v.clone() for k, v in cache0.items()}
+        copies.append({
+            "Q": Q0.clone(), "cache": c,
+            "A": torch.empty((w.P, w.B, w.D), device=dev), "T": torch.empty((w.P, w.B, w.D), device=dev),
+            "out": torch.empty((w.P, w.B, w.S), device=dev)})
+
+    stream = torch.cuda.Stream(dev)
+    try:
+        torch.cuda.Event(enable_timing=True, external=True)
+        ext = True
+    except TypeError:
+        ext = False
+
+    def step(cp, evs=None):
+        tq.prepare_queries(cp["Q"], Pi, S_mat, out=(cp["A"], cp["T"]))
+        if evs:
+            evs[0].record()
+        score_call(tq, w, path, cp["A"], cp["T"], cp["cache"], cb, cp["out"])
+        if evs:
+            evs[1].record()
+
+    with torch.cuda.stream(stream):
+        for cp in copies:          # eager pass over every copy before capture
+            step(cp)
+    torch.cuda.synchronize(dev)
+    graphs, kevents = [], []
+    for cp in copies:
+        g = torch.cuda.CUDAGraph()
+        evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)] if ext else None
+        with torch.cuda.graph(g, stream=stream):
+            step(cp, evs)
+        graphs.append(g)
+        kevents.append(evs)
+    torch.cuda.synchronize(dev)
+
+    clocks = ClockSampler(local)
+    with torch.cuda.stream(stream):
+        for k in range(args.warmup):
+            graphs[k % R].replay()
+    torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    with torch.cuda.stream(stream):
+        start.record()
+        for k in range(args.steps):
+            graphs[(args.warmup + k) % R].replay()
+        end.record()
+    torch.cuda.synchronize(dev)
+    t_wall1 = time.time()
+    if dist:
+        dist.barrier()
+    elapsed_ms = start.elapsed_time(end)
+    if dist:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    clk = clocks.stop((t_wall0, t_wall1))
+
+    # scoring-kernel duration: events recorded inside the graphs on the launching stream
+    if ext:
+        used = sorted({(args.warmup + k) % R for k in range(args.steps)})
+        kms = [kevents[i][0].elapsed_time(kevents[i][1]) for i in used]
+        kernel_ms = statistics.mean(kms)
+        ktiming = f"CUDA events inside the step graphs, last replay of each of {len(kms)} copies"
+    else:
+        kernel_ms = elapsed_ms / args.steps
+        ktiming = "whole step (graph-internal events unavailable in this torch)"
+
+    scores_per_step = w.P * w.B * w.S
+    value = world * scores_per_step * args.steps / (elapsed_ms / 1e3)
+    peak, peak_src = hbm_peak()
+    kbytes = score_kernel_bytes(w)
+    achieved = kbytes / (kernel_ms / 1e3) / 1e9
+    fp = kernel_fingerprint()
+    traffic = NCU_TRAFFIC.get((args.config, path, fp))
+
+    # end to end through the public fused API with host buffers
+    if True:
+        hostQ = Q0.cpu().pin_memory()
+        hcache = {k: v.cpu().pin_memory() for k, v in cache0.items()}
+        hPi, hS, hcb = Pi.cpu().pin_memory(), S_mat.cpu().pin_memory(), cb.cpu().pin_memory()
+        hout = torch.empty((w.P, w.B, w.S), dtype=torch.float32).pin_memory()
+        dQ, dcache = torch.empty_like(Q0), {k: torch.empty_like(v) for k, v in cache0.items()}
+        dPi, dS, dcb = torch.empty_like(Pi), torch.empty_like(S_mat), torch.empty_like(cb)
+        dout = torch.empty((w.P, w.B, w.S), device=dev)
+        ws = torch.empty(tq.workspace_bytes(w.P, w.B, w.D), dtype=torch.uint8, device=dev)
+        h2d = (hostQ.numel() * hostQ.element_size() + sum(v.numel() * v.element_size() for v in hcache.values())
+               + (hPi.numel() + hS.numel() + hcb.numel()) * 4)
+        d2h = hout.numel() * 4
+
+        def e2e_step():
+            dQ.copy_(hostQ, non_blocking=True)
+            for k in dcache:
+                dcache[k].copy_(hcache[k], non_blocking=True)
+            dPi.copy_(hPi, non_blocking=True)
+            dS.copy_(hS, non_blocking=True)
+            dcb.copy_(hcb, non_blocking=True)
+            if w.layout == "unpacked":
+                tq.solve(dQ, dcache["idx"], dcache["signs"], dcache["gamma"], dPi, dS, dcb, path=path,
+                         workspace=ws, out=dout)
+            else:
+                tq.solve_packed(dQ, dcache["idx"], dcache["signs"], dcache["gamma"], dPi, dS, dcb,
+                                w.mse_bits, path=path, workspace=ws, out=dout)
+            hout.copy_(dout, non_blocking=True)
+
+        e_steps = max(3, min(args.steps, 50))
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                e2e_step()
+        torch.cuda.synchronize(dev)
+        es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            es.record()
+            for _ in range(e_steps):
+                e2e_step()
+            ee.record()
+        torch.cuda.synchronize(dev)
+        e_ms = es.elapsed_time(ee)
+        e2e = {"value": scores_per_step * e_steps / (e_ms / 1e3), "unit": "scores/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": e_steps}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = time_oracle(w, args.cpu_seconds)
+
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "scores/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32" if path == "fp32" else "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "P": w.P, "H": w.H, "B": w.B, "S": w.S, "D": w.D,
+                   "idx_bits": w.mse_bits, "layout": w.layout, "gamma": w.gamma_dtype,
+                   "queries": w.q_dtype, "path": path,
+                   "l2": f"{R} rotating input/output copies, {R * per_copy / 1e6:.0f} MB > 2x L2 "
+                         f"({l2 / 1e6:.0f} MB); every step reads its cache from HBM",
+                   "parallelism": f"replicas x{world}"},
+        "hbm_gbs": achieved,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "scoring kernel", "kernel_ms": kernel_ms, "bytes_per_launch": kbytes,
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback 6.8 TB/s",
+                     "timing": ktiming, "kernel_fingerprint": fp},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

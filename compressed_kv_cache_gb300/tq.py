@@ -48,6 +48,9 @@ _SIGNATURES = {
     "tq_unpack_indices": ([_P, _P, _L, _I, _I, _P], _I),
     "tq_pack_signs": ([_P, _P, _L, _I, _P], _I),
     "tq_unpack_signs": ([_P, _P, _L, _I, _P], _I),
+    "tq_compress_keys": ([_P, _P, _P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _P], _I),
+    "tq_lloyd_max_codebook": ([_I, _I, _I, _I, _P], _I),
+    "tq_haar_rotation": ([_P, _I, _P], _I),
 }
 
 
@@ -257,3 +260,40 @@ def unpack_signs(plane, D, out=None):
     _check("tq_unpack_signs", lib().tq_unpack_signs(
         _dev(plane, "sign_plane", (torch.uint8,)), _dev(o, "signs", (torch.int8,)), n, D, _stream()))
     return o
+
+
+def lloyd_max_codebook(D: int, mse_bits: int, grid_points: int = 400_001, iterations: int = 300):
+    """Lloyd-Max codebook (host computation in libtq), float32 numpy array of 2^mse_bits."""
+    import numpy as np
+    out = np.empty(1 << mse_bits, dtype=np.float32)
+    _check("tq_lloyd_max_codebook", lib().tq_lloyd_max_codebook(
+        D, mse_bits, grid_points, iterations, out.ctypes.data))
+    return out
+
+
+def haar_rotation(G):
+    """Sign-fixed QR rotation of a float64 [D,D] numpy matrix (host computation in libtq)."""
+    import numpy as np
+    G = np.ascontiguousarray(G, dtype=np.float64)
+    D = G.shape[0]
+    out = np.empty((D, D), dtype=np.float32)
+    _check("tq_haar_rotation", lib().tq_haar_rotation(G.ctypes.data, D, out.ctypes.data))
+    return out
+
+
+def compress_keys(keys, Pi, S_mat, codebook, gamma_dtype=torch.float32):
+    """TurboQuant_prod compression on the GPU.  keys fp32 [P,S,D] (or [S,D]); Pi, S_mat
+    [H,D,D] (or [D,D]).  Returns (K_idx uint8, signs int8, gamma fp32 or fp16)."""
+    P, S, D = _as3(keys)
+    H = 1 if Pi.dim() == 2 else Pi.shape[0]
+    K_idx = torch.empty(keys.shape, device=keys.device, dtype=torch.uint8)
+    signs = torch.empty(keys.shape, device=keys.device, dtype=torch.int8)
+    gamma = torch.empty(keys.shape[:-1], device=keys.device, dtype=gamma_dtype)
+    g32 = _dev(gamma, "gamma", (torch.float32,)) if gamma_dtype == torch.float32 else None
+    g16 = _dev(gamma, "gamma", (torch.float16,)) if gamma_dtype == torch.float16 else None
+    _check("tq_compress_keys", lib().tq_compress_keys(
+        _dev(keys, "keys", (torch.float32,)), _dev(Pi, "Pi", (torch.float32,)),
+        _dev(S_mat, "S_mat", (torch.float32,)), _dev(codebook, "codebook", (torch.float32,)),
+        codebook.numel(), _dev(K_idx, "K_idx", (torch.uint8,)), _dev(signs, "signs", (torch.int8,)),
+        g32, g16, P, H, S, D, _stream()))
+    return K_idx, signs, gamma

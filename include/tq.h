@@ -160,6 +160,40 @@ tq_status tq_pack_signs(const int8_t* signs, uint8_t* sign_plane, int64_t n_keys
 tq_status tq_unpack_signs(const uint8_t* sign_plane, int8_t* signs, int64_t n_keys, int D,
                           cudaStream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Compressor: the write side of the cache (TurboQuant_prod, kanthi.in §3
+ * TurboQuantProd and "Kernel checklist" of §8: rotate, search the midpoints,
+ * residual sketch; zededa.com "Theorem 2").
+ *
+ * tq_compress_keys (device): for each unit-norm key k of problem p (head
+ * h = p % H): y = Pi_h k; idx_d = number of codebook midpoints strictly below
+ * y_d (ties go to the lower index); r = k - Pi_h^T c[idx]; sign_d = +1 when
+ * (S_mat_h r)_d >= 0, else -1; gamma = ||r||_2.  keys: [P,S,D] fp32; Pi,
+ * S_mat: [H,D,D]; codebook: [C] fp32 sorted ascending; outputs K_idx [P,S,D]
+ * uint8, signs [P,S,D] int8 and exactly one of gamma_f32 / gamma_f16 [P,S]
+ * (the other NULL).  Computed in fp32: a coordinate within ~1e-6 of a cell
+ * edge may fall on either side.  D % 32 == 0, D <= 128, C <= 256.  Keys are
+ * taken as unit length (the score has no key-norm term).  Pack the outputs
+ * with tq_pack_indices / tq_pack_signs for the packed layout.
+ *
+ * tq_lloyd_max_codebook (HOST pointer out): the 2^mse_bits Lloyd-Max centroids
+ * of one coordinate of a uniform unit vector in R^D, density proportional to
+ * (1-x^2)^((D-3)/2) on [-1,1] sampled at grid_points even points (kanthi.in
+ * §2-§4: 400001 points, 300 rounds, start evenly spaced on +-2/sqrt(D)).
+ * D >= 3, 1 <= mse_bits <= 8.
+ *
+ * tq_haar_rotation (HOST pointers): Pi = Q diag(sign(diag R)) for the QR
+ * factorisation G = QR of a D x D float64 matrix G (row-major), written as
+ * fp32 row-major (kanthi.in §3, HaarRotation).  D <= 4096.
+ * ---------------------------------------------------------------------- */
+tq_status tq_compress_keys(const float* keys, const float* Pi, const float* S_mat,
+                           const float* codebook, int C, uint8_t* K_idx, int8_t* signs,
+                           float* gamma_f32, uint16_t* gamma_f16, int P, int H, int S, int D,
+                           cudaStream_t stream);
+tq_status tq_lloyd_max_codebook(int D, int mse_bits, int grid_points, int iterations,
+                                float* centroids);
+tq_status tq_haar_rotation(const double* G, int D, float* Pi);
+
 #ifdef __cplusplus
 }
 #endif

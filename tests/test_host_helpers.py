@@ -1,0 +1,49 @@
+"""libtq's host-side setup helpers (codebook, rotation) against the CPU oracle.
+Both run on the host, so these tests need no GPU."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from conftest import codebook
+from compressed_kv_cache_gb300 import build as tqbuild
+from compressed_kv_cache_gb300 import tq
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    tqbuild.build()
+
+
+@pytest.mark.parametrize("bits", [1, 2, 3, 4])
+def test_lloyd_max_matches_oracle(bits):
+    want = codebook(128, bits)[0]
+    got = tq.lloyd_max_codebook(128, bits)
+    # same algorithm and grid, different summation order: agree to float32 rounding
+    np.testing.assert_allclose(got, want.astype(np.float32), rtol=2e-6, atol=1e-9)
+
+
+def test_lloyd_max_other_dims():
+    for D in (16, 64):
+        want = oracle.lloyd_max_sphere(D, 2, iters=80)[0]
+        np.testing.assert_allclose(tq.lloyd_max_codebook(D, 2, 400_001, 80), want, rtol=2e-6)
+
+
+@pytest.mark.parametrize("D", [2, 5, 128])
+def test_haar_rotation_matches_oracle(D):
+    G = synth.rotation_seed_matrix(1234, 3, D)
+    want = oracle.haar_rotation(G).astype(np.float32)
+    got = tq.haar_rotation(G)
+    np.testing.assert_allclose(got, want, rtol=0, atol=4e-7)
+    assert np.abs(got.astype(np.float64) @ got.T.astype(np.float64) - np.eye(D)).max() < 1e-6
+
+
+def test_host_helper_argument_errors():
+    L = tq.lib()
+    out = np.empty(4, np.float32)
+    assert L.tq_lloyd_max_codebook(2, 2, 1001, 10, out.ctypes.data) == 1
+    assert L.tq_lloyd_max_codebook(128, 9, 1001, 10, out.ctypes.data) == 1
+    assert L.tq_haar_rotation(None, 4, out.ctypes.data) == 1
+    f = 0x100000
+    assert L.tq_compress_keys(f, f, f, f, 4, f, f, f, f, 1, 1, 8, 128, None) == 1   # both gammas
+    assert L.tq_compress_keys(f, f, f, f, 4, f, f, f, None, 1, 1, 8, 160, None) == 2  # D > 128

@@ -145,20 +145,55 @@ struct Params {
   float kappa;
 };
 
-// Dequantise one 128-key tile into the X buffer at `xbuf` (shared address).
-// Thread t: row r = t % 128, half t / 128 (0: the 128 centroids, 1: the 128 signs).
+// Raw bytes of one key row held in registers between the load and the dequantisation,
+// so that the next tile's loads are in flight while the current tile is drained.
+// Thread t: row r = t % 128, half t / 128 (0: the code row and gamma, 1: the sign row).
 template <int LAYOUT>
-__device__ __forceinline__ void dequant_tile(const Params& prm, int p, int kt, uint32_t xbuf,
-                                             const uint32_t* lut, const uint16_t* cbf,
-                                             float* gam) {
-  constexpr int kBits = LAYOUT >= kPacked1 ? LAYOUT - kPacked1 + 1 : 8;
+struct RawRow {
+  static constexpr int kBits = LAYOUT >= kPacked1 ? LAYOUT - kPacked1 + 1 : 8;
+  static constexpr int kVec = LAYOUT >= kPacked1 ? kBits : 8;   // uint4 per code row
+  uint4 v[kVec];
+  float g;
+  bool valid;
+};
+
+template <int LAYOUT>
+__device__ __forceinline__ void load_row(const Params& prm, int p, int kt, RawRow<LAYOUT>& raw) {
   const int r = threadIdx.x & (kM - 1);
   const int half = threadIdx.x >> 7;
   const int s = kt * kM + r;
-  const bool valid = s < prm.S;
+  raw.valid = s < prm.S;
+  if (!raw.valid) return;
   const size_t key = static_cast<size_t>(p) * prm.S + s;
+  if constexpr (LAYOUT >= kPacked1) {
+    constexpr int kBits = RawRow<LAYOUT>::kBits;
+    if (half == 0) {
+      const uint4* src = reinterpret_cast<const uint4*>(prm.idx + key * (16 * kBits));
+#pragma unroll
+      for (int i = 0; i < kBits; ++i) raw.v[i] = __ldg(src + i);
+      raw.g = __half2float(__ushort_as_half(__ldg(static_cast<const uint16_t*>(prm.gamma) + key)));
+    } else {
+      raw.v[0] = __ldg(reinterpret_cast<const uint4*>(prm.signs + key * 16));
+    }
+  } else {
+    const uint4* src = reinterpret_cast<const uint4*>((half == 0 ? prm.idx : prm.signs) + key * 128);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) raw.v[i] = __ldg(src + i);
+    if (half == 0) raw.g = __ldg(static_cast<const float*>(prm.gamma) + key);
+  }
+}
+
+// Dequantise the row into the X buffer at `xbuf` (shared address): half 0 writes the
+// 128 centroids (core-matrix columns 0..15), half 1 the 128 signs (columns 16..31).
+template <int LAYOUT>
+__device__ __forceinline__ void store_row(const Params& prm, const RawRow<LAYOUT>& raw,
+                                          uint32_t xbuf, const uint32_t* lut,
+                                          const uint16_t* cbf, float* gam) {
+  constexpr int kBits = RawRow<LAYOUT>::kBits;
+  const int r = threadIdx.x & (kM - 1);
+  const int half = threadIdx.x >> 7;
   const uint32_t rowbase = xbuf + r * 16 + (half ? 16 * 2048 : 0);
-  if (!valid) {
+  if (!raw.valid) {
 #pragma unroll
     for (int kc = 0; kc < 16; ++kc) st_shared_v4(rowbase + kc * 2048, 0, 0, 0, 0);
     if (half == 0) gam[r] = 0.f;
@@ -166,13 +201,11 @@ __device__ __forceinline__ void dequant_tile(const Params& prm, int p, int kt, u
   }
   if (half == 0) {
     if constexpr (LAYOUT >= kPacked1) {
-      constexpr int kWords = 4 * kBits;                 // 16*bits bytes per row
+      constexpr int kWords = 4 * kBits;
       uint32_t w[kWords + 1];
-      const uint4* src = reinterpret_cast<const uint4*>(prm.idx + key * (16 * kBits));
 #pragma unroll
       for (int i = 0; i < kBits; ++i) {
-        const uint4 v = __ldg(src + i);
-        w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+        w[4 * i] = raw.v[i].x; w[4 * i + 1] = raw.v[i].y; w[4 * i + 2] = raw.v[i].z; w[4 * i + 3] = raw.v[i].w;
       }
       w[kWords] = 0u;
 #pragma unroll
@@ -185,14 +218,10 @@ __device__ __forceinline__ void dequant_tile(const Params& prm, int p, int kt, u
         st_shared_v4(rowbase + kc * 2048, lut[v & kPm], lut[(v >> (2 * kBits)) & kPm],
                      lut[(v >> (4 * kBits)) & kPm], lut[(v >> (6 * kBits)) & kPm]);
       }
-      const __half g = __ushort_as_half(__ldg(static_cast<const uint16_t*>(prm.gamma) + key));
-      gam[r] = __half2float(g);
     } else {
-      const uint4* src = reinterpret_cast<const uint4*>(prm.idx + key * 128);
-#pragma unroll 4
-      for (int c2 = 0; c2 < 8; ++c2) {                  // 16 codes per 16-byte load
-        const uint4 v = __ldg(src + c2);
-        const uint32_t ws[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int c2 = 0; c2 < 8; ++c2) {                  // 16 codes per 16-byte vector
+        const uint32_t ws[4] = {raw.v[c2].x, raw.v[c2].y, raw.v[c2].z, raw.v[c2].w};
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           uint32_t o[4];
@@ -210,12 +239,11 @@ __device__ __forceinline__ void dequant_tile(const Params& prm, int p, int kt, u
           st_shared_v4(rowbase + (2 * c2 + h) * 2048, o[0], o[1], o[2], o[3]);
         }
       }
-      gam[r] = __ldg(static_cast<const float*>(prm.gamma) + key);
     }
+    gam[r] = raw.g;
   } else {
     if constexpr (LAYOUT >= kPacked1) {
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(prm.signs + key * 16));
-      const uint32_t ws[4] = {~v.x, ~v.y, ~v.z, ~v.w};  // 1 = sigma is -1
+      const uint32_t ws[4] = {~raw.v[0].x, ~raw.v[0].y, ~raw.v[0].z, ~raw.v[0].w};  // 1 = sigma -1
 #pragma unroll
       for (int kc = 0; kc < 16; ++kc) {
         const uint32_t nb = (ws[kc >> 2] >> (8 * (kc & 3))) & 0xFFu;
@@ -223,11 +251,9 @@ __device__ __forceinline__ void dequant_tile(const Params& prm, int p, int kt, u
                      sign_pair(nb, 3));
       }
     } else {
-      const uint4* src = reinterpret_cast<const uint4*>(prm.signs + key * 128);
-#pragma unroll 4
+#pragma unroll
       for (int c2 = 0; c2 < 8; ++c2) {
-        const uint4 v = __ldg(src + c2);
-        const uint32_t ws[4] = {v.x, v.y, v.z, v.w};
+        const uint32_t ws[4] = {raw.v[c2].x, raw.v[c2].y, raw.v[c2].z, raw.v[c2].w};
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           uint32_t o[4];
@@ -341,10 +367,12 @@ __global__ void __launch_bounds__(kThreads, 1) scores_mma_kernel(Params prm) {
 
   int i = 0;
   int prev_kt = -1;
+  RawRow<LAYOUT> raw;
+  if (static_cast<int>(blockIdx.x) < prm.key_tiles) load_row<LAYOUT>(prm, p, blockIdx.x, raw);
   for (int kt = blockIdx.x; kt < prm.key_tiles; kt += gridDim.x, ++i) {
     const int stage = i & 1;
     const uint32_t xbuf = xaddr0 + stage * kXBytes;
-    dequant_tile<LAYOUT>(prm, p, kt, xbuf, lut, cbf, gam + stage * kM);
+    store_row<LAYOUT>(prm, raw, xbuf, lut, cbf, gam + stage * kM);
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -360,6 +388,8 @@ __global__ void __launch_bounds__(kThreads, 1) scores_mma_kernel(Params prm) {
       }
       mma_commit(smem_u32(mbar + stage));
     }
+    // the next tile's rows are in flight while this thread drains the previous tile
+    if (kt + static_cast<int>(gridDim.x) < prm.key_tiles) load_row<LAYOUT>(prm, p, kt + gridDim.x, raw);
     if (prev_kt >= 0) epilogue(prev_kt, stage ^ 1, ((i - 1) >> 1) & 1);
     prev_kt = kt;
   }
@@ -373,30 +403,36 @@ __global__ void __launch_bounds__(kThreads, 1) scores_mma_kernel(Params prm) {
 
 template <int LAYOUT>
 cudaError_t launch_layout(const Params& prm, int P, int qtiles, cudaStream_t st) {
-  // The opt-in shared-memory size is a per-device function attribute: set it on the
-  // first launch on each device (outside any stream capture in normal use).
-  static std::atomic<uint64_t> configured{0};
-  constexpr size_t smem = 232448;   // 227 KB, the per-CTA opt-in maximum of sm_100-class GPUs
-  static_assert(smem >= 2 * kXBytes + static_cast<size_t>(kMaxN) * kK * 2 + 256 * 4 + 256 * 2 +
-                            2 * kM * 4 + 2 * 8 + 16, "layout does not fit");
+  // The opt-in shared-memory size is a per-device function attribute: on the first
+  // launch on each device the kernel is given everything the device allows next to
+  // its static shared memory (one CTA per SM either way), so every descriptor the
+  // kernel builds addresses memory it owns.
+  static std::atomic<int> dyn_bytes[64];
+  constexpr size_t need = 2 * kXBytes + static_cast<size_t>(kMaxN) * kK * 2 + 256 * 4 + 256 * 2 +
+                          2 * kM * 4 + 2 * 8 + 16;
   int dev = 0, sms = 148;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  const uint64_t bit = 1ull << (dev & 63);
-  if (!(configured.load(std::memory_order_acquire) & bit)) {
-    e = cudaFuncSetAttribute(scores_mma_kernel<LAYOUT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
+  int smem = dyn_bytes[dev & 63].load(std::memory_order_acquire);
+  if (smem == 0) {
+    int optin = 0;
+    e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (e != cudaSuccess) return e;
-    configured.fetch_or(bit, std::memory_order_acq_rel);
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, scores_mma_kernel<LAYOUT>);
+    if (e != cudaSuccess) return e;
+    smem = optin - static_cast<int>(fa.sharedSizeBytes);
+    if (smem < static_cast<int>(need)) return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(scores_mma_kernel<LAYOUT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    dyn_bytes[dev & 63].store(smem, std::memory_order_release);
   }
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int per = P * qtiles;
   int gx = (sms + per - 1) / per;
   gx = gx < 1 ? 1 : (gx > prm.key_tiles ? prm.key_tiles : gx);
   dim3 grid(gx, qtiles, P);
-  // The CTA always takes the full opt-in shared memory (one CTA per SM either way):
-  // every descriptor the kernel builds then addresses memory it owns.
-  scores_mma_kernel<LAYOUT><<<grid, kThreads, smem, st>>>(prm);
+  scores_mma_kernel<LAYOUT><<<grid, kThreads, static_cast<size_t>(smem), st>>>(prm);
   return cudaGetLastError();
 }
 

@@ -51,6 +51,7 @@ _SIGNATURES = {
     "tq_compress_keys": ([_P, _P, _P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _P], _I),
     "tq_lloyd_max_codebook": ([_I, _I, _I, _I, _P], _I),
     "tq_haar_rotation": ([_P, _I, _P], _I),
+    "tq_solve_packed_noalloc": ([_P, _I, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P], _I),
 }
 
 

@@ -194,6 +194,35 @@ tq_status tq_lloyd_max_codebook(int D, int mse_bits, int grid_points, int iterat
                                 float* centroids);
 tq_status tq_haar_rotation(const double* G, int D, float* Pi);
 
+/* ------------------------------------------------------------------------
+ * tq_solve_packed_noalloc: tq_solve_packed for callers that cannot allocate
+ * device memory.  The pages have no counterpart: this is a deployment entry
+ * point of this library.
+ *
+ * Some callers have no way to hand over a workspace: an inference-engine
+ * plugin that receives only its input and output buffers while the engine owns
+ * all device memory, or a service that reserves its device memory once at
+ * start-up and must not allocate later (an allocation can fail or synchronise
+ * the device).  This entry point takes the same arguments as tq_solve_packed
+ * minus the workspace and keeps A and T in a fixed 1 MiB array inside libtq
+ * (a file-scope device array that every GPU loading the library holds until the
+ * process exits).  It calls no allocator.
+ *
+ * Limit: tq_workspace_bytes(P, B, D) must be <= 1048576 (for D = 128 that is
+ * P*B <= 1024 queries); larger calls return TQ_ERR_WORKSPACE and launch nothing.
+ * The first call on each device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  Nothing in the array needs to start at zero (the transform writes
+ * all of A and T before scoring reads them).  All calls on one device share the
+ * array: calls that may overlap on the GPU (other streams, other host threads)
+ * race on it and must be serialised by the caller.
+ * ---------------------------------------------------------------------- */
+tq_status tq_solve_packed_noalloc(const void* Q, tq_qtype qtype, const uint8_t* idx_plane,
+                                  const uint8_t* sign_plane, const uint16_t* gamma_f16,
+                                  const float* Pi, const float* S_mat, const float* codebook,
+                                  float* scores, int P, int H, int B, int S, int D, int idx_bits,
+                                  tq_path path, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

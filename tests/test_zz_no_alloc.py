@@ -1,0 +1,76 @@
+"""tq_solve_packed_noalloc, the entry point for callers that cannot allocate device
+memory (engine plugins handed only their input and output buffers, services that
+reserve all device memory up front).  It keeps A and T in a fixed array inside the
+library instead of a caller workspace.
+
+Checked through the C ABI against tq_solve_packed (the workspace entry point) on two
+calls in a row with different shapes, so the second call runs on scratch that still
+holds the first call's data; plus the size limit.  This file is collected last so that
+a run stopping at its first failure has already run every other test."""
+import ctypes
+
+import numpy as np
+import pytest
+
+from cases import Case
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+TQ_ERR_WORKSPACE = 4
+
+
+@pytest.fixture(scope="module")
+def tq():
+    from compressed_kv_cache_gb300 import build as tqbuild
+    tqbuild.build()
+    from compressed_kv_cache_gb300 import tq as mod
+    assert torch.cuda.is_available()
+    return mod
+
+
+def _dev(x):
+    return torch.from_numpy(np.ascontiguousarray(x)).cuda()
+
+
+def _run_both(tq, c):
+    ip, sp = c.packed()
+    Q, idx, sg = _dev(c.Q), _dev(ip), _dev(sp)
+    gamma = _dev(c.gamma.astype(np.float16))
+    Pi, Sm, cb = _dev(c.Pi), _dev(c.S_mat), _dev(c.cb)
+    stream = torch.cuda.current_stream().cuda_stream
+    out_new = torch.full((c.P, c.B, c.S), float("nan"), device="cuda")
+    L = tq.lib()
+    st = L.tq_solve_packed_noalloc(Q.data_ptr(), 0, idx.data_ptr(), sg.data_ptr(), gamma.data_ptr(),
+                                   Pi.data_ptr(), Sm.data_ptr(), cb.data_ptr(), out_new.data_ptr(),
+                                   c.P, c.H, c.B, c.S, c.D, c.bits, 1, stream)
+    assert st == 0, tq.status_string(st)
+    out_ref = torch.empty_like(out_new)
+    ws = torch.empty(tq.workspace_bytes(c.P, c.B, c.D), dtype=torch.uint8, device="cuda")
+    st = L.tq_solve_packed(Q.data_ptr(), 0, idx.data_ptr(), sg.data_ptr(), gamma.data_ptr(),
+                           Pi.data_ptr(), Sm.data_ptr(), cb.data_ptr(), out_ref.data_ptr(),
+                           c.P, c.H, c.B, c.S, c.D, c.bits, ctypes.c_void_p(ws.data_ptr()), ws.numel(),
+                           1, stream)
+    assert st == 0, tq.status_string(st)
+    torch.cuda.synchronize()
+    return out_new.cpu().numpy().astype(np.float64), out_ref.cpu().numpy().astype(np.float64)
+
+
+def test_noalloc_matches_workspace_entry_on_two_calls(tq):
+    # first call: one problem, one query; second call: more problems and queries, so the
+    # scratch it reuses still holds the first call's A and T
+    for case in (Case(1, 1, 1, 4096, 128, 2, seed=61, random_codebook=True),
+                 Case(6, 3, 4, 1000, 128, 3, seed=62, random_codebook=True)):
+        new, ref = _run_both(tq, case)
+        assert np.isfinite(new).all()
+        err = np.abs(new - ref)
+        assert (err <= 1e-5 * (1.0 + np.abs(ref))).all(), err.max()
+
+
+def test_noalloc_rejects_work_beyond_the_fixed_scratch(tq):
+    L = tq.lib()
+    f = 0x100000     # never dereferenced: the size check comes first
+    # A and T for 8 x 128 queries of D = 128 need 2 x 512 KiB + 1 byte more than 1 MiB
+    st = L.tq_solve_packed_noalloc(f, 0, f, f, f, f, f, f, f, 8, 8, 129, 64, 128, 2, 1, None)
+    assert st == TQ_ERR_WORKSPACE
+    assert tq.workspace_bytes(8, 129, 128) > 1 << 20 >= tq.workspace_bytes(8, 128, 128)

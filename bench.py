@@ -4,19 +4,23 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config c1] [--path auto]
     python bench.py --impl reference ...      # the CPU oracle on the host cores
 
-One step = one pass of the whole hot path over one workload: the query
-transform A = Pi q, T = S_mat q for every query, then every raw score read from
-the compressed cache.  Inputs are synthetic (the ``synth`` draws), compressed on
-the GPU by libtq's own compressor before timing starts; nothing on the timed
-path touches the CPU oracle.  Prints one JSON line (rank 0).
+One step = one pass of the whole hot path over one workload through the fused
+public entry (tq_solve / tq_solve_packed): the query transform A = Pi q,
+T = S_mat q for every query, then every raw score read from the compressed
+cache.  Inputs are synthetic (the ``synth`` draws), compressed on the GPU by
+libtq's own compressor before timing starts; nothing on the timed path touches
+the CPU oracle.  Prints one JSON line (rank 0).
 
-Timing: each step is one replay of a CUDA graph holding the step's two kernels;
-steps rotate over enough independent input/output copies that their union is
-more than twice the L2, so every step reads its cache from HBM.  The scoring
-kernel's own duration is taken with CUDA events recorded inside those graphs
-on the launching stream.  Under torchrun every rank runs its own replica of the
-workload (weak scaling, no data-path collective); the timed region is bracketed
-by a barrier and the max over ranks is reported.
+Timing: the timed region replays CUDA graphs that hold 8 consecutive steps each
+(one graph per step for a remainder), exactly K steps, bracketed by CUDA events
+on the launching stream.  Steps rotate over enough independent input/output
+copies that their union is more than twice the L2, so every step reads its
+cache from HBM.  The roofline's kernel time is the mean of back-to-back
+launches of the dominant kernel (the scoring kernel, or the single fused
+kernel when the step is one launch) over the same copies.  Under torchrun every
+rank runs its own replica of the workload (weak scaling, no data-path
+collective); the timed region is bracketed by a barrier and the max over ranks
+is reported.
 """
 from __future__ import annotations
 
@@ -73,6 +77,11 @@ def score_kernel_bytes(w) -> int:
     """Algorithmic bytes of one scoring launch: the compressed cache once, the
     scores once, A and T once, the codebook."""
     return (w.P * w.S * key_bytes(w) + 4 * w.P * w.B * w.S + 2 * 4 * w.P * w.B * w.D + 4 * w.C)
+
+
+def fused_kernel_extra_bytes(w) -> int:
+    """Inputs the single fused kernel also reads once: the queries and Pi, S_mat."""
+    return w.P * w.B * w.D * (2 if w.q_dtype == "bf16" else 4) + 2 * 4 * w.H * w.D * w.D - 8 * w.P * w.B * w.D
 
 
 def step_input_bytes(w) -> int:
@@ -276,52 +285,58 @@ def main():
     path = args.path if args.path != "auto" else tq.auto_path(w.B, w.D)
     Q0, Pi, S_mat, cb, cache0 = build_device_workload(w, tq, torch, dev)
 
-    # rotating copies: their union exceeds twice the L2 so that every step reads HBM
+    # rotating copies: their union exceeds twice the L2 so that every step reads HBM;
+    # R is a multiple of G, the number of consecutive steps one timed graph holds
+    G = 8
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     per_copy = score_kernel_bytes(w)
     R = max(1, math.ceil(2.2 * l2 / per_copy))
     R = min(R, max(1, int(40e9 // per_copy)))
+    R = math.ceil(R / G) * G if R > 1 else 1
     copies = []
     for r in range(R):
         c = {k: v.clone() for k, v in cache0.items()}
         copies.append({
             "Q": Q0.clone(), "cache": c,
             "A": torch.empty((w.P, w.B, w.D), device=dev), "T": torch.empty((w.P, w.B, w.D), device=dev),
+            "ws": torch.empty(tq.workspace_bytes(w.P, w.B, w.D), dtype=torch.uint8, device=dev),
             "out": torch.empty((w.P, w.B, w.S), device=dev)})
 
     stream = torch.cuda.Stream(dev)
-    try:
-        torch.cuda.Event(enable_timing=True, external=True)
-        ext = True
-    except TypeError:
-        ext = False
+    fused_single = (w.layout == "packed" and path == "fp32" and w.D == 128 and w.B <= 8)
 
-    def step(cp, evs=None):
-        tq.prepare_queries(cp["Q"], Pi, S_mat, out=(cp["A"], cp["T"]))
-        if evs:
-            evs[0].record()
-        score_call(tq, w, path, cp["A"], cp["T"], cp["cache"], cb, cp["out"])
-        if evs:
-            evs[1].record()
+    def solve_call(cp):
+        # one step = the fused public entry over the whole workload
+        if w.layout == "unpacked":
+            tq.solve(cp["Q"], cp["cache"]["idx"], cp["cache"]["signs"], cp["cache"]["gamma"], Pi, S_mat, cb,
+                     path=path, workspace=cp["ws"], out=cp["out"])
+        else:
+            tq.solve_packed(cp["Q"], cp["cache"]["idx"], cp["cache"]["signs"], cp["cache"]["gamma"], Pi, S_mat,
+                            cb, w.mse_bits, path=path, workspace=cp["ws"], out=cp["out"])
 
     with torch.cuda.stream(stream):
         for cp in copies:          # eager pass over every copy before capture
-            step(cp)
+            solve_call(cp)
     torch.cuda.synchronize(dev)
-    graphs, kevents = [], []
+    single, chunk = [], []
     for cp in copies:
         g = torch.cuda.CUDAGraph()
-        evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)] if ext else None
         with torch.cuda.graph(g, stream=stream):
-            step(cp, evs)
-        graphs.append(g)
-        kevents.append(evs)
+            solve_call(cp)
+        single.append(g)
+    nG = G if R >= G else 1
+    for b in range(R // nG):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for j in range(nG):
+                solve_call(copies[b * nG + j])
+        chunk.append(g)
     torch.cuda.synchronize(dev)
 
     clocks = ClockSampler(local)
     with torch.cuda.stream(stream):
-        for k in range(args.warmup):
-            graphs[k % R].replay()
+        for k in range(args.warmup):          # the least recently used copies are the first timed ones
+            single[(R - 1 - k) % R].replay()
     torch.cuda.synchronize(dev)
     if dist:
         dist.barrier()
@@ -330,8 +345,14 @@ def main():
     t_wall0 = time.time()
     with torch.cuda.stream(stream):
         start.record()
-        for k in range(args.steps):
-            graphs[(args.warmup + k) % R].replay()
+        k = 0
+        while k < args.steps:                 # exactly K steps; step k uses copy k mod R
+            if k % nG == 0 and k + nG <= args.steps:
+                chunk[(k % R) // nG].replay()
+                k += nG
+            else:
+                single[k % R].replay()
+                k += 1
         end.record()
     torch.cuda.synchronize(dev)
     t_wall1 = time.time()
@@ -344,21 +365,21 @@ def main():
         elapsed_ms = float(t.item())
     clk = clocks.stop((t_wall0, t_wall1))
 
-    # Scoring-kernel duration, two ways, both with CUDA events on the launching stream:
-    # (a) events recorded inside the step graphs around the scoring launch (includes
-    #     the event nodes' own cost); (b) the sustained average of one graph holding
-    #     R back-to-back scoring launches over the rotating copies (launch gaps
-    #     included, event cost amortised).  The roofline uses (b).
-    inside_ms = None
-    if ext:
-        used = sorted({(args.warmup + k) % R for k in range(args.steps)})
-        inside_ms = statistics.mean(kevents[i][0].elapsed_time(kevents[i][1]) for i in used)
+    # Dominant-kernel duration: the mean of back-to-back launches in one graph over the
+    # rotating copies (CUDA events on the launching stream, launch gaps included).
     gk = torch.cuda.CUDAGraph()
     reps = max(R, 16)
+    with torch.cuda.stream(stream):      # A, T of every copy for the scoring-only launches
+        for cp in copies:
+            tq.prepare_queries(cp["Q"], Pi, S_mat, out=(cp["A"], cp["T"]))
+    torch.cuda.synchronize(dev)
     with torch.cuda.graph(gk, stream=stream):
         for k in range(reps):
             cp = copies[k % R]
-            score_call(tq, w, path, cp["A"], cp["T"], cp["cache"], cb, cp["out"])
+            if fused_single:      # the step is this one kernel (transform + scoring)
+                solve_call(cp)
+            else:
+                score_call(tq, w, path, cp["A"], cp["T"], cp["cache"], cb, cp["out"])
     with torch.cuda.stream(stream):
         gk.replay()
     torch.cuda.synchronize(dev)
@@ -370,14 +391,13 @@ def main():
         ke.record()
     torch.cuda.synchronize(dev)
     kernel_ms = ks.elapsed_time(ke) / (3 * reps)
-    ktiming = (f"mean of {3 * reps} back-to-back scoring launches in one graph over the {R} rotating copies "
-               f"(CUDA events on the launching stream); in-step events: "
-               f"{'%.4f ms' % inside_ms if inside_ms is not None else 'n/a'}")
+    ktiming = (f"mean of {3 * reps} back-to-back launches in one graph over the {R} rotating copies "
+               f"(CUDA events on the launching stream)")
 
     scores_per_step = w.P * w.B * w.S
     value = world * scores_per_step * args.steps / (elapsed_ms / 1e3)
     peak, peak_src = hbm_peak()
-    kbytes = score_kernel_bytes(w)
+    kbytes = score_kernel_bytes(w) + (fused_kernel_extra_bytes(w) if fused_single else 0)
     achieved = kbytes / (kernel_ms / 1e3) / 1e9
     fp = kernel_fingerprint()
     traffic = NCU_TRAFFIC.get((args.config, path, fp))
@@ -450,13 +470,12 @@ def main():
         "hbm_gbs": achieved,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "scoring kernel", "kernel_ms": kernel_ms, "bytes_per_launch": kbytes,
+                     "kernel": "fused transform+scoring kernel" if fused_single else "scoring kernel", "kernel_ms": kernel_ms, "bytes_per_launch": kbytes,
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback 6.8 TB/s",
                      "timing": ktiming, "kernel_fingerprint": fp},
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": 2 * args.steps,
-        "kernel_ms_in_step": inside_ms,
+        "gpu_launches": (1 if fused_single else 2) * args.steps,
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)

@@ -196,6 +196,10 @@ tq_status tq_solve_packed(const void* Q, tq_qtype qtype, const uint8_t* idx_plan
   if ((st = check_packed(A, T, idx_plane, sign_plane, gamma_f16, codebook, scores, P, B, S, D,
                          idx_bits, path, &p)) != TQ_OK)
     return st;
+  if (p == TQ_PATH_FP32 && tq::fused_packed_supported(B, D))   // one kernel, workspace untouched
+    return from_cuda(tq::launch_solve_packed_fused(Q, qtype, Pi, S_mat, H, idx_plane, sign_plane,
+                                                   gamma_f16, codebook, scores, P, B, S,
+                                                   idx_bits, stream));
   if ((st = from_cuda(tq::launch_prepare(Q, qtype, Pi, S_mat, A, T, P, H, B, D, stream))) != TQ_OK)
     return st;
   return run_packed(A, T, idx_plane, sign_plane, gamma_f16, codebook, scores, P, B, S, D, idx_bits,

@@ -31,6 +31,14 @@ cudaError_t launch_scores_packed_fp32(const float* A, const float* T, const uint
                                       const float* codebook, float* scores, int P, int B, int S,
                                       int D, int idx_bits, cudaStream_t st);
 
+// Fused query transform + packed fp32 scoring (one kernel), D == 128 and B <= 8.
+bool fused_packed_supported(int B, int D);
+cudaError_t launch_solve_packed_fused(const void* Q, tq_qtype qtype, const float* Pi,
+                                      const float* S_mat, int H, const uint8_t* idx_plane,
+                                      const uint8_t* sign_plane, const uint16_t* gamma_f16,
+                                      const float* codebook, float* scores, int P, int B, int S,
+                                      int idx_bits, cudaStream_t st);
+
 // bf16 tensor-core path (D == 128). `packed` selects the cache layout; for the
 // unpacked layout idx_bits is ignored and C is the codebook size.
 bool mma_path_available();

@@ -16,13 +16,20 @@
 // no-swizzle canonical layout: 8-row x 16-byte core matrices, row groups 128 B
 // apart (SBO), K-adjacent core matrices one row-group column apart (LBO).
 //
-// Pipeline of one persistent CTA (256 threads): key tiles t0, t1, ... of one
-// (problem, query tile); for tile i all threads dequantise into smem buffer
-// i%2, one thread issues the 16 MMAs into TMEM stage i%2 and commits them to
-// mbarrier i%2, then all threads run the epilogue of tile i-1 (TMEM -> fp32 ->
-// coalesced global stores) while the tensor core works on tile i.  Every wait
-// on an mbarrier is bounded; a wait that runs out writes NaN scores for its
-// tile, stops the CTA early and still releases TMEM.
+// One persistent CTA per SM, warp-specialised, 17 warps:
+//   warps 0-7   producers: thread = (key row, half); load the next tile's rows into
+//               registers, wait for a free shared-memory stage, dequantise into it,
+//               arrive on x_full;
+//   warps 8-15  epilogue: two warps per TMEM lane quarter (each drains half of the N
+//               columns); wait for a full accumulator stage, tcgen05.ld, apply
+//               gamma, coalesced global stores, arrive on acc_empty;
+//   warp 16     MMA: allocates TMEM; one lane waits for x_full and acc_empty, issues
+//               the 16 MMAs of a tile and commits them to x_empty and acc_full.
+// Two shared-memory stages and two TMEM accumulator stages, so dequantisation of tile
+// i+1, the MMAs of tile i and the stores of tile i-1 run at the same time.  Every wait
+// on an mbarrier is bounded; a wait that runs out raises a CTA-wide abort flag, every
+// role leaves its loop (the epilogue writes NaN for a tile it could not drain), and
+// TMEM is still released.
 #include <atomic>
 
 #include "tq_internal.cuh"
@@ -32,7 +39,10 @@ namespace {
 
 constexpr int kM = 128;                 // keys per tile
 constexpr int kK = 256;                 // 2D
-constexpr int kThreads = 256;
+constexpr int kProducerThreads = 256;   // warps 0-7
+constexpr int kEpilogueThreads = 256;   // warps 8-15
+constexpr int kMmaWarp = 16;
+constexpr int kThreads = kProducerThreads + kEpilogueThreads + 32;
 constexpr int kMaxN = 128;              // queries per tile
 constexpr int kXBytes = kM * kK * 2;    // 64 KB per key-tile buffer
 constexpr uint32_t kWaitPolls = 1u << 22;
@@ -57,11 +67,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
-}
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kWaitPolls; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
-  return false;
 }
 
 // ---- tcgen05 ---------------------------------------------------------------
@@ -146,14 +151,13 @@ struct Params {
 };
 
 // Raw bytes of one key row held in registers between the load and the dequantisation,
-// so that the next tile's loads are in flight while the current tile is drained.
-// Thread t: row r = t % 128, half t / 128 (0: the code row and gamma, 1: the sign row).
+// so that the next tile's loads are in flight while the producer waits for a stage.
+// Producer thread t: row r = t % 128, half t / 128 (0: the code row, 1: the sign row).
 template <int LAYOUT>
 struct RawRow {
   static constexpr int kBits = LAYOUT >= kPacked1 ? LAYOUT - kPacked1 + 1 : 8;
   static constexpr int kVec = LAYOUT >= kPacked1 ? kBits : 8;   // uint4 per code row
   uint4 v[kVec];
-  float g;
   bool valid;
 };
 
@@ -171,7 +175,6 @@ __device__ __forceinline__ void load_row(const Params& prm, int p, int kt, RawRo
       const uint4* src = reinterpret_cast<const uint4*>(prm.idx + key * (16 * kBits));
 #pragma unroll
       for (int i = 0; i < kBits; ++i) raw.v[i] = __ldg(src + i);
-      raw.g = __half2float(__ushort_as_half(__ldg(static_cast<const uint16_t*>(prm.gamma) + key)));
     } else {
       raw.v[0] = __ldg(reinterpret_cast<const uint4*>(prm.signs + key * 16));
     }
@@ -179,7 +182,6 @@ __device__ __forceinline__ void load_row(const Params& prm, int p, int kt, RawRo
     const uint4* src = reinterpret_cast<const uint4*>((half == 0 ? prm.idx : prm.signs) + key * 128);
 #pragma unroll
     for (int i = 0; i < 8; ++i) raw.v[i] = __ldg(src + i);
-    if (half == 0) raw.g = __ldg(static_cast<const float*>(prm.gamma) + key);
   }
 }
 
@@ -188,7 +190,7 @@ __device__ __forceinline__ void load_row(const Params& prm, int p, int kt, RawRo
 template <int LAYOUT>
 __device__ __forceinline__ void store_row(const Params& prm, const RawRow<LAYOUT>& raw,
                                           uint32_t xbuf, const uint32_t* lut,
-                                          const uint16_t* cbf, float* gam) {
+                                          const uint16_t* cbf) {
   constexpr int kBits = RawRow<LAYOUT>::kBits;
   const int r = threadIdx.x & (kM - 1);
   const int half = threadIdx.x >> 7;
@@ -196,7 +198,6 @@ __device__ __forceinline__ void store_row(const Params& prm, const RawRow<LAYOUT
   if (!raw.valid) {
 #pragma unroll
     for (int kc = 0; kc < 16; ++kc) st_shared_v4(rowbase + kc * 2048, 0, 0, 0, 0);
-    if (half == 0) gam[r] = 0.f;
     return;
   }
   if (half == 0) {
@@ -240,7 +241,6 @@ __device__ __forceinline__ void store_row(const Params& prm, const RawRow<LAYOUT
         }
       }
     }
-    gam[r] = raw.g;
   } else {
     if constexpr (LAYOUT >= kPacked1) {
       const uint32_t ws[4] = {~raw.v[0].x, ~raw.v[0].y, ~raw.v[0].z, ~raw.v[0].w};  // 1 = sigma -1
@@ -269,29 +269,47 @@ __device__ __forceinline__ void store_row(const Params& prm, const RawRow<LAYOUT
   }
 }
 
+// Bounded wait that also gives up once another role has raised the abort flag.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  for (uint32_t i = 0; i < kWaitPolls; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 255u && *abort_flag) return false;
+  }
+  *abort_flag = 1;
+  return false;
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(bar) : "memory");
+}
+
 template <int LAYOUT>
 __global__ void __launch_bounds__(kThreads, 1) scores_mma_kernel(Params prm) {
   extern __shared__ __align__(1024) uint8_t smem[];
-  // [X0 64K][X1 64K][Y NT*512][lut 256 words][cbf 256 halves][gam 2x128][mbar 2][tmem slot]
+  // [X0 64K][X1 64K][Y NT*512][lut 256 words][cbf 256 halves][8 mbarriers][tmem slot]
   uint8_t* X = smem;
   uint8_t* Yp = X + 2 * kXBytes;
   uint32_t* lut = reinterpret_cast<uint32_t*>(Yp + prm.NT * kK * 2);
   uint16_t* cbf = reinterpret_cast<uint16_t*>(lut + 256);
-  float* gam = reinterpret_cast<float*>(cbf + 256);
-  uint64_t* mbar = reinterpret_cast<uint64_t*>(gam + 2 * kM);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + 2);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(cbf + 256);   // x_full[2], x_empty[2], acc_full[2], acc_empty[2]
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 8);
   __shared__ int abort_flag;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int p = blockIdx.z;
   const int q0 = blockIdx.y * prm.NT;
   const int NT = prm.NT;
+  const uint32_t x_full = smem_u32(bars), x_empty = smem_u32(bars + 2);
+  const uint32_t acc_full = smem_u32(bars + 4), acc_empty = smem_u32(bars + 6);
 
   // --- set-up: TMEM, barriers, tables, the query operand ---
-  if (warp == 0) tmem_alloc(smem_u32(tslot), prm.tmem_cols);
+  if (warp == kMmaWarp) tmem_alloc(smem_u32(tslot), prm.tmem_cols);
   if (tid == 0) {
-    mbar_init(smem_u32(mbar), 1);
-    mbar_init(smem_u32(mbar + 1), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(x_full + 8 * b, kProducerThreads);
+      mbar_init(x_empty + 8 * b, 1);
+      mbar_init(acc_full + 8 * b, 1);
+      mbar_init(acc_empty + 8 * b, kEpilogueThreads);
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     abort_flag = 0;
   }
@@ -327,78 +345,102 @@ __global__ void __launch_bounds__(kThreads, 1) scores_mma_kernel(Params prm) {
       st_shared_v4(ybase + (kc * ngroups + (n >> 3)) * 128 + (n & 7) * 16, o[0], o[1], o[2], o[3]);
     }
   }
+  fence_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
-
   const uint32_t xaddr0 = smem_u32(X);
-  const uint32_t yaddr = smem_u32(Yp);
-  const uint32_t idesc = idesc_bf16(kM, NT);
-  const uint32_t ylbo = (NT / 8) * 128;
-  const int lg = warp & 3;           // TMEM lane group of this warp
-  const int colhalf = warp >> 2;     // which half of the N columns this warp drains
+  volatile int* abort_v = &abort_flag;
 
-  auto epilogue = [&](int kt, int stage, uint32_t parity) {
-    const bool ok = mbar_wait_bounded(smem_u32(mbar + stage), parity);
-    tc_fence_after();
+  if (warp < kProducerThreads / 32) {
+    // ------------------------------ producers ------------------------------
+    RawRow<LAYOUT> raw;
+    int i = 0;
+    if (static_cast<int>(blockIdx.x) < prm.key_tiles) load_row<LAYOUT>(prm, p, blockIdx.x, raw);
+    for (int kt = blockIdx.x; kt < prm.key_tiles; kt += gridDim.x, ++i) {
+      const int st = i & 1;
+      if (!wait_or_abort(x_empty + 8 * st, ((i >> 1) & 1) ^ 1, abort_v)) break;
+      store_row<LAYOUT>(prm, raw, xaddr0 + st * kXBytes, lut, cbf);
+      fence_async_smem();
+      mbar_arrive(x_full + 8 * st);
+      if (kt + static_cast<int>(gridDim.x) < prm.key_tiles) load_row<LAYOUT>(prm, p, kt + gridDim.x, raw);
+    }
+  } else if (warp < (kProducerThreads + kEpilogueThreads) / 32) {
+    // ------------------------------ epilogue -------------------------------
+    const int e = warp - kProducerThreads / 32;      // 0..7
+    const int lg = warp & 3;                         // TMEM lane quarter this warp may read
+    const int colhalf = e >> 2;
     const int r = lg * 32 + lane;
-    const int s = kt * kM + r;
-    const float kg = prm.kappa * gam[stage * kM + r];
-    const uint32_t trow = tmem + (static_cast<uint32_t>(lg * 32) << 16) + stage * 2 * NT;
     const int half_n = NT / 2;
-    for (int c = colhalf * half_n; c < (colhalf + 1) * half_n; c += 8) {
-      uint32_t m[8], q[8];
-      tmem_ld8(trow + c, m);
-      tmem_ld8(trow + NT + c, q);
-      tmem_ld_wait();
+    int i = 0;
+    for (int kt = blockIdx.x; kt < prm.key_tiles; kt += gridDim.x, ++i) {
+      const int as = i & 1;
+      const int s = kt * kM + r;
+      float g = 0.f;
+      if (s < prm.S) {
+        const size_t key = static_cast<size_t>(p) * prm.S + s;
+        g = LAYOUT >= kPacked1
+                ? __half2float(__ushort_as_half(__ldg(static_cast<const uint16_t*>(prm.gamma) + key)))
+                : __ldg(static_cast<const float*>(prm.gamma) + key);
+      }
+      const float kg = prm.kappa * g;
+      // tcgen05.ld is warp-collective: the whole warp takes the same branch
+      const bool ok = __all_sync(0xffffffffu, wait_or_abort(acc_full + 8 * as, (i >> 1) & 1, abort_v));
+      tc_fence_after();
+      const uint32_t trow = tmem + (static_cast<uint32_t>(lg * 32) << 16) + as * 2 * NT;
+      float* out = prm.scores + (static_cast<size_t>(p) * prm.B + q0) * prm.S + s;
+      for (int c = colhalf * half_n; c < (colhalf + 1) * half_n; c += 8) {
+        uint32_t m[8], q[8];
+        if (ok) {
+          tmem_ld8(trow + c, m);
+          tmem_ld8(trow + NT + c, q);
+          tmem_ld_wait();
+        }
+        if (s < prm.S) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int b = q0 + c + j;
-        if (s < prm.S && b < prm.B) {
-          const float v = ok ? fmaf(kg, __uint_as_float(q[j]), __uint_as_float(m[j])) : __int_as_float(0x7fc00000);
-          prm.scores[(static_cast<size_t>(p) * prm.B + b) * prm.S + s] = v;
+          for (int j = 0; j < 8; ++j) {
+            if (q0 + c + j < prm.B) {
+              out[static_cast<size_t>(c + j) * prm.S] =
+                  ok ? fmaf(kg, __uint_as_float(q[j]), __uint_as_float(m[j])) : __int_as_float(0x7fc00000);
+            }
+          }
         }
       }
+      if (!ok) break;
+      tc_fence_before();
+      mbar_arrive(acc_empty + 8 * as);
     }
-    if (!ok) abort_flag = 1;
-    tc_fence_before();
-  };
-
-  int i = 0;
-  int prev_kt = -1;
-  RawRow<LAYOUT> raw;
-  if (static_cast<int>(blockIdx.x) < prm.key_tiles) load_row<LAYOUT>(prm, p, blockIdx.x, raw);
-  for (int kt = blockIdx.x; kt < prm.key_tiles; kt += gridDim.x, ++i) {
-    const int stage = i & 1;
-    const uint32_t xbuf = xaddr0 + stage * kXBytes;
-    store_row<LAYOUT>(prm, raw, xbuf, lut, cbf, gam + stage * kM);
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    if (abort_flag) break;
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t dm = tmem + stage * 2 * NT;
+  } else {
+    // -------------------------------- MMA ----------------------------------
+    if (lane == 0) {
+      const uint32_t yaddr = smem_u32(Yp);
+      const uint32_t idesc = idesc_bf16(kM, NT);
+      const uint32_t ylbo = (NT / 8) * 128;
+      int i = 0;
+      for (int kt = blockIdx.x; kt < prm.key_tiles; kt += gridDim.x, ++i) {
+        const int st = i & 1;
+        if (!wait_or_abort(x_full + 8 * st, (i >> 1) & 1, abort_v)) break;
+        if (!wait_or_abort(acc_empty + 8 * st, ((i >> 1) & 1) ^ 1, abort_v)) break;
+        tc_fence_after();
+        const uint32_t xbuf = xaddr0 + st * kXBytes;
+        const uint32_t dm = tmem + st * 2 * NT;
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const uint64_t ad = smem_desc(xbuf + k * 2 * 2048, 2048, 128);
-        const uint64_t bd = smem_desc(yaddr + k * 2 * ylbo, ylbo, 128);
-        mma_bf16(k < 8 ? dm : dm + NT, ad, bd, idesc, (k & 7) != 0);
+        for (int k = 0; k < 16; ++k) {
+          const uint64_t ad = smem_desc(xbuf + k * 2 * 2048, 2048, 128);
+          const uint64_t bd = smem_desc(yaddr + k * 2 * ylbo, ylbo, 128);
+          mma_bf16(k < 8 ? dm : dm + NT, ad, bd, idesc, (k & 7) != 0);
+        }
+        mma_commit(x_empty + 8 * st);
+        mma_commit(acc_full + 8 * st);
       }
-      mma_commit(smem_u32(mbar + stage));
     }
-    // the next tile's rows are in flight while this thread drains the previous tile
-    if (kt + static_cast<int>(gridDim.x) < prm.key_tiles) load_row<LAYOUT>(prm, p, kt + gridDim.x, raw);
-    if (prev_kt >= 0) epilogue(prev_kt, stage ^ 1, ((i - 1) >> 1) & 1);
-    prev_kt = kt;
+    __syncwarp();
   }
-  __syncthreads();
-  if (prev_kt >= 0 && !abort_flag) epilogue(prev_kt, (i - 1) & 1, ((i - 1) >> 1) & 1);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 0) tmem_dealloc(tmem, prm.tmem_cols);
+  if (warp == kMmaWarp) tmem_dealloc(tmem, prm.tmem_cols);
 }
 
 template <int LAYOUT>
@@ -409,7 +451,7 @@ cudaError_t launch_layout(const Params& prm, int P, int qtiles, cudaStream_t st)
   // kernel builds addresses memory it owns.
   static std::atomic<int> dyn_bytes[64];
   constexpr size_t need = 2 * kXBytes + static_cast<size_t>(kMaxN) * kK * 2 + 256 * 4 + 256 * 2 +
-                          2 * kM * 4 + 2 * 8 + 16;
+                          8 * 8 + 16;
   int dev = 0, sms = 148;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;

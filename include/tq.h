@@ -126,7 +126,8 @@ tq_status tq_scores_packed(const float* A, const float* T, const uint8_t* idx_pl
  * passes `workspace`, a device buffer of at least tq_workspace_bytes(P, B, D)
  * bytes that holds A and T between the two steps; it is scratch, its contents
  * on return are unspecified, and calls that may run concurrently must not
- * share it.
+ * share it.  (tq_solve_packed on the fp32 path with B <= 8 and D = 128 runs the
+ * transform inside its single scoring kernel and leaves the workspace untouched.)
  * ---------------------------------------------------------------------- */
 size_t tq_workspace_bytes(int P, int B, int D);
 

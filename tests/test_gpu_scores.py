@@ -130,9 +130,10 @@ def test_scores_packed_fp32(tq, bits, D, B):
     A, T = tq.prepare_queries(Qt, dev(c.Pi), dev(c.S_mat))
     out = tq.scores_packed(A, T, dev(ip), dev(sp), f16(c.gamma), dev(c.cb), bits, path="fp32").cpu().numpy()
     assert_fp32(out, c.expected())
+    # the fused entry (for B <= 8 at D = 128 a single kernel that also does the transform)
     fused = tq.solve_packed(Qt, dev(ip), dev(sp), f16(c.gamma), dev(c.Pi), dev(c.S_mat), dev(c.cb), bits,
                             path="fp32").cpu().numpy()
-    np.testing.assert_array_equal(fused, out)
+    assert_fp32(fused, c.expected())
 
 
 # ---------------------------------------------------------------------------

@@ -57,10 +57,11 @@ def _run_both(tq, c):
 
 
 def test_noalloc_matches_workspace_entry_on_two_calls(tq):
-    # first call: one problem, one query; second call: more problems and queries, so the
-    # scratch it reuses still holds the first call's A and T
-    for case in (Case(1, 1, 1, 4096, 128, 2, seed=61, random_codebook=True),
-                 Case(6, 3, 4, 1000, 128, 3, seed=62, random_codebook=True)):
+    # B > 8 on the fp32 path: the query transform writes A and T into the fixed scratch
+    # and the scorer reads them back.  The second call has more problems and queries,
+    # and the scratch it reuses still holds the first call's A and T.
+    for case in (Case(1, 1, 12, 4096, 128, 2, seed=61, random_codebook=True),
+                 Case(6, 3, 20, 1000, 128, 3, seed=62, random_codebook=True)):
         new, ref = _run_both(tq, case)
         assert np.isfinite(new).all()
         err = np.abs(new - ref)

@@ -29,6 +29,11 @@ size_t at_bytes(int P, int B, int D) {
   return round_up(static_cast<size_t>(P) * B * D * sizeof(float), 256);
 }
 
+// Workspace: [A][T][bf16 query operand of the tensor-core path (D = 128, B >= 16 only)].
+size_t y_bytes(int P, int B, int D) {
+  return (D == 128 && B >= 16) ? round_up(tq::mma_y_bytes(P, B), 256) : 0;
+}
+
 tq_status check_prepare_sizes(int P, int H, int B, int D, tq_qtype qtype) {
   if (P < 1 || H < 1 || H > P || B < 1 || D < 1 || D > 256) return TQ_ERR_INVALID_VALUE;
   if (P > kMaxGridYZ || (B + 7) / 8 > kMaxGridYZ) return TQ_ERR_INVALID_VALUE;
@@ -77,10 +82,11 @@ tq_status check_packed(const float* A, const float* T, const uint8_t* idx_plane,
 
 tq_status run_unpacked(const float* A, const float* T, const uint8_t* K_idx, const int8_t* signs,
                        const float* gamma, const float* codebook, float* scores, int P, int B,
-                       int S, int D, int C, tq_path path, cudaStream_t stream) {
+                       int S, int D, int C, tq_path path, cudaStream_t stream,
+                       bool after_prepare = false, const uint16_t* Ybf = nullptr) {
   if (path == TQ_PATH_BF16_MMA)
     return from_cuda(tq::launch_scores_mma(A, T, K_idx, signs, gamma, codebook, scores, P, B, S,
-                                           C, 0, false, stream));
+                                           C, 0, false, after_prepare, stream, Ybf));
   return from_cuda(tq::launch_scores_unpacked_fp32(A, T, K_idx, signs, gamma, codebook, scores,
                                                    P, B, S, D, C, stream));
 }
@@ -88,11 +94,11 @@ tq_status run_unpacked(const float* A, const float* T, const uint8_t* K_idx, con
 tq_status run_packed(const float* A, const float* T, const uint8_t* idx_plane,
                      const uint8_t* sign_plane, const uint16_t* gamma_f16, const float* codebook,
                      float* scores, int P, int B, int S, int D, int idx_bits, tq_path path,
-                     cudaStream_t stream) {
+                     cudaStream_t stream, bool after_prepare = false, const uint16_t* Ybf = nullptr) {
   if (path == TQ_PATH_BF16_MMA)
     return from_cuda(tq::launch_scores_mma(A, T, idx_plane, sign_plane, gamma_f16, codebook,
                                            scores, P, B, S, 1 << idx_bits, idx_bits, true,
-                                           stream));
+                                           after_prepare, stream, Ybf));
   return from_cuda(tq::launch_scores_packed_fp32(A, T, idx_plane, sign_plane, gamma_f16, codebook,
                                                  scores, P, B, S, D, idx_bits, stream));
 }
@@ -156,7 +162,7 @@ tq_status tq_scores_packed(const float* A, const float* T, const uint8_t* idx_pl
 
 size_t tq_workspace_bytes(int P, int B, int D) {
   if (P < 1 || B < 1 || D < 1) return 0;
-  return 2 * at_bytes(P, B, D);
+  return 2 * at_bytes(P, B, D) + y_bytes(P, B, D);
 }
 
 tq_status tq_solve(const void* Q, tq_qtype qtype, const uint8_t* K_idx, const int8_t* signs,
@@ -174,9 +180,12 @@ tq_status tq_solve(const void* Q, tq_qtype qtype, const uint8_t* K_idx, const in
   tq_path p;
   if ((st = check_unpacked(A, T, K_idx, signs, gamma, codebook, scores, P, B, S, D, C, path, &p)) != TQ_OK)
     return st;
-  if ((st = from_cuda(tq::launch_prepare(Q, qtype, Pi, S_mat, A, T, P, H, B, D, stream))) != TQ_OK)
+  uint16_t* Y = (p == TQ_PATH_BF16_MMA && y_bytes(P, B, D) > 0)
+                    ? reinterpret_cast<uint16_t*>(static_cast<char*>(workspace) + 2 * at_bytes(P, B, D))
+                    : nullptr;
+  if ((st = from_cuda(tq::launch_prepare(Q, qtype, Pi, S_mat, A, T, P, H, B, D, stream, Y))) != TQ_OK)
     return st;
-  return run_unpacked(A, T, K_idx, signs, gamma, codebook, scores, P, B, S, D, C, p, stream);
+  return run_unpacked(A, T, K_idx, signs, gamma, codebook, scores, P, B, S, D, C, p, stream, true, Y);
 }
 
 tq_status tq_solve_packed(const void* Q, tq_qtype qtype, const uint8_t* idx_plane,
@@ -200,10 +209,13 @@ tq_status tq_solve_packed(const void* Q, tq_qtype qtype, const uint8_t* idx_plan
     return from_cuda(tq::launch_solve_packed_fused(Q, qtype, Pi, S_mat, H, idx_plane, sign_plane,
                                                    gamma_f16, codebook, scores, P, B, S,
                                                    idx_bits, stream));
-  if ((st = from_cuda(tq::launch_prepare(Q, qtype, Pi, S_mat, A, T, P, H, B, D, stream))) != TQ_OK)
+  uint16_t* Y = (p == TQ_PATH_BF16_MMA && y_bytes(P, B, D) > 0)
+                    ? reinterpret_cast<uint16_t*>(static_cast<char*>(workspace) + 2 * at_bytes(P, B, D))
+                    : nullptr;
+  if ((st = from_cuda(tq::launch_prepare(Q, qtype, Pi, S_mat, A, T, P, H, B, D, stream, Y))) != TQ_OK)
     return st;
   return run_packed(A, T, idx_plane, sign_plane, gamma_f16, codebook, scores, P, B, S, D, idx_bits,
-                    p, stream);
+                    p, stream, true, Y);
 }
 
 tq_status tq_pack_indices(const uint8_t* K_idx, uint8_t* idx_plane, int64_t n_keys, int D,

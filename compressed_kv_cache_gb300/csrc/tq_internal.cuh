@@ -18,8 +18,19 @@ inline float qjl_scale(int D) { return kSqrtHalfPi / static_cast<float>(D); }
 
 // ---- launchers (return the CUDA error of the launch, cudaSuccess otherwise) ----
 
+// Query tile of the tensor-core path: NT = min(B, 128) rounded up to 16, ceil(B/NT) tiles.
+inline int mma_query_tile(int B) { const int n = B < 128 ? B : 128; return (n + 15) / 16 * 16; }
+inline int mma_query_tiles(int B) { const int nt = mma_query_tile(B); return (B + nt - 1) / nt; }
+// Bytes of the bf16 query operand of the tensor-core path for P problems (D = 128):
+// per (problem, query tile) NT rows x 256 K in the no-swizzle core-matrix layout.
+inline size_t mma_y_bytes(int P, int B) {
+  return static_cast<size_t>(P) * mma_query_tiles(B) * mma_query_tile(B) * 512;
+}
+
+// Ybf (optional, D == 128 only): also write A and T as the tensor-core query operand.
 cudaError_t launch_prepare(const void* Q, tq_qtype qtype, const float* Pi, const float* S_mat,
-                           float* A, float* T, int P, int H, int B, int D, cudaStream_t st);
+                           float* A, float* T, int P, int H, int B, int D, cudaStream_t st,
+                           uint16_t* Ybf = nullptr);
 
 cudaError_t launch_scores_unpacked_fp32(const float* A, const float* T, const uint8_t* K_idx,
                                         const int8_t* signs, const float* gamma,
@@ -40,12 +51,17 @@ cudaError_t launch_solve_packed_fused(const void* Q, tq_qtype qtype, const float
                                       int idx_bits, cudaStream_t st);
 
 // bf16 tensor-core path (D == 128). `packed` selects the cache layout; for the
-// unpacked layout idx_bits is ignored and C is the codebook size.
+// unpacked layout idx_bits is ignored and C is the codebook size.  `after_prepare`:
+// the launch directly follows this call's query transform on the same stream and may
+// start early (programmatic dependent launch); A and T are read only after the
+// transform grid has completed.  Ybf: the query operand prepared by that transform
+// (one bulk copy per CTA instead of converting A and T).
 bool mma_path_available();
 cudaError_t launch_scores_mma(const float* A, const float* T, const uint8_t* idx,
                               const void* signs, const void* gamma, const float* codebook,
                               float* scores, int P, int B, int S, int C, int idx_bits,
-                              bool packed, cudaStream_t st);
+                              bool packed, bool after_prepare, cudaStream_t st,
+                              const uint16_t* Ybf = nullptr);
 
 cudaError_t launch_pack_indices(const uint8_t* K_idx, uint8_t* plane, int64_t n, int D, int bits,
                                 cudaStream_t st);

@@ -28,8 +28,11 @@ template <typename QT>
 __global__ void __launch_bounds__(kWarps * 32)
 prepare_kernel(const QT* __restrict__ Q, const float* __restrict__ Pi,
                const float* __restrict__ Sm, float* __restrict__ A, float* __restrict__ T,
-               int H, int B, int D) {
+               int H, int B, int D, uint16_t* __restrict__ Ybf, int NT, int qtiles) {
   extern __shared__ __align__(16) float sQ[];   // [kQ][D]
+  // a scorer launched behind this grid may start its own prologue now (it reads A and T
+  // only after this grid has completed)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int b0 = blockIdx.x * kQ;
   const int p = blockIdx.y;
   const int h = p % H;
@@ -66,21 +69,33 @@ prepare_kernel(const QT* __restrict__ Q, const float* __restrict__ Pi,
     for (int q = 1; q < kQ; ++q)
       if (lane == q) v = acc[q];
     (is_t ? T : A)[qbase + static_cast<size_t>(lane) * D + d] = v;
+    if (Ybf != nullptr) {
+      // tensor-core query operand: query b, K index k = d (A) or 128 + d (T), bf16 RNE,
+      // 8-row x 16-byte core matrices (K-major, no swizzle) per (problem, query tile)
+      const int b = b0 + lane;
+      const int qt = b / NT, n = b % NT, k = (is_t ? 128 : 0) + d;
+      const size_t off = (static_cast<size_t>(p) * qtiles + qt) * NT * 256 +
+                         ((k >> 3) * (NT >> 3) + (n >> 3)) * 64 + (n & 7) * 8 + (k & 7);
+      Ybf[off] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+    }
   }
 }
 
 }  // namespace
 
 cudaError_t launch_prepare(const void* Q, tq_qtype qtype, const float* Pi, const float* S_mat,
-                           float* A, float* T, int P, int H, int B, int D, cudaStream_t st) {
+                           float* A, float* T, int P, int H, int B, int D, cudaStream_t st,
+                           uint16_t* Ybf) {
   dim3 grid(ceil_div(B, kQ), P, ceil_div(2 * D, kWarps));
   const size_t smem = static_cast<size_t>(kQ) * D * sizeof(float);
+  const int NT = mma_query_tile(B), qtiles = mma_query_tiles(B);
+  if (D != 128) Ybf = nullptr;
   if (qtype == TQ_Q_BF16) {
     prepare_kernel<__nv_bfloat16><<<grid, kWarps * 32, smem, st>>>(
-        static_cast<const __nv_bfloat16*>(Q), Pi, S_mat, A, T, H, B, D);
+        static_cast<const __nv_bfloat16*>(Q), Pi, S_mat, A, T, H, B, D, Ybf, NT, qtiles);
   } else {
     prepare_kernel<float><<<grid, kWarps * 32, smem, st>>>(static_cast<const float*>(Q), Pi,
-                                                           S_mat, A, T, H, B, D);
+                                                           S_mat, A, T, H, B, D, Ybf, NT, qtiles);
   }
   return cudaGetLastError();
 }

@@ -4,29 +4,32 @@
 // on NVIDIA's AGX Thor", zededa.com, v5 "Extended 2D": <[Pi q | S q], [c | sigma]>
 // over R^{2D}) makes a block of scores one dense contraction with K = 2D = 256:
 //
-//   X[s, 0:128]   = c[idx[s, :]]      (bf16, dequantised in shared memory)
-//   X[s, 128:256] = sigma[s, :]       (+1 / -1, exact in bf16)
+//   X[s, 0:128]   = c[idx[s, :]]                      (bf16, dequantised in shared memory)
+//   X[s, 128:256] = sigma[s, :] * bf16(kappa gamma[s])  (the sign flips a bf16 magnitude)
 //   Y[b, 0:128]   = A[b, :],  Y[b, 128:256] = T[b, :]   (bf16, round to nearest even)
-//   mse[s, b] = sum_{k<128} X Y,  res[s, b] = sum_{k>=128} X Y   (fp32, in TMEM)
-//   score[b, s] = mse[s, b] + (sqrt(pi/2)/D) gamma[s] res[s, b]   (fp32 epilogue)
+//   score[b, s]   = sum_k X[s, k] Y[b, k]               (fp32, accumulated in TMEM)
+// with kappa = sqrt(pi/2)/D.  Folding kappa*gamma into the sign operand rounds it to
+// bf16 (relative 2^-9 on the residual term), well inside the path's bound, and leaves
+// one accumulator per tile, so the epilogue only copies TMEM to memory (the HBM write of
+// the scores is what bounds this kernel).
 //
 // Tile: M = 128 keys (TMEM lanes) x N = up to 128 queries x K = 256, as 16
-// tcgen05.mma.kind::f16 instructions of K = 16 (8 into the mse accumulator,
-// 8 into the residual accumulator).  Both operands are K-major in the
+// tcgen05.mma.kind::f16 instructions of K = 16 into one fp32 accumulator.  Both operands are K-major in the
 // no-swizzle canonical layout: 8-row x 16-byte core matrices, row groups 128 B
 // apart (SBO), K-adjacent core matrices one row-group column apart (LBO).
 //
-// One persistent CTA per SM, warp-specialised, 17 warps:
+// Persistent CTAs, warp-specialised (shown for the full configuration, 25 warps):
 //   warps 0-7   producers: thread = (key row, half); load the next tile's rows into
 //               registers, wait for a free shared-memory stage, dequantise into it,
 //               arrive on x_full;
-//   warps 8-15  epilogue: two warps per TMEM lane quarter (each drains half of the N
-//               columns); wait for a full accumulator stage, tcgen05.ld, apply
-//               gamma, coalesced global stores, arrive on acc_empty;
-//   warp 16     MMA: allocates TMEM; one lane waits for x_full and acc_empty, issues
+//   warps 8-23  epilogue: four warps per TMEM lane quarter (each drains a quarter of
+//               the N columns); wait for a full accumulator stage, tcgen05.ld,
+//               coalesced global stores, arrive on acc_empty;
+//   warp 24     MMA: allocates TMEM; one lane waits for x_full and acc_empty, issues
 //               the 16 MMAs of a tile and commits them to x_empty and acc_full.
-// Two shared-memory stages and two TMEM accumulator stages, so dequantisation of tile
-// i+1, the MMAs of tile i and the stores of tile i-1 run at the same time.  Every wait
+// Two shared-memory stages and up to four TMEM accumulator stages, so dequantisation,
+// the MMAs and the draining of several tiles overlap.  The epilogue reads its columns
+// 32 at a time with one tcgen05.wait::ld per batch.  Every wait
 // on an mbarrier is bounded; a wait that runs out raises a CTA-wide abort flag, every
 // role leaves its loop (the epilogue writes NaN for a tile it could not drain), and
 // TMEM is still released.
@@ -40,9 +43,13 @@ namespace {
 constexpr int kM = 128;                 // keys per tile
 constexpr int kK = 256;                 // 2D
 constexpr int kProducerThreads = 256;   // warps 0-7
-constexpr int kEpilogueThreads = 256;   // warps 8-15
-constexpr int kMmaWarp = 16;
-constexpr int kThreads = kProducerThreads + kEpilogueThreads + 32;
+// Two configurations: "full" (16 epilogue warps, 2 shared-memory stages, one CTA per SM)
+// and "lite" (4 epilogue warps, 1 stage, two CTAs per SM) for problems with few tiles.
+template <int EPIW> struct Cfg {
+  static constexpr int kEpilogueThreads = EPIW * 32;
+  static constexpr int kMmaWarp = 8 + EPIW;
+  static constexpr int kThreads = kProducerThreads + kEpilogueThreads + 32;
+};
 constexpr int kMaxN = 128;              // queries per tile
 constexpr int kXBytes = kM * kK * 2;    // 64 KB per key-tile buffer
 constexpr uint32_t kWaitPolls = 1u << 22;
@@ -119,6 +126,11 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&v)[8]) {
                  "=r"(v[6]), "=r"(v[7])
                : "r"(taddr));
 }
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t* v) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
+               : "r"(taddr));
+}
 __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -133,9 +145,10 @@ __device__ __forceinline__ uint32_t bf16_bits(float x) {
   return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(x)));
 }
 
-// +1/-1 bf16 pair for sign bits b0 (low element) and b1 (high element), bit = 1 means +1.
-__device__ __forceinline__ uint32_t sign_pair(uint32_t neg_bits, int j) {
-  return 0x3F803F80u | (((neg_bits >> (2 * j)) & 1u) << 15) | (((neg_bits >> (2 * j + 1)) & 1u) << 31);
+// bf16 pair (+-mag, +-mag) for sign bits 2j (low element) and 2j+1 (high element) of
+// neg_bits, where a set bit means sigma = -1; mag2 holds the magnitude in both halves.
+__device__ __forceinline__ uint32_t sign_pair(uint32_t mag2, uint32_t neg_bits, int j) {
+  return mag2 | (((neg_bits >> (2 * j)) & 1u) << 15) | (((neg_bits >> (2 * j + 1)) & 1u) << 31);
 }
 
 struct Params {
@@ -145,8 +158,9 @@ struct Params {
   const uint8_t* signs;    // [P,S,D] int8 (unpacked) or [P,S,D/8] plane (packed)
   const void* gamma;       // fp32 (unpacked) or fp16 (packed) [P,S]
   const float* codebook;
+  const uint16_t* Ybf;     // query operand prepared by the transform (bulk-copied), or null
   float* scores;
-  int B, S, C, NT, key_tiles, tmem_cols;
+  int B, S, C, NT, key_tiles, tmem_cols, acc_stages;
   float kappa;
 };
 
@@ -158,6 +172,7 @@ struct RawRow {
   static constexpr int kBits = LAYOUT >= kPacked1 ? LAYOUT - kPacked1 + 1 : 8;
   static constexpr int kVec = LAYOUT >= kPacked1 ? kBits : 8;   // uint4 per code row
   uint4 v[kVec];
+  float g;       // gamma of the row (sign half only)
   bool valid;
 };
 
@@ -177,11 +192,13 @@ __device__ __forceinline__ void load_row(const Params& prm, int p, int kt, RawRo
       for (int i = 0; i < kBits; ++i) raw.v[i] = __ldg(src + i);
     } else {
       raw.v[0] = __ldg(reinterpret_cast<const uint4*>(prm.signs + key * 16));
+      raw.g = __half2float(__ushort_as_half(__ldg(static_cast<const uint16_t*>(prm.gamma) + key)));
     }
   } else {
     const uint4* src = reinterpret_cast<const uint4*>((half == 0 ? prm.idx : prm.signs) + key * 128);
 #pragma unroll
     for (int i = 0; i < 8; ++i) raw.v[i] = __ldg(src + i);
+    if (half == 1) raw.g = __ldg(static_cast<const float*>(prm.gamma) + key);
   }
 }
 
@@ -242,13 +259,15 @@ __device__ __forceinline__ void store_row(const Params& prm, const RawRow<LAYOUT
       }
     }
   } else {
+    const uint32_t mag = bf16_bits(prm.kappa * raw.g);      // kappa*gamma >= 0
+    const uint32_t mag2 = mag | (mag << 16);
     if constexpr (LAYOUT >= kPacked1) {
       const uint32_t ws[4] = {~raw.v[0].x, ~raw.v[0].y, ~raw.v[0].z, ~raw.v[0].w};  // 1 = sigma -1
 #pragma unroll
       for (int kc = 0; kc < 16; ++kc) {
         const uint32_t nb = (ws[kc >> 2] >> (8 * (kc & 3))) & 0xFFu;
-        st_shared_v4(rowbase + kc * 2048, sign_pair(nb, 0), sign_pair(nb, 1), sign_pair(nb, 2),
-                     sign_pair(nb, 3));
+        st_shared_v4(rowbase + kc * 2048, sign_pair(mag2, nb, 0), sign_pair(mag2, nb, 1),
+                     sign_pair(mag2, nb, 2), sign_pair(mag2, nb, 3));
       }
     } else {
 #pragma unroll
@@ -260,7 +279,7 @@ __device__ __forceinline__ void store_row(const Params& prm, const RawRow<LAYOUT
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const uint32_t u = ws[2 * h + (q >> 1)] >> (16 * (q & 1));   // bytes b0 (low), b1
-            o[q] = 0x3F803F80u | ((u & 0x80u) << 8) | ((u & 0x8000u) << 16);
+            o[q] = mag2 | ((u & 0x80u) << 8) | ((u & 0x8000u) << 16);
           }
           st_shared_v4(rowbase + (2 * c2 + h) * 2048, o[0], o[1], o[2], o[3]);
         }
@@ -282,16 +301,19 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(bar) : "memory");
 }
 
-template <int LAYOUT>
-__global__ void __launch_bounds__(kThreads, 1) scores_mma_kernel(Params prm) {
+template <int LAYOUT, int EPIW, int XS>
+__global__ void __launch_bounds__(Cfg<EPIW>::kThreads, (EPIW == 4 ? 2 : 1)) scores_mma_kernel(Params prm) {
+  constexpr int kEpilogueThreads = Cfg<EPIW>::kEpilogueThreads;
+  constexpr int kMmaWarp = Cfg<EPIW>::kMmaWarp;
+  constexpr int kThreads = Cfg<EPIW>::kThreads;
   extern __shared__ __align__(1024) uint8_t smem[];
-  // [X0 64K][X1 64K][Y NT*512][lut 256 words][cbf 256 halves][8 mbarriers][tmem slot]
+  // [X: XS x 64K][Y NT*512][lut 256 words][cbf 256 halves][13 mbarriers][tmem slot]
   uint8_t* X = smem;
-  uint8_t* Yp = X + 2 * kXBytes;
+  uint8_t* Yp = X + XS * kXBytes;
   uint32_t* lut = reinterpret_cast<uint32_t*>(Yp + prm.NT * kK * 2);
   uint16_t* cbf = reinterpret_cast<uint16_t*>(lut + 256);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(cbf + 256);   // x_full[2], x_empty[2], acc_full[2], acc_empty[2]
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 8);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(cbf + 256);   // x_full[2] x_empty[2] acc_full[4] acc_empty[4] y
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 13);
   __shared__ int abort_flag;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -299,24 +321,86 @@ __global__ void __launch_bounds__(kThreads, 1) scores_mma_kernel(Params prm) {
   const int q0 = blockIdx.y * prm.NT;
   const int NT = prm.NT;
   const uint32_t x_full = smem_u32(bars), x_empty = smem_u32(bars + 2);
-  const uint32_t acc_full = smem_u32(bars + 4), acc_empty = smem_u32(bars + 6);
+  const uint32_t acc_full = smem_u32(bars + 4), acc_empty = smem_u32(bars + 8);
+  const uint32_t y_bar = smem_u32(bars + 12);
+  const int AS = prm.acc_stages;
 
-  // --- set-up: TMEM, barriers, tables, the query operand ---
-  if (warp == kMmaWarp) tmem_alloc(smem_u32(tslot), prm.tmem_cols);
   if (tid == 0) {
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(x_full + 8 * b, kProducerThreads);
+    for (int b = 0; b < XS; ++b) {
+      mbar_init(x_full + 8 * b, kProducerThreads / 32);     // one arrival per producer warp
       mbar_init(x_empty + 8 * b, 1);
-      mbar_init(acc_full + 8 * b, 1);
-      mbar_init(acc_empty + 8 * b, kEpilogueThreads);
     }
+    for (int b = 0; b < 4; ++b) {
+      mbar_init(acc_full + 8 * b, 1);
+      mbar_init(acc_empty + 8 * b, kEpilogueThreads / 32);  // one arrival per epilogue warp
+    }
+    mbar_init(y_bar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     abort_flag = 0;
   }
-  const int C = prm.C;
-  for (int e = tid; e < 256; e += kThreads) {
-    cbf[e] = e < C ? static_cast<uint16_t>(bf16_bits(prm.codebook[e])) : 0;
+  // Producers request their first tiles' rows before the rest of the set-up, so the
+  // loads are in flight while TMEM and the query operand are prepared.
+  constexpr bool kTwoDeep = false;   // one tile ahead: the register budget of 800 threads
+  RawRow<LAYOUT> raw0, raw1;
+  const int gx = gridDim.x;
+  if (warp < kProducerThreads / 32) {
+    if (static_cast<int>(blockIdx.x) < prm.key_tiles) load_row<LAYOUT>(prm, p, blockIdx.x, raw0);
+    if (kTwoDeep && static_cast<int>(blockIdx.x) + gx < prm.key_tiles)
+      load_row<LAYOUT>(prm, p, blockIdx.x + gx, raw1);
   }
+
+  // --- set-up: TMEM, barriers, tables, the query operand ---
+  if (warp == kMmaWarp) tmem_alloc(smem_u32(tslot), prm.tmem_cols);
+  // When launched right behind the query transform of the same call (programmatic
+  // dependent launch), everything above ran while the transform was still going;
+  // A and T are read only after this wait, which returns once that grid is complete.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // One round trip for every global input of the set-up: each thread requests its
+  // codebook entry and its chunks of A/T, then converts and stores them.
+  const int C = prm.C;
+  const float cval = tid < C ? __ldg(prm.codebook + tid) : 0.f;
+  const uint32_t ybytes = static_cast<uint32_t>(NT) * 512u;
+  if (prm.Ybf != nullptr) {
+    // the transform already wrote this tile of the query operand: one bulk copy
+    if (tid == 0) {
+      asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(y_bar),
+                   "r"(ybytes)
+                   : "memory");
+      const uint16_t* src = prm.Ybf + (static_cast<size_t>(p) * gridDim.y + blockIdx.y) * NT * 256;
+      asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_u32(Yp)),
+                   "l"(src), "r"(ybytes), "r"(y_bar)
+                   : "memory");
+    }
+  } else {  // Y: query n (row) x 256 K, bf16, core-matrix layout; queries past B are zero
+    const uint32_t ybase = smem_u32(Yp);
+    const int ngroups = NT / 8;
+    constexpr int kBatch = 2;
+    for (int e0 = tid; e0 < NT * 32; e0 += kThreads * kBatch) {
+      float4 lo[kBatch], hi[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int e = e0 + u * kThreads;
+        const int n = e >> 5, kc = e & 31;
+        lo[u] = hi[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (e < NT * 32 && q0 + n < prm.B) {
+          const float* src = (kc < 16 ? prm.A : prm.T) + (static_cast<size_t>(p) * prm.B + q0 + n) * 128 + (kc & 15) * 8;
+          lo[u] = __ldg(reinterpret_cast<const float4*>(src));
+          hi[u] = __ldg(reinterpret_cast<const float4*>(src + 4));
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int e = e0 + u * kThreads;
+        if (e < NT * 32) {
+          const int n = e >> 5, kc = e & 31;
+          st_shared_v4(ybase + (kc * ngroups + (n >> 3)) * 128 + (n & 7) * 16,
+                       bf16_bits(lo[u].x) | (bf16_bits(lo[u].y) << 16), bf16_bits(lo[u].z) | (bf16_bits(lo[u].w) << 16),
+                       bf16_bits(hi[u].x) | (bf16_bits(hi[u].y) << 16), bf16_bits(hi[u].z) | (bf16_bits(hi[u].w) << 16));
+        }
+      }
+    }
+  }
+  if (tid < 256) cbf[tid] = tid < C ? static_cast<uint16_t>(bf16_bits(cval)) : 0;
   __syncthreads();
   if constexpr (LAYOUT == kUnpackedSmallC) {
     for (int e = tid; e < C * C; e += kThreads) lut[e] = cbf[e % C] | (static_cast<uint32_t>(cbf[e / C]) << 16);
@@ -325,25 +409,6 @@ __global__ void __launch_bounds__(kThreads, 1) scores_mma_kernel(Params prm) {
     constexpr int kPc = 1 << kBits;
     for (int e = tid; e < kPc * kPc; e += kThreads)
       lut[e] = cbf[e & (kPc - 1)] | (static_cast<uint32_t>(cbf[e >> kBits]) << 16);
-  }
-  {  // Y: query n (row) x 256 K, bf16, core-matrix layout; queries past B are zero
-    const uint32_t ybase = smem_u32(Yp);
-    const int ngroups = NT / 8;
-    for (int e = tid; e < NT * 32; e += kThreads) {
-      const int n = e >> 5, kc = e & 31;
-      uint32_t o[4] = {0u, 0u, 0u, 0u};
-      const int b = q0 + n;
-      if (b < prm.B) {
-        const float* src = (kc < 16 ? prm.A : prm.T) + (static_cast<size_t>(p) * prm.B + b) * 128 + (kc & 15) * 8;
-        const float4 lo = __ldg(reinterpret_cast<const float4*>(src));
-        const float4 hi = __ldg(reinterpret_cast<const float4*>(src + 4));
-        o[0] = bf16_bits(lo.x) | (bf16_bits(lo.y) << 16);
-        o[1] = bf16_bits(lo.z) | (bf16_bits(lo.w) << 16);
-        o[2] = bf16_bits(hi.x) | (bf16_bits(hi.y) << 16);
-        o[3] = bf16_bits(hi.z) | (bf16_bits(hi.w) << 16);
-      }
-      st_shared_v4(ybase + (kc * ngroups + (n >> 3)) * 128 + (n & 7) * 16, o[0], o[1], o[2], o[3]);
-    }
   }
   fence_async_smem();
   tc_fence_before();
@@ -355,84 +420,94 @@ __global__ void __launch_bounds__(kThreads, 1) scores_mma_kernel(Params prm) {
 
   if (warp < kProducerThreads / 32) {
     // ------------------------------ producers ------------------------------
-    RawRow<LAYOUT> raw;
-    int i = 0;
-    if (static_cast<int>(blockIdx.x) < prm.key_tiles) load_row<LAYOUT>(prm, p, blockIdx.x, raw);
-    for (int kt = blockIdx.x; kt < prm.key_tiles; kt += gridDim.x, ++i) {
-      const int st = i & 1;
-      if (!wait_or_abort(x_empty + 8 * st, ((i >> 1) & 1) ^ 1, abort_v)) break;
+    auto consume = [&](const RawRow<LAYOUT>& raw, int i) -> bool {
+      const int st = i % XS;
+      if (!wait_or_abort(x_empty + 8 * st, ((i / XS) & 1) ^ 1, abort_v)) return false;
       store_row<LAYOUT>(prm, raw, xaddr0 + st * kXBytes, lut, cbf);
       fence_async_smem();
-      mbar_arrive(x_full + 8 * st);
-      if (kt + static_cast<int>(gridDim.x) < prm.key_tiles) load_row<LAYOUT>(prm, p, kt + gridDim.x, raw);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(x_full + 8 * st);
+      return true;
+    };
+    if constexpr (kTwoDeep) {
+      // two register sets: tile i+2 is requested as soon as tile i has been stored
+      int i = 0;
+      for (int kt = blockIdx.x; kt < prm.key_tiles; kt += 2 * gx, i += 2) {
+        if (!consume(raw0, i)) break;
+        if (kt + 2 * gx < prm.key_tiles) load_row<LAYOUT>(prm, p, kt + 2 * gx, raw0);
+        if (kt + gx >= prm.key_tiles) break;
+        if (!consume(raw1, i + 1)) break;
+        if (kt + 3 * gx < prm.key_tiles) load_row<LAYOUT>(prm, p, kt + 3 * gx, raw1);
+      }
+    } else {
+      int i = 0;
+      for (int kt = blockIdx.x; kt < prm.key_tiles; kt += gx, ++i) {
+        if (!consume(raw0, i)) break;
+        if (kt + gx < prm.key_tiles) load_row<LAYOUT>(prm, p, kt + gx, raw0);
+      }
     }
   } else if (warp < (kProducerThreads + kEpilogueThreads) / 32) {
     // ------------------------------ epilogue -------------------------------
-    const int e = warp - kProducerThreads / 32;      // 0..7
+    const int e = warp - kProducerThreads / 32;      // 0..EPIW-1
     const int lg = warp & 3;                         // TMEM lane quarter this warp may read
-    const int colhalf = e >> 2;
+    const int width = NT / (EPIW / 4);               // columns per warp, a multiple of 4
+    const int cbeg = (e >> 2) * width;
     const int r = lg * 32 + lane;
-    const int half_n = NT / 2;
     int i = 0;
     for (int kt = blockIdx.x; kt < prm.key_tiles; kt += gridDim.x, ++i) {
-      const int as = i & 1;
+      const int as = i % AS;
       const int s = kt * kM + r;
-      float g = 0.f;
-      if (s < prm.S) {
-        const size_t key = static_cast<size_t>(p) * prm.S + s;
-        g = LAYOUT >= kPacked1
-                ? __half2float(__ushort_as_half(__ldg(static_cast<const uint16_t*>(prm.gamma) + key)))
-                : __ldg(static_cast<const float*>(prm.gamma) + key);
-      }
-      const float kg = prm.kappa * g;
       // tcgen05.ld is warp-collective: the whole warp takes the same branch
-      const bool ok = __all_sync(0xffffffffu, wait_or_abort(acc_full + 8 * as, (i >> 1) & 1, abort_v));
+      const bool ok = __all_sync(0xffffffffu, wait_or_abort(acc_full + 8 * as, (i / AS) & 1, abort_v));
       tc_fence_after();
-      const uint32_t trow = tmem + (static_cast<uint32_t>(lg * 32) << 16) + as * 2 * NT;
-      float* out = prm.scores + (static_cast<size_t>(p) * prm.B + q0) * prm.S + s;
-      for (int c = colhalf * half_n; c < (colhalf + 1) * half_n; c += 8) {
-        uint32_t m[8], q[8];
+      const uint32_t trow = tmem + (static_cast<uint32_t>(lg * 32) << 16) + as * NT + cbeg;
+      float* out = prm.scores + (static_cast<size_t>(p) * prm.B + q0 + cbeg) * prm.S + s;
+      const int ncol = min(width, prm.B - (q0 + cbeg));
+      for (int c0 = 0; c0 < width; c0 += 16) {        // batches of up to 16 columns, one wait each
+        uint32_t v[16];
         if (ok) {
-          tmem_ld8(trow + c, m);
-          tmem_ld8(trow + NT + c, q);
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+            if (c0 + 4 * t < width) tmem_ld4(trow + c0 + 4 * t, v + 4 * t);
           tmem_ld_wait();
         }
         if (s < prm.S) {
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            if (q0 + c + j < prm.B) {
-              out[static_cast<size_t>(c + j) * prm.S] =
-                  ok ? fmaf(kg, __uint_as_float(q[j]), __uint_as_float(m[j])) : __int_as_float(0x7fc00000);
-            }
+          for (int j = 0; j < 16; ++j) {
+            if (c0 + j < ncol)
+              out[static_cast<size_t>(c0 + j) * prm.S] = ok ? __uint_as_float(v[j]) : __int_as_float(0x7fc00000);
           }
         }
       }
       if (!ok) break;
       tc_fence_before();
-      mbar_arrive(acc_empty + 8 * as);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty + 8 * as);
     }
   } else {
     // -------------------------------- MMA ----------------------------------
     if (lane == 0) {
       const uint32_t yaddr = smem_u32(Yp);
+      bool y_ready = prm.Ybf == nullptr || wait_or_abort(y_bar, 0, abort_v);
       const uint32_t idesc = idesc_bf16(kM, NT);
       const uint32_t ylbo = (NT / 8) * 128;
       int i = 0;
-      for (int kt = blockIdx.x; kt < prm.key_tiles; kt += gridDim.x, ++i) {
-        const int st = i & 1;
-        if (!wait_or_abort(x_full + 8 * st, (i >> 1) & 1, abort_v)) break;
-        if (!wait_or_abort(acc_empty + 8 * st, ((i >> 1) & 1) ^ 1, abort_v)) break;
+      for (int kt = blockIdx.x; kt < prm.key_tiles && y_ready; kt += gridDim.x, ++i) {
+        const int st = i % XS;
+        const int as = i % AS;
+        if (!wait_or_abort(x_full + 8 * st, (i / XS) & 1, abort_v)) break;
+        if (!wait_or_abort(acc_empty + 8 * as, ((i / AS) & 1) ^ 1, abort_v)) break;
         tc_fence_after();
         const uint32_t xbuf = xaddr0 + st * kXBytes;
-        const uint32_t dm = tmem + st * 2 * NT;
+        const uint32_t dm = tmem + as * NT;
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
           const uint64_t ad = smem_desc(xbuf + k * 2 * 2048, 2048, 128);
           const uint64_t bd = smem_desc(yaddr + k * 2 * ylbo, ylbo, 128);
-          mma_bf16(k < 8 ? dm : dm + NT, ad, bd, idesc, (k & 7) != 0);
+          mma_bf16(dm, ad, bd, idesc, k != 0);
         }
         mma_commit(x_empty + 8 * st);
-        mma_commit(acc_full + 8 * st);
+        mma_commit(acc_full + 8 * as);
       }
     }
     __syncwarp();
@@ -443,16 +518,20 @@ __global__ void __launch_bounds__(kThreads, 1) scores_mma_kernel(Params prm) {
   if (warp == kMmaWarp) tmem_dealloc(tmem, prm.tmem_cols);
 }
 
-template <int LAYOUT>
-cudaError_t launch_layout(const Params& prm, int P, int qtiles, cudaStream_t st) {
-  // The opt-in shared-memory size is a per-device function attribute: on the first
-  // launch on each device the kernel is given everything the device allows next to
-  // its static shared memory (one CTA per SM either way), so every descriptor the
-  // kernel builds addresses memory it owns.
+template <int LAYOUT, int EPIW, int XS>
+cudaError_t launch_cfg(const Params& prm, int P, int qtiles, bool after_prepare, int sms,
+                       cudaStream_t st) {
+  using K = Cfg<EPIW>;
+  constexpr bool kLite = EPIW == 4;
+  // Dynamic shared memory: the lite configuration takes exactly its layout so that two
+  // CTAs share an SM; the full one takes what the device allows next to its static
+  // shared memory (one CTA per SM).  The opt-in size is a per-device attribute, set on
+  // the first launch on each device.
   static std::atomic<int> dyn_bytes[64];
-  constexpr size_t need = 2 * kXBytes + static_cast<size_t>(kMaxN) * kK * 2 + 256 * 4 + 256 * 2 +
-                          8 * 8 + 16;
-  int dev = 0, sms = 148;
+  constexpr int kNMax = kLite ? 64 : kMaxN;           // the lite configuration serves NT <= 64
+  constexpr size_t need = XS * static_cast<size_t>(kXBytes) + static_cast<size_t>(kNMax) * kK * 2 +
+                          256 * 4 + 256 * 2 + 13 * 8 + 16;
+  int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   int smem = dyn_bytes[dev & 63].load(std::memory_order_acquire);
@@ -461,21 +540,44 @@ cudaError_t launch_layout(const Params& prm, int P, int qtiles, cudaStream_t st)
     e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (e != cudaSuccess) return e;
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, scores_mma_kernel<LAYOUT>);
+    e = cudaFuncGetAttributes(&fa, scores_mma_kernel<LAYOUT, EPIW, XS>);
     if (e != cudaSuccess) return e;
-    smem = optin - static_cast<int>(fa.sharedSizeBytes);
-    if (smem < static_cast<int>(need)) return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(scores_mma_kernel<LAYOUT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    smem = kLite ? static_cast<int>(need) : optin - static_cast<int>(fa.sharedSizeBytes);
+    if (smem < static_cast<int>(need) || smem > optin) return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(scores_mma_kernel<LAYOUT, EPIW, XS>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     dyn_bytes[dev & 63].store(smem, std::memory_order_release);
   }
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int per = P * qtiles;
-  int gx = (sms + per - 1) / per;
+  const int slots = kLite ? 2 * sms : sms;
+  int gx = (slots + per - 1) / per;
   gx = gx < 1 ? 1 : (gx > prm.key_tiles ? prm.key_tiles : gx);
-  dim3 grid(gx, qtiles, P);
-  scores_mma_kernel<LAYOUT><<<grid, kThreads, static_cast<size_t>(smem), st>>>(prm);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(gx, qtiles, P);
+  cfg.blockDim = dim3(K::kThreads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = after_prepare ? 1 : 0;
+  e = cudaLaunchKernelEx(&cfg, scores_mma_kernel<LAYOUT, EPIW, XS>, prm);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+template <int LAYOUT>
+cudaError_t launch_layout(const Params& prm, int P, int qtiles, bool after_prepare, cudaStream_t st) {
+  int dev = 0, sms = 148;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  // few tiles per SM: two lighter CTAs per SM run every tile at once
+  const int64_t tiles = static_cast<int64_t>(prm.key_tiles) * qtiles * P;
+  if (prm.NT <= 64 && tiles <= 4LL * sms) return launch_cfg<LAYOUT, 4, 1>(prm, P, qtiles, after_prepare, sms, st);
+  return launch_cfg<LAYOUT, 16, 2>(prm, P, qtiles, after_prepare, sms, st);
 }
 
 }  // namespace
@@ -485,8 +587,10 @@ bool mma_path_available() { return true; }
 cudaError_t launch_scores_mma(const float* A, const float* T, const uint8_t* idx,
                               const void* signs, const void* gamma, const float* codebook,
                               float* scores, int P, int B, int S, int C, int idx_bits,
-                              bool packed, cudaStream_t st) {
+                              bool packed, bool after_prepare, cudaStream_t st,
+                              const uint16_t* Ybf) {
   Params prm;
+  prm.Ybf = Ybf;
   prm.A = A;
   prm.T = T;
   prm.idx = idx;
@@ -497,22 +601,22 @@ cudaError_t launch_scores_mma(const float* A, const float* T, const uint8_t* idx
   prm.B = B;
   prm.S = S;
   prm.C = C;
-  const int nt = B < kMaxN ? B : kMaxN;
-  prm.NT = (nt + 15) / 16 * 16;
-  const int qtiles = (B + prm.NT - 1) / prm.NT;
+  prm.NT = mma_query_tile(B);
+  const int qtiles = mma_query_tiles(B);
   prm.key_tiles = (S + kM - 1) / kM;
+  prm.acc_stages = 4;                      // 4 x NT <= 512 TMEM columns for NT <= 128
   int cols = 32;
-  while (cols < 4 * prm.NT) cols <<= 1;
+  while (cols < prm.acc_stages * prm.NT) cols <<= 1;
   prm.tmem_cols = cols;
   prm.kappa = qjl_scale(128);
   if (!packed) {
-    return C <= 16 ? launch_layout<kUnpackedSmallC>(prm, P, qtiles, st)
-                   : launch_layout<kUnpackedLargeC>(prm, P, qtiles, st);
+    return C <= 16 ? launch_layout<kUnpackedSmallC>(prm, P, qtiles, after_prepare, st)
+                   : launch_layout<kUnpackedLargeC>(prm, P, qtiles, after_prepare, st);
   }
   switch (idx_bits) {
-    case 1: return launch_layout<kPacked1>(prm, P, qtiles, st);
-    case 2: return launch_layout<kPacked2>(prm, P, qtiles, st);
-    default: return launch_layout<kPacked3>(prm, P, qtiles, st);
+    case 1: return launch_layout<kPacked1>(prm, P, qtiles, after_prepare, st);
+    case 2: return launch_layout<kPacked2>(prm, P, qtiles, after_prepare, st);
+    default: return launch_layout<kPacked3>(prm, P, qtiles, after_prepare, st);
   }
 }
 

@@ -124,7 +124,8 @@ tq_status tq_scores_packed(const float* A, const float* T, const uint8_t* idx_pl
  * per-call cudaMalloc/cudaFree (riteshyadav.xyz, "What the rearrangement
  * saves": its solve "allocates temporary arrays on every call").  The caller
  * passes `workspace`, a device buffer of at least tq_workspace_bytes(P, B, D)
- * bytes that holds A and T between the two steps; it is scratch, its contents
+ * bytes that holds A and T between the two steps (and, for D = 128 and B >= 16,
+ * their bf16 copy laid out for the tensor cores); it is scratch, its contents
  * on return are unspecified, and calls that may run concurrently must not
  * share it.  (tq_solve_packed on the fp32 path with B <= 8 and D = 128 runs the
  * transform inside its single scoring kernel and leaves the workspace untouched.)
@@ -210,7 +211,8 @@ tq_status tq_haar_rotation(const double* G, int D, float* Pi);
  * process exits).  It calls no allocator.
  *
  * Limit: tq_workspace_bytes(P, B, D) must be <= 1048576 (for D = 128 that is
- * P*B <= 1024 queries); larger calls return TQ_ERR_WORKSPACE and launch nothing.
+ * about 1 KB per query, 1.5 KB per query when B >= 16); larger calls return
+ * TQ_ERR_WORKSPACE and launch nothing.
  * The first call on each device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream
  * capture.  Nothing in the array needs to start at zero (the transform writes

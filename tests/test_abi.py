@@ -28,8 +28,9 @@ def test_status_strings(L):
 
 
 def test_workspace_bytes(L):
-    assert tq.workspace_bytes(1, 32, 128) == 2 * 32 * 128 * 4
+    assert tq.workspace_bytes(1, 32, 128) == 2 * 32 * 128 * 4 + 32 * 512     # A, T, bf16 query operand
     assert tq.workspace_bytes(1, 1, 2) == 2 * 256          # each half rounded up to 256 bytes
+    assert tq.workspace_bytes(1, 8, 128) == 2 * 8 * 128 * 4                 # no tensor-core copy below B = 16
     assert tq.workspace_bytes(0, 1, 1) == 0
 
 

@@ -89,6 +89,24 @@ def step_input_bytes(w) -> int:
     return qbytes + w.P * w.S * key_bytes(w) + 2 * 4 * w.H * w.D * w.D + 4 * w.C
 
 
+def rank_workload(w, rank: int):
+    """The workload rank `rank` scores under torchrun: the same shape, its own seed, so
+    that every rank processes distinct problems (weak scaling; no data is exchanged)."""
+    import dataclasses
+    return dataclasses.replace(w, seed=w.seed + 7919 * rank)
+
+
+def max_over_ranks(value: float, dist, device) -> float:
+    """Maximum of `value` over all ranks (the slowest rank bounds the job); identity when
+    not distributed."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def hbm_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -280,6 +298,7 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
+    w = rank_workload(w, rank)
 
     tq.lib()
     path = args.path if args.path != "auto" else tq.auto_path(w.B, w.D)
@@ -358,11 +377,7 @@ def main():
     t_wall1 = time.time()
     if dist:
         dist.barrier()
-    elapsed_ms = start.elapsed_time(end)
-    if dist:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(start.elapsed_time(end), dist, dev)
     clk = clocks.stop((t_wall0, t_wall1))
 
     # Dominant-kernel duration: the mean of back-to-back launches in one graph over the

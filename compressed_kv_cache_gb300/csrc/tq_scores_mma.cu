@@ -463,17 +463,17 @@ __global__ void __launch_bounds__(Cfg<EPIW>::kThreads, (EPIW == 4 ? 2 : 1)) scor
       const uint32_t trow = tmem + (static_cast<uint32_t>(lg * 32) << 16) + as * NT + cbeg;
       float* out = prm.scores + (static_cast<size_t>(p) * prm.B + q0 + cbeg) * prm.S + s;
       const int ncol = min(width, prm.B - (q0 + cbeg));
-      for (int c0 = 0; c0 < width; c0 += 16) {        // batches of up to 16 columns, one wait each
-        uint32_t v[16];
+      for (int c0 = 0; c0 < width; c0 += 32) {        // batches of up to 32 columns, one wait each
+        uint32_t v[32];
         if (ok) {
 #pragma unroll
-          for (int t = 0; t < 4; ++t)
+          for (int t = 0; t < 8; ++t)
             if (c0 + 4 * t < width) tmem_ld4(trow + c0 + 4 * t, v + 4 * t);
           tmem_ld_wait();
         }
         if (s < prm.S) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
+          for (int j = 0; j < 32; ++j) {
             if (c0 + j < ncol)
               out[static_cast<size_t>(c0 + j) * prm.S] = ok ? __uint_as_float(v[j]) : __int_as_float(0x7fc00000);
           }

@@ -222,8 +222,9 @@ scores_packed_kernel(const float* __restrict__ A, const float* __restrict__ T,
 //
 // Each query's A and T turn into small tables of partial sums in shared memory
 // (the byte-level table of zededa.com's "Dead End: Byte-Level Lookup Table",
-// moved from global to shared memory and cut to 4/6-bit keys so that a warp's
-// 32 lookups into one table never conflict on a bank):
+// moved from global to shared memory and cut to 4-bit keys, whose 16-entry
+// tables take a warp's 32 lookups without a bank conflict; the 6-bit keys of
+// 3-bit codes index 64-entry tables, at most two-way conflicts):
 //   code table  (position g, value v) = sum_{i<G} A[g*G+i] * c[(v >> BITS*i) & (C-1)]
 //   sign table  (position g, value v) = sum_{i<4} T[4g+i] * (bit i of v ? +1 : -1)
 // with G = 2 codes per lookup for 2- and 3-bit codes and 4 for 1-bit codes.  A
@@ -239,6 +240,140 @@ struct LutShape {
   static constexpr int PER_Q = NPI * NV + NPS * 16;      // floats per query
 };
 
+// One key of the packed cache in registers: BITS 16-byte rows of codes, the
+// 16-byte row of signs and the fp16 gamma.
+template <int BITS>
+struct PackedKey {
+  uint4 idx[BITS];
+  uint4 sg;
+  uint16_t g;
+};
+
+template <int BITS>
+__device__ __forceinline__ void load_packed_key(PackedKey<BITS>& k,
+                                                const uint8_t* __restrict__ idx_plane,
+                                                const uint8_t* __restrict__ sign_plane,
+                                                const uint16_t* __restrict__ gamma_f16,
+                                                size_t key) {
+  const uint4* ip = reinterpret_cast<const uint4*>(idx_plane + key * (16 * BITS));
+#pragma unroll
+  for (int i = 0; i < BITS; ++i) k.idx[i] = __ldg(ip + i);
+  k.sg = __ldg(reinterpret_cast<const uint4*>(sign_plane + key * 16));
+  k.g = __ldg(gamma_f16 + key);
+}
+
+// Code and sign sums of one key for QB queries, read from the tables [QB][PER_Q].
+// Two partial sums per part give two independent add chains.
+template <int BITS, int QB>
+__device__ __forceinline__ void lut_key_sums(const float* lut, const PackedKey<BITS>& k,
+                                             float (&mm)[QB], float (&rr)[QB]) {
+  using L = LutShape<BITS>;
+  uint32_t w[4 * BITS + 1];
+#pragma unroll
+  for (int i = 0; i < BITS; ++i) {
+    w[4 * i] = k.idx[i].x; w[4 * i + 1] = k.idx[i].y; w[4 * i + 2] = k.idx[i].z; w[4 * i + 3] = k.idx[i].w;
+  }
+  w[4 * BITS] = 0u;
+  const uint32_t ws[4] = {k.sg.x, k.sg.y, k.sg.z, k.sg.w};
+  float m[2][QB], r[2][QB];
+#pragma unroll
+  for (int q = 0; q < QB; ++q) { m[0][q] = m[1][q] = 0.f; r[0][q] = r[1][q] = 0.f; }
+#pragma unroll
+  for (int gi = 0; gi < L::NPI; ++gi) {
+    const int off = L::KB * gi;
+    const int wd = off >> 5, sh = off & 31;
+    uint32_t v;
+    if (sh + L::KB <= 32) {
+      v = (w[wd] >> sh) & (L::NV - 1);
+    } else {
+      v = __funnelshift_r(w[wd], w[wd + 1], sh) & (L::NV - 1);
+    }
+#pragma unroll
+    for (int q = 0; q < QB; ++q) m[gi & 1][q] += lut[q * L::PER_Q + gi * L::NV + v];
+  }
+#pragma unroll
+  for (int gi = 0; gi < L::NPS; ++gi) {
+    const uint32_t v = (ws[gi >> 3] >> (4 * (gi & 7))) & 15u;
+#pragma unroll
+    for (int q = 0; q < QB; ++q) r[gi & 1][q] += lut[q * L::PER_Q + L::NPI * L::NV + gi * 16 + v];
+  }
+#pragma unroll
+  for (int q = 0; q < QB; ++q) { mm[q] = m[0][q] + m[1][q]; rr[q] = r[0][q] + r[1][q]; }
+}
+
+// Centroids of the table value this thread keeps fixed while it builds tables
+// (value v = thread % NV; code i of v is bits BITS*i .. BITS*i+BITS-1).
+template <int BITS>
+__device__ __forceinline__ void table_centroids(const float* __restrict__ codebook,
+                                                float (&cv)[LutShape<BITS>::G]) {
+  using L = LutShape<BITS>;
+  const int v = threadIdx.x % L::NV;
+#pragma unroll
+  for (int k = 0; k < L::G; ++k) cv[k] = __ldg(codebook + ((v >> (BITS * k)) & ((1 << BITS) - 1)));
+}
+
+// Tables of QB queries from A (a[0..127]) and T (a[128..255]) of each query,
+// a = at(q).  NT threads; thread t keeps one table value fixed and walks positions.
+template <int BITS, int QB, int NT, typename At>
+__device__ __forceinline__ void build_luts(At at, float* lut, const float (&cv)[LutShape<BITS>::G]) {
+  using L = LutShape<BITS>;
+  static_assert(NT % L::NV == 0, "code tables must tile the CTA");
+  const int v = threadIdx.x % L::NV;
+  const int vs = threadIdx.x & 15;
+  for (int q = 0; q < QB; ++q) {
+    float* tq = lut + q * L::PER_Q;
+    for (int g = threadIdx.x / L::NV; g < L::NPI; g += NT / L::NV) {
+      float acc = 0.f;
+#pragma unroll
+      for (int k = 0; k < L::G; ++k) acc = fmaf(at(q, g * L::G + k), cv[k], acc);
+      tq[g * L::NV + v] = acc;
+    }
+    for (int g = threadIdx.x >> 4; g < L::NPS; g += NT / 16) {
+      float acc = 0.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float t = at(q, 128 + 4 * g + i);
+        acc += ((vs >> i) & 1) ? t : -t;
+      }
+      tq[L::NPI * L::NV + g * 16 + vs] = acc;
+    }
+  }
+}
+
+// Keys first, first + stride, ... below end (end <= S): two keys are always in
+// flight ahead of the one being reduced.
+template <int BITS, int QB>
+__device__ __forceinline__ void lut_score_keys(const float* lut, const uint8_t* __restrict__ idx_plane,
+                                               const uint8_t* __restrict__ sign_plane,
+                                               const uint16_t* __restrict__ gamma_f16,
+                                               float* __restrict__ scores, PackedKey<BITS>& k0,
+                                               PackedKey<BITS>& k1, int first, int stride, int end,
+                                               int p, int b0, int B, int S, float kappa) {
+  const size_t base = static_cast<size_t>(p) * S;
+  for (int64_t s = first; s < end; s += stride) {
+    const PackedKey<BITS> cur = k0;
+    k0 = k1;
+    if (s + 2 * static_cast<int64_t>(stride) < end)
+      load_packed_key<BITS>(k1, idx_plane, sign_plane, gamma_f16, base + s + 2 * static_cast<int64_t>(stride));
+    float mm[QB], rr[QB];
+    lut_key_sums<BITS, QB>(lut, cur, mm, rr);
+    store_scores<QB>(scores, mm, rr, kappa * __half2float(__ushort_as_half(cur.g)), p, b0, B, S,
+                     static_cast<int>(s));
+  }
+}
+
+template <int BITS>
+__device__ __forceinline__ void prefetch_two_keys(PackedKey<BITS>& k0, PackedKey<BITS>& k1,
+                                                  const uint8_t* __restrict__ idx_plane,
+                                                  const uint8_t* __restrict__ sign_plane,
+                                                  const uint16_t* __restrict__ gamma_f16, int p,
+                                                  int first, int stride, int end, int S) {
+  const size_t base = static_cast<size_t>(p) * S;
+  if (first < end) load_packed_key<BITS>(k0, idx_plane, sign_plane, gamma_f16, base + first);
+  if (first + static_cast<int64_t>(stride) < end)
+    load_packed_key<BITS>(k1, idx_plane, sign_plane, gamma_f16, base + first + stride);
+}
+
 template <int BITS, int QB>
 __global__ void __launch_bounds__(256)
 scores_packed_lut_kernel(const float* __restrict__ A, const float* __restrict__ T,
@@ -247,101 +382,31 @@ scores_packed_lut_kernel(const float* __restrict__ A, const float* __restrict__ 
                          const uint16_t* __restrict__ gamma_f16,
                          const float* __restrict__ codebook, float* __restrict__ scores, int B,
                          int S, float kappa) {
-  using L = LutShape<BITS>;
-  constexpr int D = 128;
-  constexpr int kC = 1 << BITS;
   extern __shared__ __align__(16) float smem[];
   float* lut = smem;                      // [QB][NPI*NV + NPS*16]
   const int p = blockIdx.z;
   const int b0 = blockIdx.y * QB;
   const int stride = gridDim.x * blockDim.x;
+  const int first = blockIdx.x * blockDim.x + threadIdx.x;
 
-  // Rows of the first key are requested before the tables are built, and every
-  // iteration requests the next key's rows before it reduces the current key.
-  uint4 nxt_i[BITS], nxt_s;
-  uint16_t nxt_g = 0;
-  auto fetch = [&](int s) {
-    if (s < S) {
-      const size_t key = static_cast<size_t>(p) * S + s;
-      const uint4* ip = reinterpret_cast<const uint4*>(idx_plane + key * (16 * BITS));
-#pragma unroll
-      for (int i = 0; i < BITS; ++i) nxt_i[i] = __ldg(ip + i);
-      nxt_s = __ldg(reinterpret_cast<const uint4*>(sign_plane + key * 16));
-      nxt_g = __ldg(gamma_f16 + key);
-    }
-  };
-  fetch(blockIdx.x * blockDim.x + threadIdx.x);
+  // the first two keys' rows are requested before the tables are built
+  PackedKey<BITS> k0, k1;
+  prefetch_two_keys<BITS>(k0, k1, idx_plane, sign_plane, gamma_f16, p, first, stride, S, S);
 
-  // Table build.  Thread t keeps one table value v fixed (so its centroids, or its
-  // signs, are fixed) and walks the table positions; A and T are read through L1.
-  static_assert(256 % L::NV == 0, "code tables must tile the CTA");
-  {
-    const int v = threadIdx.x % L::NV;
-    float cv[L::G];
-#pragma unroll
-    for (int k = 0; k < L::G; ++k) {
-      const int code = (v >> (BITS * k)) & (kC - 1);
-      cv[k] = __ldg(codebook + code);
-    }
-    const int vs = threadIdx.x & 15;
-    for (int q = 0; q < QB; ++q) {
-      const bool live = b0 + q < B;
-      const size_t row = (static_cast<size_t>(p) * B + (live ? b0 + q : b0)) * D;
-      float* tq = lut + q * L::PER_Q;
-      for (int g = threadIdx.x / L::NV; g < L::NPI; g += 256 / L::NV) {
-        float acc = 0.f;
-#pragma unroll
-        for (int k = 0; k < L::G; ++k) acc = fmaf(__ldg(A + row + g * L::G + k), cv[k], acc);
-        tq[g * L::NV + v] = live ? acc : 0.f;
-      }
-      for (int g = threadIdx.x >> 4; g < L::NPS; g += 16) {
-        float acc = 0.f;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float t = __ldg(T + row + 4 * g + i);
-          acc += ((vs >> i) & 1) ? t : -t;
-        }
-        tq[L::NPI * L::NV + g * 16 + vs] = live ? acc : 0.f;
-      }
-    }
-  }
+  // A and T are read through L1; rows of queries past B give zero tables
+  float cv[LutShape<BITS>::G];
+  table_centroids<BITS>(codebook, cv);
+  build_luts<BITS, QB, 256>(
+      [&](int q, int e) {
+        const bool live = b0 + q < B;
+        const size_t row = (static_cast<size_t>(p) * B + (live ? b0 + q : b0)) * 128;
+        const float x = e < 128 ? __ldg(A + row + e) : __ldg(T + row + e - 128);
+        return live ? x : 0.f;
+      },
+      lut, cv);
   __syncthreads();
-
-  for (int s = blockIdx.x * blockDim.x + threadIdx.x; s < S; s += stride) {
-    uint32_t w[4 * BITS + 1];
-#pragma unroll
-    for (int i = 0; i < BITS; ++i) {
-      w[4 * i] = nxt_i[i].x; w[4 * i + 1] = nxt_i[i].y; w[4 * i + 2] = nxt_i[i].z; w[4 * i + 3] = nxt_i[i].w;
-    }
-    w[4 * BITS] = 0u;
-    const uint32_t ws[4] = {nxt_s.x, nxt_s.y, nxt_s.z, nxt_s.w};
-    const float g = __half2float(__ushort_as_half(nxt_g));
-    fetch(s + stride);
-
-    float m[QB], r[QB];
-#pragma unroll
-    for (int q = 0; q < QB; ++q) { m[q] = 0.f; r[q] = 0.f; }
-#pragma unroll
-    for (int gi = 0; gi < L::NPI; ++gi) {
-      const int off = L::KB * gi;
-      const int wd = off >> 5, sh = off & 31;
-      uint32_t v;
-      if (sh + L::KB <= 32) {
-        v = (w[wd] >> sh) & (L::NV - 1);
-      } else {
-        v = __funnelshift_r(w[wd], w[wd + 1], sh) & (L::NV - 1);
-      }
-#pragma unroll
-      for (int q = 0; q < QB; ++q) m[q] += lut[q * L::PER_Q + gi * L::NV + v];
-    }
-#pragma unroll
-    for (int gi = 0; gi < L::NPS; ++gi) {
-      const uint32_t v = (ws[gi >> 3] >> (4 * (gi & 7))) & 15u;
-#pragma unroll
-      for (int q = 0; q < QB; ++q) r[q] += lut[q * L::PER_Q + L::NPI * L::NV + gi * 16 + v];
-    }
-    store_scores<QB>(scores, m, r, kappa * g, p, b0, B, S, s);
-  }
+  lut_score_keys<BITS, QB>(lut, idx_plane, sign_plane, gamma_f16, scores, k0, k1, first, stride, S,
+                           p, b0, B, S, kappa);
 }
 
 template <int BITS, int QB>
@@ -385,215 +450,315 @@ cudaError_t launch_lut_bits(const float* A, const float* T, const uint8_t* idx_p
 
 
 // ---------------------------------------------------------------------------
-// Fused query transform + packed scoring for few queries (D = 128): one
-// persistent CTA per SM stages Pi and S_mat of its problem's head in shared
-// memory (rows padded to 129 floats, so "thread d reads row d" is free of bank
-// conflicts), computes A = Pi q and T = S_mat q for its query tile there
-// ("TurboQuant Attention in CUDA", "Two kernels, two jobs": the first kernel,
-// here inside the second), builds the same lookup tables as
-// scores_packed_lut_kernel and scores its share of the keys.  The first keys'
-// rows are in flight during the whole prologue.  One kernel per call, nothing
-// written to a workspace.
+// Fused query transform + packed scoring for few queries (D = 128), one kernel
+// per call with nothing written to a workspace ("TurboQuant Attention in CUDA",
+// "Two kernels, two jobs": the first kernel, here inside the second).
+//
+// A cluster of CS CTAs (8 for few problems, 2 for many) serves one (problem,
+// query tile); each CTA scores one contiguous range of the keys.  The stacked
+// matrix [Pi; S_mat] of the problem's head has 256 rows; CTA rank r brings rows
+// r*R .. r*R+R-1 (R = 256/CS) into its shared memory with one bulk copy, forms
+// those rows of A = Pi q and T = S_mat q for its QB queries (a warp per 8 rows,
+// the query in registers), and sends each group of 8 rows to every CTA of the
+// cluster by a shared-to-shared bulk copy that completes bytes on the receiver's
+// mbarrier.  Once that mbarrier has seen all 256 rows a CTA holds all of A and
+// T, builds the same lookup tables as scores_packed_lut_kernel and scores its
+// keys.  Order of requests: the rows and, for short ranges, an L2 prefetch of the
+// key rows (copy engine), then the query and the codebook, then - after the rows
+// have landed - every thread's first two keys, which stay in flight through the
+// exchange and the table build.  The kernel is launched as a programmatic
+// dependent: everything it reads from global memory is read after
+// griddepcontrol.wait.
 // ---------------------------------------------------------------------------
-template <int BITS, int QB>
-constexpr size_t fused_smem_bytes() {
-  return 2 * 128 * 128 * sizeof(float) + 16 + (QB * 128 + QB * 256 + QB * LutShape<BITS>::PER_Q) * sizeof(float);
-}
 template <int QB>
 __host__ __device__ constexpr int fused_threads() { return QB <= 2 ? 512 : 256; }
+// CTAs per SM the register budget is cut for (64 registers a thread for 512
+// threads, 128 for 256)
+template <int QB>
+__host__ __device__ constexpr int fused_min_blocks() { return 2; }
 
-__device__ __forceinline__ float load_query(const float* q, size_t i) { return q[i]; }
-__device__ __forceinline__ float load_query(const __nv_bfloat16* q, size_t i) {
-  return __bfloat162float(q[i]);
+// Shared memory of the fused kernel: the CTA's rows of [Pi; S_mat], two mbarriers,
+// its slice of A/T, all of A/T and the tables.
+template <int BITS, int QB, int CS>
+constexpr size_t fused_smem_bytes() {
+  return (256 / CS) * 128 * sizeof(float) + 16 +
+         ((256 / CS) * QB + QB * 256 + QB * LutShape<BITS>::PER_Q) * sizeof(float);
 }
 
-template <int BITS, int QB, typename QT>
-__global__ void __launch_bounds__(fused_threads<QB>(), 1)
+// Bounded wait for the given phase parity of a local mbarrier (about a second at most).
+__device__ __forceinline__ bool wait_parity(uint32_t bar, uint32_t parity) {
+  for (uint32_t it = 0; it < (1u << 22); ++it) {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    if (ok) return true;
+  }
+  return false;
+}
+
+__device__ __forceinline__ void expect_bytes(uint32_t bar, uint32_t bytes) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(bar),
+               "r"(bytes)
+               : "memory");
+}
+
+// Coordinates 4*lane .. 4*lane+3 of one query row of 128.
+__device__ __forceinline__ float4 load_query4(const float* q, int lane) {
+  return __ldg(reinterpret_cast<const float4*>(q) + lane);
+}
+__device__ __forceinline__ float4 load_query4(const __nv_bfloat16* q, int lane) {
+  const uint2 v = __ldg(reinterpret_cast<const uint2*>(q) + lane);
+  return make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u),
+                     __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
+}
+
+// Sums over the 32 lanes of 8 per-lane values v[0..7] at once (a transposing
+// butterfly): afterwards lane l holds the full sum of value
+// 4*bit4(l) + 2*bit3(l) + bit2(l), in v[0].  Nine shuffles instead of forty.
+__device__ __forceinline__ float warp_sum8(float (&v)[8], int lane) {
+  const bool h4 = (lane >> 4) & 1, h3 = (lane >> 3) & 1, h2 = (lane >> 2) & 1;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float send = h4 ? v[i] : v[i + 4];
+    const float keep = h4 ? v[i + 4] : v[i];
+    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float send = h3 ? v[i] : v[i + 2];
+    const float keep = h3 ? v[i + 2] : v[i];
+    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+  }
+  {
+    const float send = h2 ? v[0] : v[1];
+    const float keep = h2 ? v[1] : v[0];
+    v[0] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+  }
+  v[0] += __shfl_xor_sync(0xffffffffu, v[0], 2);
+  v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+  return v[0];
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t local_addr, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
+  return remote;
+}
+template <int BITS, int QB, int CS, typename QT>
+__global__ void __launch_bounds__(fused_threads<QB>(), fused_min_blocks<QB>())
 solve_packed_lut_kernel(const QT* __restrict__ Q, const float* __restrict__ Pi,
                         const float* __restrict__ Sm, int H, const uint8_t* __restrict__ idx_plane,
                         const uint8_t* __restrict__ sign_plane,
                         const uint16_t* __restrict__ gamma_f16,
                         const float* __restrict__ codebook, float* __restrict__ scores, int B,
                         int S, float kappa) {
-  using L = LutShape<BITS>;
   constexpr int D = 128;
-  constexpr int kC = 1 << BITS;
   constexpr int kT = fused_threads<QB>();
+  constexpr int R = 256 / CS;                             // rows of [Pi; S_mat] per CTA
+  static_assert(R % 8 == 0 && CS <= 32, "transform split");
   extern __shared__ __align__(16) float smem[];
-  float* sM = smem;                                       // [2][128][128]: Pi, then S_mat
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sM + 2 * 128 * 128);
-  float* sQ = reinterpret_cast<float*>(bar + 2);          // [QB][128]
-  float* sAT = sQ + QB * 128;                             // [QB][256]: A then T
+  float* sRows = smem;                                    // [R][128]
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sRows + R * D);   // [0]: rows, [1]: A/T
+  float* sMine = reinterpret_cast<float*>(bar + 2);       // [R][QB]: this CTA's rows of A/T
+  float* sAT = sMine + R * QB;                            // [256][QB]: rows of A, then of T
   float* lut = sAT + QB * 256;                            // [QB][PER_Q]
   const int p = blockIdx.z;
   const int h = p % H;
   const int b0 = blockIdx.y * QB;
-  const int stride = gridDim.x * kT;
   const int tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  // this CTA's keys: one contiguous range, walked by the threads in steps of kT
+  const int chunk = static_cast<int>((static_cast<int64_t>(S) + gridDim.x - 1) / gridDim.x);
+  const int k_begin = static_cast<int>(min(static_cast<int64_t>(blockIdx.x) * chunk, static_cast<int64_t>(S)));
+  const int k_end = k_begin + chunk < S ? k_begin + chunk : S;
+  const int first = k_begin + tid;
+  const uint32_t rank = cluster_ctarank();
+  const int row0 = static_cast<int>(rank) * R;
 
-  // Pi and S_mat of head h arrive by two bulk copies on one mbarrier.  The barrier is
-  // initialised and made visible to every thread before anyone issues or polls it.
-  const uint32_t bar_a = static_cast<uint32_t>(__cvta_generic_to_shared(bar));
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const uint32_t bar_rows = static_cast<uint32_t>(__cvta_generic_to_shared(bar));
+  const uint32_t bar_at = bar_rows + 8;
   if (tid == 0) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar_a) : "memory");
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar_rows) : "memory");
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar_at) : "memory");
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    expect_bytes(bar_at, 256 * QB * 4);
   }
+  // both barriers are initialised before any thread of the cluster uses them, and
+  // every CTA of the cluster runs before anyone copies into a peer
   __syncthreads();
+  cluster_arrive_relaxed();
+  cluster_wait();
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (tid == 0) {
-    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(bar_a),
-                 "r"(2u * D * D * 4u)
+    expect_bytes(bar_rows, R * D * 4);
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     static_cast<uint32_t>(__cvta_generic_to_shared(sRows))),
+                 "l"((row0 < D ? Pi : Sm) + (static_cast<size_t>(h) * D + (row0 & (D - 1))) * D),
+                 "r"(static_cast<uint32_t>(R * D * 4)), "r"(bar_rows)
                  : "memory");
-    const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(sM));
-    const float* src0 = Pi + static_cast<size_t>(h) * D * D;
-    const float* src1 = Sm + static_cast<size_t>(h) * D * D;
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-                 "l"(src0), "r"(D * D * 4u), "r"(bar_a)
-                 : "memory");
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst + D * D * 4u),
-                 "l"(src1), "r"(D * D * 4u), "r"(bar_a)
-                 : "memory");
-  }
-
-  uint4 nxt_i[BITS], nxt_s;
-  uint16_t nxt_g = 0;
-  auto fetch = [&](int s) {
-    if (s < S) {
-      const size_t key = static_cast<size_t>(p) * S + s;
-      const uint4* ip = reinterpret_cast<const uint4*>(idx_plane + key * (16 * BITS));
-#pragma unroll
-      for (int i = 0; i < BITS; ++i) nxt_i[i] = __ldg(ip + i);
-      nxt_s = __ldg(reinterpret_cast<const uint4*>(sign_plane + key * 16));
-      nxt_g = __ldg(gamma_f16 + key);
+    // a short range of key rows (up to 64 KB) starts streaming from HBM into L2
+    // now, through the copy engine rather than the load pipe, so the prologue's own
+    // reads are not held up
+    if (k_end > k_begin && (k_end - k_begin) * (16 * BITS + 16) <= 65536) {
+      const size_t key0 = static_cast<size_t>(p) * S + k_begin;
+      const uint32_t n = static_cast<uint32_t>(k_end - k_begin);
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(idx_plane + key0 * (16 * BITS)),
+                   "r"(n * (16u * BITS))
+                   : "memory");
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(sign_plane + key0 * 16), "r"(n * 16u)
+                   : "memory");
     }
-  };
-  fetch(blockIdx.x * kT + tid);
-
-  for (int e = tid; e < QB * D; e += kT) {
-    const int q = e / D;
-    sQ[e] = b0 + q < B ? load_query(Q, (static_cast<size_t>(p) * B + b0) * D + e) : 0.f;
   }
-  // bounded wait for the two copies (about a second at most)
-  bool landed = false;
-  for (uint32_t it = 0; it < (1u << 22) && !landed; ++it) {
-    uint32_t ok;
-    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-                 : "=r"(ok) : "r"(bar_a) : "memory");
-    landed = ok != 0;
-  }
-  __syncthreads();
-  // thread t < 256: output coordinate d = t % 128 of A (t < 128) or of T; row d is walked in
-  // the column order j = (jj + d) mod 128, so the 32 lanes of a warp read 32 banks
-  if (tid < 256) {
-    const int d = tid & 127;
-    const float* row = sM + (tid >> 7) * D * D + d * D;
-    float acc[QB];
+  float cv[LutShape<BITS>::G];
+  table_centroids<BITS>(codebook, cv);
+  // rows of A/T: warp w takes groups of 8 rows; lane l reads coordinates 4l .. 4l+3
+  // of each row (one conflict-free 512-byte row a warp) and the warp sums them.  Each
+  // group goes to every CTA of the cluster by its own bulk copies, completing bytes
+  // on the receiver's mbarrier, so no warp waits for another here.
+  // Every warp waits for the rows before its keys are requested, so that their
+  // flood does not delay the query and the rows.
+  float4 qx[QB];                                          // the query tile; rows past B are zero
+  if (warp < R / 8) {
 #pragma unroll
-    for (int q = 0; q < QB; ++q) acc[q] = 0.f;
-#pragma unroll 8
-    for (int jj = 0; jj < D; ++jj) {
-      const int j = (jj + d) & (D - 1);
-      const float m = row[j];
-#pragma unroll
-      for (int q = 0; q < QB; ++q) acc[q] = fmaf(m, sQ[q * D + j], acc[q]);
-    }
-#pragma unroll
-    for (int q = 0; q < QB; ++q) sAT[q * 256 + tid] = landed ? acc[q] : __int_as_float(0x7fc00000);
-  }
-  __syncthreads();
-  // lookup tables from A and T (thread keeps one table value fixed)
-  {
-    const int v = tid % L::NV;
-    float cv[L::G];
-#pragma unroll
-    for (int k = 0; k < L::G; ++k) cv[k] = __ldg(codebook + ((v >> (BITS * k)) & (kC - 1)));
-    const int vs = tid & 15;
     for (int q = 0; q < QB; ++q) {
-      const float* a = sAT + q * 256;
-      float* tq = lut + q * L::PER_Q;
-      for (int g = tid / L::NV; g < L::NPI; g += kT / L::NV) {
-        float acc = 0.f;
+      qx[q] = b0 + q < B ? load_query4(Q + (static_cast<size_t>(p) * B + b0 + q) * D, lane)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+  const bool landed = wait_parity(bar_rows, 0);
+  if (warp < R / 8) {
+    for (int g = warp; g < R / 8; g += kT / 32) {
+      float part[QB][8];
 #pragma unroll
-        for (int k = 0; k < L::G; ++k) acc = fmaf(a[g * L::G + k], cv[k], acc);
-        tq[g * L::NV + v] = acc;
+      for (int i = 0; i < 8; ++i) {
+        const float4 m = *reinterpret_cast<const float4*>(sRows + (g * 8 + i) * D + 4 * lane);
+#pragma unroll
+        for (int q = 0; q < QB; ++q)
+          part[q][i] = fmaf(m.w, qx[q].w, fmaf(m.z, qx[q].z, fmaf(m.y, qx[q].y, m.x * qx[q].x)));
       }
-      for (int g = tid >> 4; g < L::NPS; g += kT / 16) {
-        float acc = 0.f;
+      const int r = g * 8 + ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float t = a[D + 4 * g + i];
-          acc += ((vs >> i) & 1) ? t : -t;
-        }
-        tq[L::NPI * L::NV + g * 16 + vs] = acc;
+      for (int q = 0; q < QB; ++q) {
+        const float v = warp_sum8(part[q], lane);
+        if ((lane & 3) == 0) sMine[r * QB + q] = landed ? v : __int_as_float(0x7fc00000);
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane < CS) {
+        const uint32_t src = static_cast<uint32_t>(__cvta_generic_to_shared(sMine + g * 8 * QB));
+        const uint32_t dst = map_to_rank(
+            static_cast<uint32_t>(__cvta_generic_to_shared(sAT + (row0 + g * 8) * QB)), static_cast<uint32_t>(lane));
+        asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                     "r"(src), "r"(static_cast<uint32_t>(8 * QB * 4)),
+                     "r"(map_to_rank(bar_at, static_cast<uint32_t>(lane)))
+                     : "memory");
       }
     }
   }
+  // the first two keys of every thread, in flight during the exchange and the tables
+  PackedKey<BITS> k0, k1;
+  prefetch_two_keys<BITS>(k0, k1, idx_plane, sign_plane, gamma_f16, p, first, kT, k_end, S);
+  // every copy into this CTA has completed (so every peer is done reading the slices
+  // it sent here); the cluster barrier below keeps each CTA alive until all have
+  const bool have_at = wait_parity(bar_at, 0);
+  cluster_arrive_relaxed();
+  build_luts<BITS, QB, kT>(
+      [&](int q, int e) { return have_at ? sAT[e * QB + q] : __int_as_float(0x7fc00000); }, lut, cv);
   __syncthreads();
-
-  for (int s = blockIdx.x * kT + tid; s < S; s += stride) {
-    uint32_t w[4 * BITS + 1];
-#pragma unroll
-    for (int i = 0; i < BITS; ++i) {
-      w[4 * i] = nxt_i[i].x; w[4 * i + 1] = nxt_i[i].y; w[4 * i + 2] = nxt_i[i].z; w[4 * i + 3] = nxt_i[i].w;
-    }
-    w[4 * BITS] = 0u;
-    const uint32_t ws[4] = {nxt_s.x, nxt_s.y, nxt_s.z, nxt_s.w};
-    const float g = __half2float(__ushort_as_half(nxt_g));
-    fetch(s + stride);
-    // two partial sums per query and part, for two independent add chains
-    float m[2][QB], r[2][QB];
-#pragma unroll
-    for (int q = 0; q < QB; ++q) { m[0][q] = m[1][q] = 0.f; r[0][q] = r[1][q] = 0.f; }
-#pragma unroll
-    for (int gi = 0; gi < L::NPI; ++gi) {
-      const int off = L::KB * gi;
-      const int wd = off >> 5, sh = off & 31;
-      uint32_t v;
-      if (sh + L::KB <= 32) {
-        v = (w[wd] >> sh) & (L::NV - 1);
-      } else {
-        v = __funnelshift_r(w[wd], w[wd + 1], sh) & (L::NV - 1);
-      }
-#pragma unroll
-      for (int q = 0; q < QB; ++q) m[gi & 1][q] += lut[q * L::PER_Q + gi * L::NV + v];
-    }
-#pragma unroll
-    for (int gi = 0; gi < L::NPS; ++gi) {
-      const uint32_t v = (ws[gi >> 3] >> (4 * (gi & 7))) & 15u;
-#pragma unroll
-      for (int q = 0; q < QB; ++q) r[gi & 1][q] += lut[q * L::PER_Q + L::NPI * L::NV + gi * 16 + v];
-    }
-    float mm[QB], rr[QB];
-#pragma unroll
-    for (int q = 0; q < QB; ++q) { mm[q] = m[0][q] + m[1][q]; rr[q] = r[0][q] + r[1][q]; }
-    store_scores<QB>(scores, mm, rr, kappa * g, p, b0, B, S, s);
-  }
+  lut_score_keys<BITS, QB>(lut, idx_plane, sign_plane, gamma_f16, scores, k0, k1, first, kT, k_end,
+                           p, b0, B, S, kappa);
+  cluster_wait();
 }
 
+// One launch of the fused kernel with clusters of CS CTAs.  The grid gets as many
+// clusters per (problem, query tile) unit as the co-resident capacity holds for
+// every unit at once (at least one), and no more than leave a CTA 64 keys.
+template <int BITS, int QB, int CS, typename QT>
+cudaError_t launch_fused_cs(const QT* Q, const float* Pi, const float* S_mat, int H,
+                            const uint8_t* idx_plane, const uint8_t* sign_plane,
+                            const uint16_t* gamma_f16, const float* codebook, float* scores,
+                            int P, int B, int S, cudaStream_t st) {
+  constexpr int kT = fused_threads<QB>();
+  constexpr size_t smem = fused_smem_bytes<BITS, QB, CS>();
+  auto kernel = solve_packed_lut_kernel<BITS, QB, CS, QT>;
+  static std::atomic<uint64_t> configured{0};
+  static std::atomic<int> capacity[64];                   // co-resident clusters per device
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CS;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.blockDim = dim3(kT);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  if (!(configured.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    int n = 0;
+    cfg.gridDim = dim3(CS);
+    cfg.numAttrs = 1;
+    e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
+    if (e != cudaSuccess) return e;
+    capacity[dev & 63].store(n > 0 ? n : 1, std::memory_order_relaxed);
+    configured.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  const int qtiles = ceil_div(B, QB);
+  const int64_t units = static_cast<int64_t>(P) * qtiles;
+  const int fill = static_cast<int>(capacity[dev & 63].load(std::memory_order_relaxed) / units);
+  const int most = ceil_div(S, 64 * CS);                  // at least 64 keys a CTA on average
+  const int clusters = fill < most ? fill : most;
+  cfg.gridDim = dim3((clusters < 1 ? 1 : clusters) * CS, qtiles, P);
+  cfg.numAttrs = 2;
+  e = cudaLaunchKernelEx(&cfg, kernel, Q, Pi, S_mat, H, idx_plane, sign_plane, gamma_f16, codebook,
+                         scores, B, S, qjl_scale(128));
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+// Few (problem, query tile) units: clusters of 8 split the transform eight ways.
+// Units enough to fill half the SMs: clusters of 2, whose larger CTAs (128 rows
+// of [Pi; S_mat] each) cost fewer prologues per key.
 template <int BITS, int QB, typename QT>
 cudaError_t launch_fused_qb(const QT* Q, const float* Pi, const float* S_mat, int H,
                             const uint8_t* idx_plane, const uint8_t* sign_plane,
                             const uint16_t* gamma_f16, const float* codebook, float* scores,
                             int P, int B, int S, cudaStream_t st) {
-  constexpr size_t smem = fused_smem_bytes<BITS, QB>();
-  static std::atomic<uint64_t> configured{0};
-  int dev = 0, sms = 148;
+  static std::atomic<int> sms_cache[64];
+  int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  const uint64_t bit = 1ull << (dev & 63);
-  if (!(configured.load(std::memory_order_acquire) & bit)) {
-    e = cudaFuncSetAttribute(solve_packed_lut_kernel<BITS, QB, QT>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  int sms = sms_cache[dev & 63].load(std::memory_order_relaxed);
+  if (sms == 0) {
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    configured.fetch_or(bit, std::memory_order_acq_rel);
+    sms_cache[dev & 63].store(sms, std::memory_order_relaxed);
   }
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int qtiles = ceil_div(B, QB);
-  const int tiles = ceil_div(S, fused_threads<QB>());
-  const int want = ceil_div(static_cast<int64_t>(sms), static_cast<int64_t>(P) * qtiles);
-  dim3 grid(tiles < want ? tiles : (want < 1 ? 1 : want), qtiles, P);
-  solve_packed_lut_kernel<BITS, QB, QT><<<grid, fused_threads<QB>(), smem, st>>>(
-      Q, Pi, S_mat, H, idx_plane, sign_plane, gamma_f16, codebook, scores, B, S, qjl_scale(128));
-  return cudaGetLastError();
+  const int64_t units = static_cast<int64_t>(P) * ceil_div(B, QB);
+  if (2 * units >= sms)
+    return launch_fused_cs<BITS, QB, 2, QT>(Q, Pi, S_mat, H, idx_plane, sign_plane, gamma_f16, codebook,
+                                            scores, P, B, S, st);
+  return launch_fused_cs<BITS, QB, 8, QT>(Q, Pi, S_mat, H, idx_plane, sign_plane, gamma_f16, codebook,
+                                          scores, P, B, S, st);
 }
 
 template <int BITS, typename QT>

@@ -120,12 +120,6 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                : "memory");
 }
-__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&v)[8]) {
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]),
-                 "=r"(v[6]), "=r"(v[7])
-               : "r"(taddr));
-}
 __device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t* v) {
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
                : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
@@ -164,27 +158,36 @@ struct Params {
   float kappa;
 };
 
-// Raw bytes of one key row held in registers between the load and the dequantisation,
-// so that the next tile's loads are in flight while the producer waits for a stage.
-// Producer thread t: row r = t % 128, half t / 128 (0: the code row, 1: the sign row).
+// Raw key bytes held in registers between the load and the dequantisation, so that the
+// next tile's loads are in flight while the producer waits for a stage.
+//
+// Packed layouts: producer thread t owns row r = t % 128 and half t / 128 (0: the code
+// row, 1: the sign row).
+//
+// Unpacked layouts (128-byte code and sign rows): producer warp w, lane l = 8g + j holds
+// for rg, ch in {0, 1} the 16-byte chunk c = 4*ch + g of row r = 64*rg + 8*w + j, of the
+// code rows (v[2*rg + ch]) and of the sign rows (v[4 + 2*rg + ch]).  One load instruction
+// of a warp then reads 64 contiguous bytes of each of 8 consecutive rows (every sector it
+// touches is used whole), and the eight lanes of a quarter-warp store 8 consecutive rows
+// of one core-matrix column (no bank conflict).
 template <int LAYOUT>
 struct RawRow {
   static constexpr int kBits = LAYOUT >= kPacked1 ? LAYOUT - kPacked1 + 1 : 8;
-  static constexpr int kVec = LAYOUT >= kPacked1 ? kBits : 8;   // uint4 per code row
+  static constexpr int kVec = LAYOUT >= kPacked1 ? kBits : 8;
   uint4 v[kVec];
-  float g;       // gamma of the row (sign half only)
-  bool valid;
+  float g[2];    // gamma: of the row (packed, sign half) or of rows r(rg = 0, 1) (unpacked)
+  bool ok[2];    // the row (packed: ok[0]) or rows r(rg) exist (s < S)
 };
 
 template <int LAYOUT>
 __device__ __forceinline__ void load_row(const Params& prm, int p, int kt, RawRow<LAYOUT>& raw) {
-  const int r = threadIdx.x & (kM - 1);
-  const int half = threadIdx.x >> 7;
-  const int s = kt * kM + r;
-  raw.valid = s < prm.S;
-  if (!raw.valid) return;
-  const size_t key = static_cast<size_t>(p) * prm.S + s;
   if constexpr (LAYOUT >= kPacked1) {
+    const int r = threadIdx.x & (kM - 1);
+    const int half = threadIdx.x >> 7;
+    const int s = kt * kM + r;
+    raw.ok[0] = s < prm.S;
+    if (!raw.ok[0]) return;
+    const size_t key = static_cast<size_t>(p) * prm.S + s;
     constexpr int kBits = RawRow<LAYOUT>::kBits;
     if (half == 0) {
       const uint4* src = reinterpret_cast<const uint4*>(prm.idx + key * (16 * kBits));
@@ -192,33 +195,106 @@ __device__ __forceinline__ void load_row(const Params& prm, int p, int kt, RawRo
       for (int i = 0; i < kBits; ++i) raw.v[i] = __ldg(src + i);
     } else {
       raw.v[0] = __ldg(reinterpret_cast<const uint4*>(prm.signs + key * 16));
-      raw.g = __half2float(__ushort_as_half(__ldg(static_cast<const uint16_t*>(prm.gamma) + key)));
+      raw.g[0] = __half2float(__ushort_as_half(__ldg(static_cast<const uint16_t*>(prm.gamma) + key)));
     }
   } else {
-    const uint4* src = reinterpret_cast<const uint4*>((half == 0 ? prm.idx : prm.signs) + key * 128);
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) raw.v[i] = __ldg(src + i);
-    if (half == 1) raw.g = __ldg(static_cast<const float*>(prm.gamma) + key);
+    for (int rg = 0; rg < 2; ++rg) {
+      const int s = kt * kM + 64 * rg + 8 * w + (l & 7);
+      raw.ok[rg] = s < prm.S;
+      if (!raw.ok[rg]) continue;
+      const size_t key = static_cast<size_t>(p) * prm.S + s;
+      const uint4* ci = reinterpret_cast<const uint4*>(prm.idx + key * 128);
+      const uint4* cs = reinterpret_cast<const uint4*>(prm.signs + key * 128);
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        raw.v[2 * rg + ch] = __ldg(ci + 4 * ch + (l >> 3));
+        raw.v[4 + 2 * rg + ch] = __ldg(cs + 4 * ch + (l >> 3));
+      }
+      raw.g[rg] = __ldg(static_cast<const float*>(prm.gamma) + key);
+    }
   }
 }
 
-// Dequantise the row into the X buffer at `xbuf` (shared address): half 0 writes the
-// 128 centroids (core-matrix columns 0..15), half 1 the 128 signs (columns 16..31).
+// Sixteen unpacked codes (one 16-byte chunk, coordinates 16c .. 16c+15) as two 16-byte
+// core-matrix rows of centroids at `dst` (column 2c) and dst + 2048 (column 2c+1).
+template <int LAYOUT>
+__device__ __forceinline__ void store_code_chunk(const Params& prm, uint4 raw, uint32_t dst,
+                                                 const uint32_t* lut, const uint16_t* cbf) {
+  const uint32_t ws[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t word = ws[2 * h + (q >> 1)];
+      const uint32_t b0 = (word >> (16 * (q & 1))) & 0xFFu;
+      const uint32_t b1 = (word >> (16 * (q & 1) + 8)) & 0xFFu;
+      if constexpr (LAYOUT == kUnpackedSmallC) {
+        o[q] = lut[b0 + prm.C * b1];
+      } else {
+        o[q] = static_cast<uint32_t>(cbf[b0]) | (static_cast<uint32_t>(cbf[b1]) << 16);
+      }
+    }
+    st_shared_v4(dst + h * 2048, o[0], o[1], o[2], o[3]);
+  }
+}
+
+// Sixteen unpacked int8 signs as +-mag bf16 (bit 7 of each byte is the sign of sigma).
+__device__ __forceinline__ void store_sign_chunk(uint4 raw, uint32_t mag2, uint32_t dst) {
+  const uint32_t ws[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t u = ws[2 * h + (q >> 1)] >> (16 * (q & 1));   // bytes b0 (low), b1
+      o[q] = mag2 | ((u & 0x80u) << 8) | ((u & 0x8000u) << 16);
+    }
+    st_shared_v4(dst + h * 2048, o[0], o[1], o[2], o[3]);
+  }
+}
+
+// Dequantise into the X buffer at `xbuf` (shared address): centroids in core-matrix
+// columns 0..15, signs times bf16(kappa gamma) in columns 16..31; rows past S are zero.
 template <int LAYOUT>
 __device__ __forceinline__ void store_row(const Params& prm, const RawRow<LAYOUT>& raw,
                                           uint32_t xbuf, const uint32_t* lut,
                                           const uint16_t* cbf) {
   constexpr int kBits = RawRow<LAYOUT>::kBits;
-  const int r = threadIdx.x & (kM - 1);
-  const int half = threadIdx.x >> 7;
-  const uint32_t rowbase = xbuf + r * 16 + (half ? 16 * 2048 : 0);
-  if (!raw.valid) {
+  if constexpr (LAYOUT < kPacked1) {
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
 #pragma unroll
-    for (int kc = 0; kc < 16; ++kc) st_shared_v4(rowbase + kc * 2048, 0, 0, 0, 0);
-    return;
-  }
-  if (half == 0) {
-    if constexpr (LAYOUT >= kPacked1) {
+    for (int rg = 0; rg < 2; ++rg) {
+      const uint32_t rowbase = xbuf + (64 * rg + 8 * w + (l & 7)) * 16;
+      const uint32_t mag = bf16_bits(prm.kappa * raw.g[rg]);      // kappa*gamma >= 0
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        const int c = 4 * ch + (l >> 3);
+        const uint32_t dcode = rowbase + (2 * c) * 2048;
+        const uint32_t dsign = rowbase + (16 + 2 * c) * 2048;
+        if (raw.ok[rg]) {
+          store_code_chunk<LAYOUT>(prm, raw.v[2 * rg + ch], dcode, lut, cbf);
+          store_sign_chunk(raw.v[4 + 2 * rg + ch], mag | (mag << 16), dsign);
+        } else {
+          st_shared_v4(dcode, 0, 0, 0, 0);
+          st_shared_v4(dcode + 2048, 0, 0, 0, 0);
+          st_shared_v4(dsign, 0, 0, 0, 0);
+          st_shared_v4(dsign + 2048, 0, 0, 0, 0);
+        }
+      }
+    }
+  } else {
+    const int r = threadIdx.x & (kM - 1);
+    const int half = threadIdx.x >> 7;
+    const uint32_t rowbase = xbuf + r * 16 + (half ? 16 * 2048 : 0);
+    if (!raw.ok[0]) {
+#pragma unroll
+      for (int kc = 0; kc < 16; ++kc) st_shared_v4(rowbase + kc * 2048, 0, 0, 0, 0);
+      return;
+    }
+    if (half == 0) {
       constexpr int kWords = 4 * kBits;
       uint32_t w[kWords + 1];
 #pragma unroll
@@ -237,52 +313,14 @@ __device__ __forceinline__ void store_row(const Params& prm, const RawRow<LAYOUT
                      lut[(v >> (4 * kBits)) & kPm], lut[(v >> (6 * kBits)) & kPm]);
       }
     } else {
-#pragma unroll
-      for (int c2 = 0; c2 < 8; ++c2) {                  // 16 codes per 16-byte vector
-        const uint32_t ws[4] = {raw.v[c2].x, raw.v[c2].y, raw.v[c2].z, raw.v[c2].w};
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t o[4];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint32_t word = ws[2 * h + (q >> 1)];
-            const uint32_t b0 = (word >> (16 * (q & 1))) & 0xFFu;
-            const uint32_t b1 = (word >> (16 * (q & 1) + 8)) & 0xFFu;
-            if constexpr (LAYOUT == kUnpackedSmallC) {
-              o[q] = lut[b0 + prm.C * b1];
-            } else {
-              o[q] = static_cast<uint32_t>(cbf[b0]) | (static_cast<uint32_t>(cbf[b1]) << 16);
-            }
-          }
-          st_shared_v4(rowbase + (2 * c2 + h) * 2048, o[0], o[1], o[2], o[3]);
-        }
-      }
-    }
-  } else {
-    const uint32_t mag = bf16_bits(prm.kappa * raw.g);      // kappa*gamma >= 0
-    const uint32_t mag2 = mag | (mag << 16);
-    if constexpr (LAYOUT >= kPacked1) {
+      const uint32_t mag = bf16_bits(prm.kappa * raw.g[0]);      // kappa*gamma >= 0
+      const uint32_t mag2 = mag | (mag << 16);
       const uint32_t ws[4] = {~raw.v[0].x, ~raw.v[0].y, ~raw.v[0].z, ~raw.v[0].w};  // 1 = sigma -1
 #pragma unroll
       for (int kc = 0; kc < 16; ++kc) {
         const uint32_t nb = (ws[kc >> 2] >> (8 * (kc & 3))) & 0xFFu;
         st_shared_v4(rowbase + kc * 2048, sign_pair(mag2, nb, 0), sign_pair(mag2, nb, 1),
                      sign_pair(mag2, nb, 2), sign_pair(mag2, nb, 3));
-      }
-    } else {
-#pragma unroll
-      for (int c2 = 0; c2 < 8; ++c2) {
-        const uint32_t ws[4] = {raw.v[c2].x, raw.v[c2].y, raw.v[c2].z, raw.v[c2].w};
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t o[4];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint32_t u = ws[2 * h + (q >> 1)] >> (16 * (q & 1));   // bytes b0 (low), b1
-            o[q] = mag2 | ((u & 0x80u) << 8) | ((u & 0x8000u) << 16);
-          }
-          st_shared_v4(rowbase + (2 * c2 + h) * 2048, o[0], o[1], o[2], o[3]);
-        }
       }
     }
   }
@@ -338,12 +376,16 @@ __global__ void __launch_bounds__(Cfg<EPIW>::kThreads, (EPIW == 4 ? 2 : 1)) scor
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     abort_flag = 0;
   }
-  // Producers request their first tiles' rows before the rest of the set-up, so the
-  // loads are in flight while TMEM and the query operand are prepared.
+  // With the query operand prepared by the transform (one bulk copy), producers request
+  // their first tile's rows before the rest of the set-up, so the loads are in flight
+  // while the transform finishes and TMEM is prepared.  Without it, the rows are
+  // requested only after A and T have been read and converted: issued together, the
+  // flood of key rows would hold up those reads and with them the whole set-up.
   constexpr bool kTwoDeep = false;   // one tile ahead: the register budget of 800 threads
   RawRow<LAYOUT> raw0, raw1;
   const int gx = gridDim.x;
-  if (warp < kProducerThreads / 32) {
+  const bool rows_early = prm.Ybf != nullptr;
+  if (rows_early && warp < kProducerThreads / 32) {
     if (static_cast<int>(blockIdx.x) < prm.key_tiles) load_row<LAYOUT>(prm, p, blockIdx.x, raw0);
     if (kTwoDeep && static_cast<int>(blockIdx.x) + gx < prm.key_tiles)
       load_row<LAYOUT>(prm, p, blockIdx.x + gx, raw1);
@@ -374,7 +416,8 @@ __global__ void __launch_bounds__(Cfg<EPIW>::kThreads, (EPIW == 4 ? 2 : 1)) scor
   } else {  // Y: query n (row) x 256 K, bf16, core-matrix layout; queries past B are zero
     const uint32_t ybase = smem_u32(Yp);
     const int ngroups = NT / 8;
-    constexpr int kBatch = 2;
+    // pairs of float4 in flight per thread (fewer next to the larger unpacked key registers)
+    constexpr int kBatch = LAYOUT >= kPacked1 ? 4 : 2;
     for (int e0 = tid; e0 < NT * 32; e0 += kThreads * kBatch) {
       float4 lo[kBatch], hi[kBatch];
 #pragma unroll
@@ -414,6 +457,11 @@ __global__ void __launch_bounds__(Cfg<EPIW>::kThreads, (EPIW == 4 ? 2 : 1)) scor
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (!rows_early && warp < kProducerThreads / 32) {
+    if (static_cast<int>(blockIdx.x) < prm.key_tiles) load_row<LAYOUT>(prm, p, blockIdx.x, raw0);
+    if (kTwoDeep && static_cast<int>(blockIdx.x) + gx < prm.key_tiles)
+      load_row<LAYOUT>(prm, p, blockIdx.x + gx, raw1);
+  }
   const uint32_t tmem = *tslot;
   const uint32_t xaddr0 = smem_u32(X);
   volatile int* abort_v = &abort_flag;
@@ -546,6 +594,9 @@ cudaError_t launch_cfg(const Params& prm, int P, int qtiles, bool after_prepare,
     if (smem < static_cast<int>(need) || smem > optin) return cudaErrorInvalidConfiguration;
     e = cudaFuncSetAttribute(scores_mma_kernel<LAYOUT, EPIW, XS>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(scores_mma_kernel<LAYOUT, EPIW, XS>,
+                             cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return e;
     dyn_bytes[dev & 63].store(smem, std::memory_order_release);
   }

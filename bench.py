@@ -322,7 +322,11 @@ def main():
             "out": torch.empty((w.P, w.B, w.S), device=dev)})
 
     stream = torch.cuda.Stream(dev)
-    fused_single = (w.layout == "packed" and path == "fp32" and w.D == 128 and w.B <= 8)
+    # tq_solve_packed runs one fused kernel for the fp32 path when D = 128, B <= 8 and
+    # the problems fill fewer than half the SMs; otherwise the transform and the scorer
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    fused_single = (w.layout == "packed" and path == "fp32" and w.D == 128 and w.B <= 8
+                    and 2 * w.P < sms)
 
     def solve_call(cp):
         # one step = the fused public entry over the whole workload

@@ -100,7 +100,7 @@ tq_status run_packed(const float* A, const float* T, const uint8_t* idx_plane,
                                            scores, P, B, S, 1 << idx_bits, idx_bits, true,
                                            after_prepare, stream, Ybf));
   return from_cuda(tq::launch_scores_packed_fp32(A, T, idx_plane, sign_plane, gamma_f16, codebook,
-                                                 scores, P, B, S, D, idx_bits, stream));
+                                                 scores, P, B, S, D, idx_bits, after_prepare, stream));
 }
 
 tq_status check_pack_sizes(int64_t n_keys, int D, int bits) {
@@ -205,7 +205,7 @@ tq_status tq_solve_packed(const void* Q, tq_qtype qtype, const uint8_t* idx_plan
   if ((st = check_packed(A, T, idx_plane, sign_plane, gamma_f16, codebook, scores, P, B, S, D,
                          idx_bits, path, &p)) != TQ_OK)
     return st;
-  if (p == TQ_PATH_FP32 && tq::fused_packed_supported(B, D))   // one kernel, workspace untouched
+  if (p == TQ_PATH_FP32 && tq::fused_packed_supported(P, B, D))   // one kernel, workspace untouched
     return from_cuda(tq::launch_solve_packed_fused(Q, qtype, Pi, S_mat, H, idx_plane, sign_plane,
                                                    gamma_f16, codebook, scores, P, B, S,
                                                    idx_bits, stream));

@@ -37,13 +37,16 @@ cudaError_t launch_scores_unpacked_fp32(const float* A, const float* T, const ui
                                         const float* codebook, float* scores, int P, int B,
                                         int S, int D, int C, cudaStream_t st);
 
+// after_prepare: launched right behind this call's query transform on the same
+// stream (programmatic dependent launch; A and T are read after that grid completes).
 cudaError_t launch_scores_packed_fp32(const float* A, const float* T, const uint8_t* idx_plane,
                                       const uint8_t* sign_plane, const uint16_t* gamma_f16,
                                       const float* codebook, float* scores, int P, int B, int S,
-                                      int D, int idx_bits, cudaStream_t st);
+                                      int D, int idx_bits, bool after_prepare, cudaStream_t st);
 
-// Fused query transform + packed fp32 scoring (one kernel), D == 128 and B <= 8.
-bool fused_packed_supported(int B, int D);
+// Fused query transform + packed fp32 scoring (one kernel): D == 128, B <= 8 and
+// fewer problems than half the SMs of the current device.
+bool fused_packed_supported(int P, int B, int D);
 cudaError_t launch_solve_packed_fused(const void* Q, tq_qtype qtype, const float* Pi,
                                       const float* S_mat, int H, const uint8_t* idx_plane,
                                       const uint8_t* sign_plane, const uint16_t* gamma_f16,

@@ -374,66 +374,101 @@ __device__ __forceinline__ void prefetch_two_keys(PackedKey<BITS>& k0, PackedKey
     load_packed_key<BITS>(k1, idx_plane, sign_plane, gamma_f16, base + first + stride);
 }
 
+// Stream-K scorer over many (problem, query tile) units: the keys of all units, laid
+// end to end (unit-major), are cut into one equal contiguous range per CTA, so every
+// SM gets the same number of keys however the units divide.  A range crosses unit
+// boundaries at most a few times; at each one the CTA rebuilds its tables from that
+// unit's A and T (read through L1).  When launched right behind the query transform
+// (programmatic dependent launch), the first keys and the codebook are requested
+// before griddepcontrol.wait and A and T after it.
 template <int BITS, int QB>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 2)
 scores_packed_lut_kernel(const float* __restrict__ A, const float* __restrict__ T,
                          const uint8_t* __restrict__ idx_plane,
                          const uint8_t* __restrict__ sign_plane,
                          const uint16_t* __restrict__ gamma_f16,
                          const float* __restrict__ codebook, float* __restrict__ scores, int B,
-                         int S, float kappa) {
+                         int S, int qtiles, int64_t total, float kappa) {
   extern __shared__ __align__(16) float smem[];
   float* lut = smem;                      // [QB][NPI*NV + NPS*16]
-  const int p = blockIdx.z;
-  const int b0 = blockIdx.y * QB;
-  const int stride = gridDim.x * blockDim.x;
-  const int first = blockIdx.x * blockDim.x + threadIdx.x;
-
-  // the first two keys' rows are requested before the tables are built
-  PackedKey<BITS> k0, k1;
-  prefetch_two_keys<BITS>(k0, k1, idx_plane, sign_plane, gamma_f16, p, first, stride, S, S);
-
-  // A and T are read through L1; rows of queries past B give zero tables
+  const int64_t per = (total + gridDim.x - 1) / gridDim.x;
+  int64_t w = min(static_cast<int64_t>(blockIdx.x) * per, total);
+  const int64_t wend = min(w + per, total);
   float cv[LutShape<BITS>::G];
   table_centroids<BITS>(codebook, cv);
-  build_luts<BITS, QB, 256>(
-      [&](int q, int e) {
-        const bool live = b0 + q < B;
-        const size_t row = (static_cast<size_t>(p) * B + (live ? b0 + q : b0)) * 128;
-        const float x = e < 128 ? __ldg(A + row + e) : __ldg(T + row + e - 128);
-        return live ? x : 0.f;
-      },
-      lut, cv);
-  __syncthreads();
-  lut_score_keys<BITS, QB>(lut, idx_plane, sign_plane, gamma_f16, scores, k0, k1, first, stride, S,
-                           p, b0, B, S, kappa);
+  bool waited = false;
+  while (w < wend) {
+    const int u = static_cast<int>(w / S);
+    const int sb = static_cast<int>(w - static_cast<int64_t>(u) * S);
+    const int se = static_cast<int>(min(static_cast<int64_t>(S), sb + (wend - w)));
+    const int p = u / qtiles;
+    const int b0 = (u - p * qtiles) * QB;
+    const int first = sb + static_cast<int>(threadIdx.x);
+    // the segment's first two keys are requested before its tables are built
+    PackedKey<BITS> k0, k1;
+    prefetch_two_keys<BITS>(k0, k1, idx_plane, sign_plane, gamma_f16, p, first, 256, se, S);
+    if (!waited) {
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      waited = true;
+    }
+    __syncthreads();                      // the previous segment's tables are no longer read
+    build_luts<BITS, QB, 256>(
+        [&](int q, int e) {
+          const bool live = b0 + q < B;
+          const size_t row = (static_cast<size_t>(p) * B + (live ? b0 + q : b0)) * 128;
+          const float x = e < 128 ? __ldg(A + row + e) : __ldg(T + row + e - 128);
+          return live ? x : 0.f;
+        },
+        lut, cv);
+    __syncthreads();
+    lut_score_keys<BITS, QB>(lut, idx_plane, sign_plane, gamma_f16, scores, k0, k1, first, 256, se,
+                             p, b0, B, S, kappa);
+    w += se - sb;
+  }
 }
 
 template <int BITS, int QB>
 cudaError_t launch_lut_qb(const float* A, const float* T, const uint8_t* idx_plane,
                           const uint8_t* sign_plane, const uint16_t* gamma_f16,
                           const float* codebook, float* scores, int P, int B, int S,
-                          cudaStream_t st) {
+                          bool after_prepare, cudaStream_t st) {
   using L = LutShape<BITS>;
   const size_t smem = static_cast<size_t>(QB) * L::PER_Q * sizeof(float);
-  static std::atomic<uint64_t> configured{0};
-  int dev = 0, sms = 148;
+  auto kernel = scores_packed_lut_kernel<BITS, QB>;
+  static std::atomic<int> slots[64];      // co-resident CTAs per device
+  int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  const uint64_t bit = 1ull << (dev & 63);
-  if (smem > 48 * 1024 && !(configured.load(std::memory_order_acquire) & bit)) {
-    e = cudaFuncSetAttribute(scores_packed_lut_kernel<BITS, QB>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  int n = slots[dev & 63].load(std::memory_order_acquire);
+  if (n == 0) {
+    if (smem > 48 * 1024) {
+      e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+      if (e != cudaSuccess) return e;
+    }
+    int sms = 0, per_sm = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    configured.fetch_or(bit, std::memory_order_acq_rel);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 256, smem);
+    if (e != cudaSuccess) return e;
+    n = sms * (per_sm > 0 ? per_sm : 1);
+    slots[dev & 63].store(n, std::memory_order_release);
   }
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int qtiles = ceil_div(B, QB);
-  const int tiles = ceil_div(S, 256);
-  const int want = ceil_div(8LL * sms, static_cast<int64_t>(P) * qtiles);
-  dim3 grid(tiles < want ? tiles : (want < 1 ? 1 : want), qtiles, P);
-  scores_packed_lut_kernel<BITS, QB><<<grid, 256, smem, st>>>(
-      A, T, idx_plane, sign_plane, gamma_f16, codebook, scores, B, S, qjl_scale(128));
+  const int64_t total = static_cast<int64_t>(P) * qtiles * S;
+  const int64_t want = (total + 255) / 256;             // at least a key per thread
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(want < n ? want : n));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = after_prepare ? 1 : 0;
+  e = cudaLaunchKernelEx(&cfg, kernel, A, T, idx_plane, sign_plane, gamma_f16, codebook, scores, B, S,
+                         qtiles, total, qjl_scale(128));
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -441,11 +476,11 @@ template <int BITS>
 cudaError_t launch_lut_bits(const float* A, const float* T, const uint8_t* idx_plane,
                             const uint8_t* sign_plane, const uint16_t* gamma_f16,
                             const float* codebook, float* scores, int P, int B, int S,
-                            cudaStream_t st) {
-  if (B <= 1) return launch_lut_qb<BITS, 1>(A, T, idx_plane, sign_plane, gamma_f16, codebook, scores, P, B, S, st);
-  if (B <= 2) return launch_lut_qb<BITS, 2>(A, T, idx_plane, sign_plane, gamma_f16, codebook, scores, P, B, S, st);
-  if (B <= 4 || BITS == 3) return launch_lut_qb<BITS, 4>(A, T, idx_plane, sign_plane, gamma_f16, codebook, scores, P, B, S, st);
-  return launch_lut_qb<BITS, 8>(A, T, idx_plane, sign_plane, gamma_f16, codebook, scores, P, B, S, st);
+                            bool after_prepare, cudaStream_t st) {
+  if (B <= 1) return launch_lut_qb<BITS, 1>(A, T, idx_plane, sign_plane, gamma_f16, codebook, scores, P, B, S, after_prepare, st);
+  if (B <= 2) return launch_lut_qb<BITS, 2>(A, T, idx_plane, sign_plane, gamma_f16, codebook, scores, P, B, S, after_prepare, st);
+  if (B <= 4 || BITS == 3) return launch_lut_qb<BITS, 4>(A, T, idx_plane, sign_plane, gamma_f16, codebook, scores, P, B, S, after_prepare, st);
+  return launch_lut_qb<BITS, 8>(A, T, idx_plane, sign_plane, gamma_f16, codebook, scores, P, B, S, after_prepare, st);
 }
 
 
@@ -735,28 +770,11 @@ cudaError_t launch_fused_cs(const QT* Q, const float* Pi, const float* S_mat, in
   return cudaGetLastError();
 }
 
-// Few (problem, query tile) units: clusters of 8 split the transform eight ways.
-// Units enough to fill half the SMs: clusters of 2, whose larger CTAs (128 rows
-// of [Pi; S_mat] each) cost fewer prologues per key.
 template <int BITS, int QB, typename QT>
 cudaError_t launch_fused_qb(const QT* Q, const float* Pi, const float* S_mat, int H,
                             const uint8_t* idx_plane, const uint8_t* sign_plane,
                             const uint16_t* gamma_f16, const float* codebook, float* scores,
                             int P, int B, int S, cudaStream_t st) {
-  static std::atomic<int> sms_cache[64];
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  int sms = sms_cache[dev & 63].load(std::memory_order_relaxed);
-  if (sms == 0) {
-    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    sms_cache[dev & 63].store(sms, std::memory_order_relaxed);
-  }
-  const int64_t units = static_cast<int64_t>(P) * ceil_div(B, QB);
-  if (2 * units >= sms)
-    return launch_fused_cs<BITS, QB, 2, QT>(Q, Pi, S_mat, H, idx_plane, sign_plane, gamma_f16, codebook,
-                                            scores, P, B, S, st);
   return launch_fused_cs<BITS, QB, 8, QT>(Q, Pi, S_mat, H, idx_plane, sign_plane, gamma_f16, codebook,
                                           scores, P, B, S, st);
 }
@@ -842,12 +860,12 @@ cudaError_t launch_scores_unpacked_fp32(const float* A, const float* T, const ui
 cudaError_t launch_scores_packed_fp32(const float* A, const float* T, const uint8_t* idx_plane,
                                       const uint8_t* sign_plane, const uint16_t* gamma_f16,
                                       const float* codebook, float* scores, int P, int B, int S,
-                                      int D, int idx_bits, cudaStream_t st) {
+                                      int D, int idx_bits, bool after_prepare, cudaStream_t st) {
   if (D == 128) {
     switch (idx_bits) {
-      case 1: return launch_lut_bits<1>(A, T, idx_plane, sign_plane, gamma_f16, codebook, scores, P, B, S, st);
-      case 2: return launch_lut_bits<2>(A, T, idx_plane, sign_plane, gamma_f16, codebook, scores, P, B, S, st);
-      default: return launch_lut_bits<3>(A, T, idx_plane, sign_plane, gamma_f16, codebook, scores, P, B, S, st);
+      case 1: return launch_lut_bits<1>(A, T, idx_plane, sign_plane, gamma_f16, codebook, scores, P, B, S, after_prepare, st);
+      case 2: return launch_lut_bits<2>(A, T, idx_plane, sign_plane, gamma_f16, codebook, scores, P, B, S, after_prepare, st);
+      default: return launch_lut_bits<3>(A, T, idx_plane, sign_plane, gamma_f16, codebook, scores, P, B, S, after_prepare, st);
     }
   }
   switch (idx_bits) {
@@ -861,7 +879,21 @@ cudaError_t launch_scores_packed_fp32(const float* A, const float* T, const uint
 
 namespace tq {
 
-bool fused_packed_supported(int B, int D) { return D == 128 && B >= 1 && B <= 8; }
+// The fused kernel gives every (problem, query tile) unit a cluster of 8 CTAs; with
+// problems enough to fill half the SMs, the transform kernel followed by the
+// stream-K scorer balances the SMs better.
+bool fused_packed_supported(int P, int B, int D) {
+  if (D != 128 || B < 1 || B > 8) return false;
+  static std::atomic<int> sms_cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  int sms = sms_cache[dev & 63].load(std::memory_order_relaxed);
+  if (sms == 0) {
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+    sms_cache[dev & 63].store(sms, std::memory_order_relaxed);
+  }
+  return 2 * static_cast<int64_t>(P) < sms;
+}
 
 cudaError_t launch_solve_packed_fused(const void* Q, tq_qtype qtype, const float* Pi,
                                       const float* S_mat, int H, const uint8_t* idx_plane,

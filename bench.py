@@ -46,7 +46,13 @@ FALLBACK_HBM_GBS = 6800.0
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the scoring kernel, from
 # the ncu captures summarised under profiles/, keyed by (workload, path, kernel source
 # fingerprint).  A changed kernel source makes the figure stale and it is reported null.
-NCU_TRAFFIC = {}
+# Writes that were still in L2 when the kernel ended are not in the figure.
+NCU_TRAFFIC = {
+    ("c1", "bf16_mma", "7ce1b9e87f60"): 8849152,      # scores_mma_kernel, unpacked, lite
+    ("c2", "fp32", "7ce1b9e87f60"): 6705920,          # solve_packed_lut_kernel, cluster of 8
+    ("c3", "fp32", "7ce1b9e87f60"): 256595968,        # scores_packed_lut_kernel, stream-K
+    ("c4", "bf16_mma", "7ce1b9e87f60"): 89685760,     # scores_mma_kernel, packed 3-bit, full
+}
 
 
 def parse_args():
@@ -131,13 +137,19 @@ def kernel_fingerprint() -> str:
 # ---------------------------------------------------------------------------
 
 class ClockSampler:
-    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+    """nvidia-smi sampling every 50 ms in the background.  Each line is stamped with its
+    arrival time; the timed region is bracketed by samples (the sampler is running
+    before the region starts and has delivered a line after it ends), so even a region
+    shorter than the sampling interval gets the samples nearest to it."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index: int):
+        import threading
         self.proc = None
-        self.t0 = time.time()
+        self.lines = []
+        self.cv = threading.Condition()
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
@@ -145,25 +157,51 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
+            return
+        self.reader = threading.Thread(target=self._read, daemon=True)
+        self.reader.start()
+        self._wait_for(lambda: len(self.lines) > 0, 10.0)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            with self.cv:
+                self.lines.append((time.time(), line))
+                self.cv.notify_all()
+
+    def _wait_for(self, pred, timeout):
+        deadline = time.time() + timeout
+        with self.cv:
+            while not pred() and time.time() < deadline:
+                self.cv.wait(timeout=0.05)
 
     def stop(self, region):
+        empty = {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "samples_in_region": 0}
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+            return empty
+        t_lo, t_hi = region
+        self._wait_for(lambda: any(t >= t_hi for t, _ in self.lines), 2.0)
         self.proc.terminate()
-        out, _ = self.proc.communicate(timeout=10)
+        try:
+            self.proc.wait(timeout=10)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        with self.cv:
+            stamped = list(self.lines)
         rows = []
-        for line in out.strip().splitlines():
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 8:
+        for t, line in stamped:
+            parts = [q.strip() for q in line.split(",")]
+            if len(parts) < 7:
                 continue
             try:
-                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
-                rows.append((ts, float(parts[1]), float(parts[2]), parts[4:8]))
+                rows.append((t, float(parts[0]), float(parts[1]), parts[3:7]))
             except ValueError:
                 continue
-        t_lo, t_hi = region
-        inside = [r for r in rows if t_lo - 1.0 <= r[0] <= t_hi + 1.0]
-        use = inside or rows
+        if not rows:
+            return empty
+        inside = [r for r in rows if t_lo <= r[0] <= t_hi]
+        before = [r for r in rows if r[0] < t_lo][-1:]
+        after = [r for r in rows if r[0] > t_hi][:1]
+        use = inside + before + after if inside else before + after
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in use for i, v in enumerate(r[3]) if v.lower() == "active"})
         return {"sm_mhz": statistics.median(r[1] for r in use) if use else None,

@@ -224,6 +224,31 @@ def test_c4_prefill_fp32_path_sampled(tq):
     assert_fp32(out[p, b, s], c.expected_sampled(p, b, s))
 
 
+def test_fused_solve_many_keys_per_thread(tq):
+    """One problem with far more keys than the fused kernel's threads: every thread walks
+    several keys of its CTA's range (two in flight), S is ragged, queries are bf16."""
+    c = Case(1, 1, 2, 400_001, 128, 3, seed=91, gamma_dtype="f16", q_dtype="bf16")
+    ip, sp = c.packed()
+    out = tq.solve_packed(q_tensor(c), dev(ip), dev(sp), f16(c.gamma), dev(c.Pi), dev(c.S_mat), dev(c.cb),
+                          c.bits, path="fp32").cpu().numpy()
+    p, b, s = _sample(c, 20000, 5)
+    assert_fp32(out[p, b, s], c.expected_sampled(p, b, s))
+
+
+def test_stream_k_ranges_cross_problems(tq):
+    """Enough problems for the transform + stream-K scorer: CTA key ranges start and end
+    inside problems, S is not a multiple of the block, and heads repeat every 4 problems."""
+    c = Case(100, 4, 3, 1001, 128, 2, seed=92, gamma_dtype="f16")
+    ip, sp = c.packed()
+    Qt = q_tensor(c)
+    out = tq.solve_packed(Qt, dev(ip), dev(sp), f16(c.gamma), dev(c.Pi), dev(c.S_mat), dev(c.cb), c.bits,
+                          path="fp32").cpu().numpy()
+    assert_fp32(out, c.expected())
+    A, T = tq.prepare_queries(Qt, dev(c.Pi), dev(c.S_mat))
+    direct = tq.scores_packed(A, T, dev(ip), dev(sp), f16(c.gamma), dev(c.cb), c.bits, path="fp32").cpu().numpy()
+    assert_fp32(direct, c.expected())
+
+
 # ---------------------------------------------------------------------------
 # properties
 # ---------------------------------------------------------------------------

@@ -35,6 +35,9 @@
 // TMEM is still released.
 #include <atomic>
 
+#include <cuda.h>            // CUtensorMap (types only; the encoder comes from the runtime)
+#include <cudaTypedefs.h>
+
 #include "tq_internal.cuh"
 
 namespace tq {
@@ -48,8 +51,10 @@ constexpr int kProducerThreads = 256;   // warps 0-7
 template <int EPIW> struct Cfg {
   static constexpr int kEpilogueThreads = EPIW * 32;
   static constexpr int kMmaWarp = 8 + EPIW;
-  static constexpr int kThreads = kProducerThreads + kEpilogueThreads + 32;
+  // the full configuration has one more warp: the loader of packed key rows
+  static constexpr int kThreads = kProducerThreads + kEpilogueThreads + 32 + (EPIW == 16 ? 32 : 0);
 };
+constexpr int kRawStages = 3;           // packed key-row stages in flight (full configuration)
 constexpr int kMaxN = 128;              // queries per tile
 constexpr int kXBytes = kM * kK * 2;    // 64 KB per key-tile buffer
 constexpr uint32_t kWaitPolls = 1u << 22;
@@ -128,6 +133,9 @@ __device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t* v) {
 __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+__device__ __forceinline__ void st_shared_f32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
@@ -156,6 +164,8 @@ struct Params {
   float* scores;
   int B, S, C, NT, key_tiles, tmem_cols, acc_stages;
   float kappa;
+  int tma_scores;          // smap describes scores as [P][B][S] fp32 (boxes of 128 keys x 32 queries)
+  CUtensorMap smap;        // 64-byte aligned by its type
 };
 
 // Raw key bytes held in registers between the load and the dequantisation, so that the
@@ -339,19 +349,55 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(bar) : "memory");
 }
 
+// ---- named barriers and bulk stores (epilogue of the full configuration) ----
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+// Barrier over `nthreads` threads that also returns the AND of every thread's `pred`.
+__device__ __forceinline__ bool named_bar_and(int id, int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "barrier.red.and.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+// Store one shared-memory box [1][32][128] fp32 to scores[z][y .. y+31][x .. x+127]
+// (the tensor map clips the parts past S and past B).
+__device__ __forceinline__ void tma_store_box(const CUtensorMap* map, int x, int y, int z, uint32_t ssrc) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(z), "r"(ssrc)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 template <int LAYOUT, int EPIW, int XS>
-__global__ void __launch_bounds__(Cfg<EPIW>::kThreads, (EPIW == 4 ? 2 : 1)) scores_mma_kernel(Params prm) {
+__global__ void __launch_bounds__(Cfg<EPIW>::kThreads, (EPIW == 4 ? 2 : 1))
+scores_mma_kernel(const __grid_constant__ Params prm) {
   constexpr int kEpilogueThreads = Cfg<EPIW>::kEpilogueThreads;
   constexpr int kMmaWarp = Cfg<EPIW>::kMmaWarp;
   constexpr int kThreads = Cfg<EPIW>::kThreads;
   extern __shared__ __align__(1024) uint8_t smem[];
-  // [X: XS x 64K][Y NT*512][lut 256 words][cbf 256 halves][13 mbarriers][tmem slot]
+  // [X: XS x 64K][Y NT*512][scores NT*512, full][key rows: kRawStages x 128 x (code row +
+  // sign row), full and packed][lut 256 words][cbf 256 halves][24 mbarriers][tmem slot]
+  constexpr bool kBulkEpilogue = EPIW == 16;
+  constexpr bool kRawTma = kBulkEpilogue && LAYOUT >= kPacked1;   // key rows by the copy engine
+  constexpr int kCodeRow = 16 * RawRow<LAYOUT>::kBits;             // bytes of codes per packed key
+  constexpr int kRawIdx = kM * kCodeRow, kRawSgn = kM * 16;        // bytes per stage
   uint8_t* X = smem;
   uint8_t* Yp = X + XS * kXBytes;
-  uint32_t* lut = reinterpret_cast<uint32_t*>(Yp + prm.NT * kK * 2);
+  float* sbuf = reinterpret_cast<float*>(Yp + prm.NT * kK * 2);   // [NT columns][128 keys]
+  uint8_t* rawp = reinterpret_cast<uint8_t*>(sbuf) + (kBulkEpilogue ? prm.NT * 512 : 0);
+  uint32_t* lut = reinterpret_cast<uint32_t*>(rawp + (kRawTma ? kRawStages * (kRawIdx + kRawSgn) : 0));
   uint16_t* cbf = reinterpret_cast<uint16_t*>(lut + 256);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(cbf + 256);   // x_full[2] x_empty[2] acc_full[4] acc_empty[4] y
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 13);
+  // x_full[2] x_empty[2] acc_full[4] acc_empty[4] y raw_full[3] raw_empty[3]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(cbf + 256);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 24);
   __shared__ int abort_flag;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -361,20 +407,62 @@ __global__ void __launch_bounds__(Cfg<EPIW>::kThreads, (EPIW == 4 ? 2 : 1)) scor
   const uint32_t x_full = smem_u32(bars), x_empty = smem_u32(bars + 2);
   const uint32_t acc_full = smem_u32(bars + 4), acc_empty = smem_u32(bars + 8);
   const uint32_t y_bar = smem_u32(bars + 12);
+  const uint32_t raw_full = smem_u32(bars + 13), raw_empty = smem_u32(bars + 16);
   const int AS = prm.acc_stages;
+  const int gx = gridDim.x;
+  // Stage j of this CTA's packed key rows (tile blockIdx.x + j*gx) into raw stage j % 3:
+  // code rows and sign rows, two bulk copies completing bytes on raw_full.
+  auto issue_rows = [&](int j) {
+    const int kt = static_cast<int>(blockIdx.x) + j * gx;
+    const int n = min(kM, prm.S - kt * kM);
+    const int rs = j % kRawStages;
+    const size_t key0 = static_cast<size_t>(p) * prm.S + static_cast<size_t>(kt) * kM;
+    const uint32_t fb = raw_full + 8 * rs;
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(fb),
+                 "r"(static_cast<uint32_t>(n * (kCodeRow + 16)))
+                 : "memory");
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(rawp + rs * kRawIdx)),
+                 "l"(prm.idx + key0 * kCodeRow), "r"(static_cast<uint32_t>(n * kCodeRow)), "r"(fb)
+                 : "memory");
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(rawp + kRawStages * kRawIdx + rs * kRawSgn)),
+                 "l"(prm.signs + key0 * 16), "r"(static_cast<uint32_t>(n * 16)), "r"(fb)
+                 : "memory");
+  };
 
+  // With packed rows staged by the loader, the single X stage is split by K: barrier 0
+  // guards the centroid columns (producer warps 0-3), barrier 1 the sign columns (warps
+  // 4-7), and the MMA frees each half as soon as its 8 MMAs have read it.
+  constexpr bool kSplitX = kRawTma && XS == 1;
   if (tid == 0) {
-    for (int b = 0; b < XS; ++b) {
-      mbar_init(x_full + 8 * b, kProducerThreads / 32);     // one arrival per producer warp
-      mbar_init(x_empty + 8 * b, 1);
+    if constexpr (kSplitX) {
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(x_full + 8 * b, kProducerThreads / 64);   // one arrival per warp of the half
+        mbar_init(x_empty + 8 * b, 1);
+      }
+    } else {
+      for (int b = 0; b < XS; ++b) {
+        mbar_init(x_full + 8 * b, kProducerThreads / 32);   // one arrival per producer warp
+        mbar_init(x_empty + 8 * b, 1);
+      }
     }
     for (int b = 0; b < 4; ++b) {
       mbar_init(acc_full + 8 * b, 1);
       mbar_init(acc_empty + 8 * b, kEpilogueThreads / 32);  // one arrival per epilogue warp
     }
     mbar_init(y_bar, 1);
+    for (int b = 0; b < kRawStages; ++b) {
+      mbar_init(raw_full + 8 * b, 1);
+      mbar_init(raw_empty + 8 * b, kProducerThreads / 32);
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     abort_flag = 0;
+    // the first stages of key rows are requested at once (the stages start empty); the
+    // copy engine reads them while the rest of the set-up runs
+    if constexpr (kRawTma) {
+      for (int j = 0; j < kRawStages && static_cast<int>(blockIdx.x) + j * gx < prm.key_tiles; ++j) issue_rows(j);
+    }
   }
   // With the query operand prepared by the transform (one bulk copy), producers request
   // their first tile's rows before the rest of the set-up, so the loads are in flight
@@ -383,9 +471,8 @@ __global__ void __launch_bounds__(Cfg<EPIW>::kThreads, (EPIW == 4 ? 2 : 1)) scor
   // flood of key rows would hold up those reads and with them the whole set-up.
   constexpr bool kTwoDeep = false;   // one tile ahead: the register budget of 800 threads
   RawRow<LAYOUT> raw0, raw1;
-  const int gx = gridDim.x;
   const bool rows_early = prm.Ybf != nullptr;
-  if (rows_early && warp < kProducerThreads / 32) {
+  if (!kRawTma && rows_early && warp < kProducerThreads / 32) {
     if (static_cast<int>(blockIdx.x) < prm.key_tiles) load_row<LAYOUT>(prm, p, blockIdx.x, raw0);
     if (kTwoDeep && static_cast<int>(blockIdx.x) + gx < prm.key_tiles)
       load_row<LAYOUT>(prm, p, blockIdx.x + gx, raw1);
@@ -457,7 +544,7 @@ __global__ void __launch_bounds__(Cfg<EPIW>::kThreads, (EPIW == 4 ? 2 : 1)) scor
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (!rows_early && warp < kProducerThreads / 32) {
+  if (!kRawTma && !rows_early && warp < kProducerThreads / 32) {
     if (static_cast<int>(blockIdx.x) < prm.key_tiles) load_row<LAYOUT>(prm, p, blockIdx.x, raw0);
     if (kTwoDeep && static_cast<int>(blockIdx.x) + gx < prm.key_tiles)
       load_row<LAYOUT>(prm, p, blockIdx.x + gx, raw1);
@@ -470,14 +557,49 @@ __global__ void __launch_bounds__(Cfg<EPIW>::kThreads, (EPIW == 4 ? 2 : 1)) scor
     // ------------------------------ producers ------------------------------
     auto consume = [&](const RawRow<LAYOUT>& raw, int i) -> bool {
       const int st = i % XS;
-      if (!wait_or_abort(x_empty + 8 * st, ((i / XS) & 1) ^ 1, abort_v)) return false;
+      const int b = kSplitX ? (tid >> 7) : st;          // split: this thread's half of X
+      const uint32_t parity = kSplitX ? ((i & 1) ^ 1) : (((i / XS) & 1) ^ 1);
+      if (!wait_or_abort(x_empty + 8 * b, parity, abort_v)) return false;
       store_row<LAYOUT>(prm, raw, xaddr0 + st * kXBytes, lut, cbf);
       fence_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(x_full + 8 * st);
+      if (lane == 0) mbar_arrive(x_full + 8 * b);
       return true;
     };
-    if constexpr (kTwoDeep) {
+    if constexpr (kRawTma) {
+      // key rows from the shared-memory stages the loader fills; gamma (2 bytes a key,
+      // sign half only) is read from global memory one tile ahead
+      const int r = tid & (kM - 1), half = tid >> 7;
+      auto load_g = [&](int kt) -> float {
+        const int s = kt * kM + r;
+        return half == 1 && s < prm.S
+                   ? __half2float(__ushort_as_half(__ldg(static_cast<const uint16_t*>(prm.gamma) +
+                                                         static_cast<size_t>(p) * prm.S + s)))
+                   : 0.f;
+      };
+      float g_cur = static_cast<int>(blockIdx.x) < prm.key_tiles ? load_g(blockIdx.x) : 0.f;
+      int i = 0;
+      for (int kt = blockIdx.x; kt < prm.key_tiles; kt += gx, ++i) {
+        const float g_next = kt + gx < prm.key_tiles ? load_g(kt + gx) : 0.f;
+        const int rs = i % kRawStages;
+        if (!wait_or_abort(raw_full + 8 * rs, (i / kRawStages) & 1, abort_v)) break;
+        RawRow<LAYOUT> raw;
+        raw.ok[0] = kt * kM + r < prm.S;
+        if (half == 0) {
+#pragma unroll
+          for (int v = 0; v < RawRow<LAYOUT>::kBits; ++v)
+            raw.v[v] = *reinterpret_cast<const uint4*>(rawp + rs * kRawIdx + r * kCodeRow + 16 * v);
+        } else {
+          raw.v[0] = *reinterpret_cast<const uint4*>(rawp + kRawStages * kRawIdx + rs * kRawSgn + r * 16);
+          raw.g[0] = g_cur;
+        }
+        // the rows are in registers: the stage may be refilled
+        __syncwarp();
+        if (lane == 0) mbar_arrive(raw_empty + 8 * rs);
+        g_cur = g_next;
+        if (!consume(raw, i)) break;
+      }
+    } else if constexpr (kTwoDeep) {
       // two register sets: tile i+2 is requested as soon as tile i has been stored
       int i = 0;
       for (int kt = blockIdx.x; kt < prm.key_tiles; kt += 2 * gx, i += 2) {
@@ -502,6 +624,46 @@ __global__ void __launch_bounds__(Cfg<EPIW>::kThreads, (EPIW == 4 ? 2 : 1)) scor
     const int cbeg = (e >> 2) * width;
     const int r = lg * 32 + lane;
     int i = 0;
+    if (kBulkEpilogue && prm.tma_scores) {
+      // Full configuration with a tensor map of the scores.  The four warps of a column
+      // group (one per lane quarter) drain their 32 columns into the shared score tile and
+      // free the TMEM stage at once; one thread of the group then writes the 32 x 128
+      // block with one tensor store, so the scores leave through the copy engine while
+      // the warps go on to the next tile.
+      const int grp = e >> 2;
+      const bool issuer = lg == 0 && lane == 0;
+      const uint32_t sb = smem_u32(sbuf) + cbeg * 512;
+      for (int kt = blockIdx.x; kt < prm.key_tiles; kt += gridDim.x, ++i) {
+        const int as = i % AS;
+        const bool okw = __all_sync(0xffffffffu, wait_or_abort(acc_full + 8 * as, (i / AS) & 1, abort_v));
+        if (issuer) bulk_wait_read();                 // the previous tile has left the buffer
+        // the whole group takes the same branch (and may overwrite the buffer)
+        const bool ok = named_bar_and(1 + grp, 128, okw);
+        tc_fence_after();
+        uint32_t v[32];
+        if (ok) {
+#pragma unroll
+          for (int t = 0; t < 8; ++t) tmem_ld4(tmem + (static_cast<uint32_t>(lg * 32) << 16) + as * NT + cbeg + 4 * t, v + 4 * t);
+          tmem_ld_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(acc_empty + 8 * as);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = 0x7fc00000u;
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j) st_shared_f32(sb + j * 512 + r * 4, v[j]);
+        fence_async_smem();
+        named_bar_sync(1 + grp, 128);
+        if (issuer && q0 + cbeg < prm.B) {
+          tma_store_box(&prm.smap, kt * kM, q0 + cbeg, p, sb);
+          bulk_commit();
+        }
+        if (!ok) break;
+      }
+      if (issuer) bulk_wait_all();
+    } else {
     for (int kt = blockIdx.x; kt < prm.key_tiles; kt += gridDim.x, ++i) {
       const int as = i % AS;
       const int s = kt * kM + r;
@@ -532,7 +694,8 @@ __global__ void __launch_bounds__(Cfg<EPIW>::kThreads, (EPIW == 4 ? 2 : 1)) scor
       __syncwarp();
       if (lane == 0) mbar_arrive(acc_empty + 8 * as);
     }
-  } else {
+    }
+  } else if (warp == kMmaWarp) {
     // -------------------------------- MMA ----------------------------------
     if (lane == 0) {
       const uint32_t yaddr = smem_u32(Yp);
@@ -543,19 +706,53 @@ __global__ void __launch_bounds__(Cfg<EPIW>::kThreads, (EPIW == 4 ? 2 : 1)) scor
       for (int kt = blockIdx.x; kt < prm.key_tiles && y_ready; kt += gridDim.x, ++i) {
         const int st = i % XS;
         const int as = i % AS;
-        if (!wait_or_abort(x_full + 8 * st, (i / XS) & 1, abort_v)) break;
-        if (!wait_or_abort(acc_empty + 8 * as, ((i / AS) & 1) ^ 1, abort_v)) break;
-        tc_fence_after();
         const uint32_t xbuf = xaddr0 + st * kXBytes;
         const uint32_t dm = tmem + as * NT;
+        if constexpr (kSplitX) {
+          // centroid half (K 0..127), then sign half (K 128..255), each freed on its own
+          if (!wait_or_abort(x_full, i & 1, abort_v)) break;
+          if (!wait_or_abort(acc_empty + 8 * as, ((i / AS) & 1) ^ 1, abort_v)) break;
+          tc_fence_after();
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const uint64_t ad = smem_desc(xbuf + k * 2 * 2048, 2048, 128);
-          const uint64_t bd = smem_desc(yaddr + k * 2 * ylbo, ylbo, 128);
-          mma_bf16(dm, ad, bd, idesc, k != 0);
+          for (int k = 0; k < 8; ++k) {
+            const uint64_t ad = smem_desc(xbuf + k * 2 * 2048, 2048, 128);
+            const uint64_t bd = smem_desc(yaddr + k * 2 * ylbo, ylbo, 128);
+            mma_bf16(dm, ad, bd, idesc, k != 0);
+          }
+          mma_commit(x_empty);
+          if (!wait_or_abort(x_full + 8, i & 1, abort_v)) break;
+          tc_fence_after();
+#pragma unroll
+          for (int k = 8; k < 16; ++k) {
+            const uint64_t ad = smem_desc(xbuf + k * 2 * 2048, 2048, 128);
+            const uint64_t bd = smem_desc(yaddr + k * 2 * ylbo, ylbo, 128);
+            mma_bf16(dm, ad, bd, idesc, true);
+          }
+          mma_commit(x_empty + 8);
+        } else {
+          if (!wait_or_abort(x_full + 8 * st, (i / XS) & 1, abort_v)) break;
+          if (!wait_or_abort(acc_empty + 8 * as, ((i / AS) & 1) ^ 1, abort_v)) break;
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const uint64_t ad = smem_desc(xbuf + k * 2 * 2048, 2048, 128);
+            const uint64_t bd = smem_desc(yaddr + k * 2 * ylbo, ylbo, 128);
+            mma_bf16(dm, ad, bd, idesc, k != 0);
+          }
+          mma_commit(x_empty + 8 * st);
         }
-        mma_commit(x_empty + 8 * st);
         mma_commit(acc_full + 8 * as);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------ loader (full configuration, packed rows) ------------------
+    if (kRawTma && lane == 0) {
+      int j = kRawStages;
+      for (int kt = blockIdx.x + kRawStages * gx; kt < prm.key_tiles; kt += gx, ++j) {
+        const int rs = j % kRawStages;
+        if (!wait_or_abort(raw_empty + 8 * rs, ((j / kRawStages) & 1) ^ 1, abort_v)) break;
+        issue_rows(j);
       }
     }
     __syncwarp();
@@ -577,8 +774,10 @@ cudaError_t launch_cfg(const Params& prm, int P, int qtiles, bool after_prepare,
   // the first launch on each device.
   static std::atomic<int> dyn_bytes[64];
   constexpr int kNMax = kLite ? 64 : kMaxN;           // the lite configuration serves NT <= 64
+  constexpr int kCodeRow = 16 * RawRow<LAYOUT>::kBits;
+  constexpr size_t kRaw = (!kLite && LAYOUT >= kPacked1) ? kRawStages * kM * (kCodeRow + 16) : 0;
   constexpr size_t need = XS * static_cast<size_t>(kXBytes) + static_cast<size_t>(kNMax) * kK * 2 +
-                          256 * 4 + 256 * 2 + 13 * 8 + 16;
+                          (kLite ? 0 : static_cast<size_t>(kNMax) * 512) + kRaw + 256 * 4 + 256 * 2 + 24 * 8 + 16;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -628,7 +827,38 @@ cudaError_t launch_layout(const Params& prm, int P, int qtiles, bool after_prepa
   // few tiles per SM: two lighter CTAs per SM run every tile at once
   const int64_t tiles = static_cast<int64_t>(prm.key_tiles) * qtiles * P;
   if (prm.NT <= 64 && tiles <= 4LL * sms) return launch_cfg<LAYOUT, 4, 1>(prm, P, qtiles, after_prepare, sms, st);
-  return launch_cfg<LAYOUT, 16, 2>(prm, P, qtiles, after_prepare, sms, st);
+  return launch_cfg<LAYOUT, 16, 1>(prm, P, qtiles, after_prepare, sms, st);
+}
+
+// Tensor map of the scores [P][B][S] fp32 for the bulk epilogue: boxes of 128 keys x 32
+// queries x 1 problem.  Needs 16-byte row pitch (S % 4 == 0); false when it cannot be
+// built, and the epilogue then stores from registers.
+bool encode_scores_map(CUtensorMap* map, float* scores, int P, int B, int S) {
+  static std::atomic<void*> encode{nullptr};
+  static std::atomic<int> looked{0};
+  if (S % 4 != 0) return false;
+  if (!looked.load(std::memory_order_acquire)) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      fn = nullptr;
+    encode.store(fn, std::memory_order_release);
+    looked.store(1, std::memory_order_release);
+  }
+  auto fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(encode.load(std::memory_order_acquire));
+  if (fn == nullptr) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(B), static_cast<cuuint64_t>(P)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(S) * 4, static_cast<cuuint64_t>(B) * S * 4};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(kM), 32, 1};
+  const cuuint32_t estride[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, scores, dims, strides, box, estride,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -660,6 +890,7 @@ cudaError_t launch_scores_mma(const float* A, const float* T, const uint8_t* idx
   while (cols < prm.acc_stages * prm.NT) cols <<= 1;
   prm.tmem_cols = cols;
   prm.kappa = qjl_scale(128);
+  prm.tma_scores = encode_scores_map(&prm.smap, scores, P, B, S) ? 1 : 0;
   if (!packed) {
     return C <= 16 ? launch_layout<kUnpackedSmallC>(prm, P, qtiles, after_prepare, st)
                    : launch_layout<kUnpackedLargeC>(prm, P, qtiles, after_prepare, st);

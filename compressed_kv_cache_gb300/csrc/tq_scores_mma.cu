@@ -624,8 +624,9 @@ scores_mma_kernel(const __grid_constant__ Params prm) {
     const int cbeg = (e >> 2) * width;
     const int r = lg * 32 + lane;
     int i = 0;
-    if (kBulkEpilogue && prm.tma_scores) {
-      // Full configuration with a tensor map of the scores.  The four warps of a column
+    if (kBulkEpilogue && prm.tma_scores && width == 32) {
+      // Full configuration (128 queries: 32 columns a warp) with a tensor map of the
+      // scores.  The four warps of a column
       // group (one per lane quarter) drain their 32 columns into the shared score tile and
       // free the TMEM stage at once; one thread of the group then writes the 32 x 128
       // block with one tensor store, so the scores leave through the copy engine while
@@ -824,9 +825,9 @@ cudaError_t launch_layout(const Params& prm, int P, int qtiles, bool after_prepa
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  // few tiles per SM: two lighter CTAs per SM run every tile at once
+  // at most two tiles per SM: two lighter CTAs per SM run every tile at once
   const int64_t tiles = static_cast<int64_t>(prm.key_tiles) * qtiles * P;
-  if (prm.NT <= 64 && tiles <= 4LL * sms) return launch_cfg<LAYOUT, 4, 1>(prm, P, qtiles, after_prepare, sms, st);
+  if (prm.NT <= 64 && tiles <= 2LL * sms) return launch_cfg<LAYOUT, 4, 1>(prm, P, qtiles, after_prepare, sms, st);
   return launch_cfg<LAYOUT, 16, 1>(prm, P, qtiles, after_prepare, sms, st);
 }
 

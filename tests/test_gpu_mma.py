@@ -54,6 +54,7 @@ UNPACKED = [  # P, B, S, mse_bits (C = 2^bits)
     (1, 32, 1000, 2),
     (2, 17, 300, 6),        # C = 64: per-code codebook lookup
     (1, 133, 257, 3),       # two query tiles, ragged last tile
+    (1, 32, 40963, 2),      # more tiles than two per SM: full configuration, unpacked rows
 ]
 
 
@@ -72,6 +73,9 @@ PACKED = [  # P, H, B, S, bits
     (2, 2, 128, 300, 3),
     (3, 3, 130, 200, 1),
     (1, 1, 256, 1024, 3),
+    (1, 1, 128, 1027, 2),     # rows not 16-byte aligned: epilogue stores from registers
+    (1, 1, 64, 41037, 2),     # more tiles than two per SM: full configuration with 64 queries
+    (1, 1, 96, 5125, 3),      # full configuration, 96 queries (24 columns an epilogue warp)
 ]
 
 

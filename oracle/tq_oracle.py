@@ -32,10 +32,12 @@ __all__ = [
     "lloyd_max_sphere",
     "nearest_cell",
     "compress_prod",
+    "compress_mse",
     "prepare_queries",
     "scores",
     "scores_from_queries",
     "scores_sampled",
+    "scores_mse",
     "pack_indices",
     "unpack_indices",
     "pack_signs",
@@ -219,6 +221,45 @@ def scores_sampled(A, T, idx_rows, sign_rows, gamma_vals, codebook, b_index) -> 
         res = float(np.dot(T[b], np.asarray(sign_rows[n], dtype=np.float64)))
         out[n] = mse + kappa(D) * float(gamma_vals[n]) * res
     return out
+
+
+# ---------------------------------------------------------------------------
+# MSE-only variant (no residual sketch; one stored norm per key)
+# ---------------------------------------------------------------------------
+
+def compress_mse(keys: np.ndarray, Pi: np.ndarray, codebook: np.ndarray):
+    """TurboQuant-MSE compression of keys of any length ([KB] §3 TurboQuantMSE.quantize).
+
+    For each key k: n = ‖k‖₂, stored as IEEE float16; y = Π (k / n); idx_d = the
+    cell of y_d among the codebook's midpoints (ties to the lower index, as in
+    :func:`compress_prod`).  Π and the codebook are used as stored (float32
+    widened).  Returns ``(idx uint8 [S,D], norm float16 [S])``.
+    """
+    k = np.asarray(keys, dtype=np.float64)
+    P = np.asarray(Pi, dtype=np.float64)
+    c = np.asarray(codebook, dtype=np.float64)
+    n = np.sqrt(np.sum(k * k, axis=1))
+    y = (k / n[:, np.newaxis]) @ P.T
+    idx = nearest_cell(y, 0.5 * (c[1:] + c[:-1]))
+    return idx.astype(np.uint8), n.astype(np.float16)
+
+
+def scores_mse(A: np.ndarray, idx: np.ndarray, norm: np.ndarray, codebook: np.ndarray,
+               norm_correction: bool = False) -> np.ndarray:
+    """Raw MSE-only scores from the rotated queries A = Π q ([KB] §8 "Kernel view":
+    ⟨q, k̂⟩ = ‖k‖ ⟨Π q, c_idx⟩; §3 TurboQuantMSE.dequantize).
+
+    score[b, s] = norm[s] * sum_d A[b,d] c[idx[s,d]], and with norm correction the
+    codeword is first put back on the unit sphere:
+    score[b, s] = norm[s] * sum_d A[b,d] c[idx[s,d]] / sqrt(sum_d c[idx[s,d]]^2).
+    float64 throughout, from the stored inputs widened exactly.
+    """
+    A = np.asarray(A, dtype=np.float64)
+    cvals = np.asarray(codebook, dtype=np.float64)[np.asarray(idx, dtype=np.int64)]
+    dots = A @ cvals.T
+    if norm_correction:
+        dots = dots / np.sqrt(np.sum(cvals * cvals, axis=1))[np.newaxis, :]
+    return dots * np.asarray(norm, dtype=np.float64)[np.newaxis, :]
 
 
 # ---------------------------------------------------------------------------

@@ -325,3 +325,95 @@ def test_synth_keys_are_unit_and_reproducible():
     q, raw = synth.queries(7, 0, 4, 128, "bf16")
     assert raw.dtype == np.uint16
     assert np.abs(q - synth.queries(7, 0, 4, 128, "f32")[0]).max() <= 2.0 ** -8 * np.abs(q).max()
+
+
+# ---------------------------------------------------------------------------
+# MSE-only variant (kanthi.in §3 TurboQuantMSE, §6 Part 1, §8 "Kernel view")
+# ---------------------------------------------------------------------------
+
+def _mse_pair_estimates(mse_bits, n, seed, D=128, norm_correction=False):
+    """kanthi.in §6 Part 1 protocol for the MSE-only quantizer: est_i = <q_i, k^_i>."""
+    rng = np.random.default_rng(seed)
+    k = rng.standard_normal((n, D))
+    k /= np.linalg.norm(k, axis=1, keepdims=True)
+    q = k + 0.6 * rng.standard_normal((n, D)) / math.sqrt(D)
+    q /= np.linalg.norm(q, axis=1, keepdims=True)
+    Pi = oracle.haar_rotation(rng.standard_normal((D, D))).astype(np.float32)
+    cb = codebook(D, mse_bits)[0].astype(np.float32)
+    idx, nrm = oracle.compress_mse(k, Pi, cb)
+    A = q @ Pi.astype(np.float64).T
+    est = np.concatenate([np.diag(oracle.scores_mse(A[i:i + 256], idx[i:i + 256], nrm[i:i + 256], cb,
+                                                    norm_correction)) for i in range(0, n, 256)])
+    return np.sum(q * k, axis=1), est
+
+
+def test_mse_score_equals_unrotated_reconstruction():
+    """kanthi.in §8: scoring in the rotated domain equals the dot product with the
+    reconstructed key n * Pi^T c_idx (the dequantize route of §3), built here coordinate
+    by coordinate; keys are not unit length, so the stored norm matters."""
+    D, S, B = 8, 6, 3
+    rng = np.random.default_rng(31)
+    keys = rng.standard_normal((S, D)) * rng.uniform(0.5, 3.0, (S, 1))
+    Q = rng.standard_normal((B, D))
+    Pi = oracle.haar_rotation(rng.standard_normal((D, D))).astype(np.float32)
+    cb = codebook(D, 2)[0].astype(np.float32)
+    idx, nrm = oracle.compress_mse(keys, Pi, cb)
+    A = Q @ Pi.astype(np.float64).T
+    for corr in (False, True):
+        got = oracle.scores_mse(A, idx, nrm, cb, norm_correction=corr)
+        for s in range(S):
+            cw = [float(cb[idx[s, d]]) for d in range(D)]
+            scale = math.sqrt(sum(x * x for x in cw)) if corr else 1.0
+            khat = [float(nrm[s]) * sum(float(Pi[d, j]) * cw[d] for d in range(D)) / scale for j in range(D)]
+            for b in range(B):
+                want = sum(Q[b, j] * khat[j] for j in range(D))
+                assert got[b, s] == pytest.approx(want, rel=1e-12, abs=1e-12)
+    # the stored norm is the key's length rounded to float16, the codes the nearest cells
+    assert np.allclose(nrm.astype(np.float64), np.linalg.norm(keys, axis=1), rtol=1e-3)
+    y = (keys / np.linalg.norm(keys, axis=1, keepdims=True)) @ Pi.astype(np.float64).T
+    dist = np.abs(y[:, :, None] - cb.astype(np.float64)[None, None, :])
+    assert np.all(dist[np.arange(S)[:, None], np.arange(D)[None, :], idx] <= dist.min(axis=2) + 1e-15)
+
+
+def test_mse_norm_correction_puts_the_codeword_on_the_sphere():
+    """With norm correction the reconstructed key has exactly the stored length: scored
+    against its own unit direction it returns the stored norm (kanthi.in §3 dequantize)."""
+    D = 16
+    rng = np.random.default_rng(32)
+    keys = rng.standard_normal((5, D)) * 2.5
+    Pi = oracle.haar_rotation(rng.standard_normal((D, D))).astype(np.float32)
+    cb = codebook(D, 3)[0].astype(np.float32)
+    idx, nrm = oracle.compress_mse(keys, Pi, cb)
+    c = cb.astype(np.float64)[idx.astype(np.int64)]
+    u = c / np.linalg.norm(c, axis=1, keepdims=True)          # unit codewords, rotated domain
+    got = oracle.scores_mse(u, idx, nrm, cb, norm_correction=True)
+    assert np.allclose(np.diag(got), nrm.astype(np.float64), rtol=1e-12)
+    plain = oracle.scores_mse(u, idx, nrm, cb, norm_correction=False)
+    assert np.allclose(np.diag(plain), nrm.astype(np.float64) * np.linalg.norm(c, axis=1), rtol=1e-12)
+
+
+def test_mse_slope_table():
+    """kanthi.in §6 Part 1 table: the MSE quantizer shrinks inner products by the printed
+    slopes at 2, 3 and 4 bits."""
+    g = golden("mse_slope.json")
+    for name, row in g["rows"].items():
+        true, est = _mse_pair_estimates(row["mse_bits"], 4096, seed=41 + row["mse_bits"])
+        slope = float(est @ true / (true @ true))
+        resid = est - slope * true
+        se = float(np.std(resid) / math.sqrt(true @ true))
+        assert abs(slope - row["slope"]) < 5 * se + 5e-4 + 2e-3, (name, slope, se)
+        assert np.std(resid) == pytest.approx(row["resid_std"], rel=0.25), name
+
+
+def test_mse_one_bit_shrinkage_closed_form():
+    """At 1 bit the codebook is +-E|y_1| for y uniform on the sphere, so the shrinkage is
+    d E|y_1|^2 = d Gamma(d/2)^2 / (pi Gamma((d+1)/2)^2), which tends to 2/pi (kanthi.in §6)."""
+    D = 128
+    c1 = math.exp(math.lgamma(D / 2) - math.lgamma((D + 1) / 2)) / math.sqrt(math.pi)
+    shrink = D * c1 * c1
+    assert shrink == pytest.approx(golden("mse_slope.json")["one_bit_shrinkage"], abs=4e-3)
+    assert float(codebook(D, 1)[0][1]) == pytest.approx(c1, rel=1e-4)
+    true, est = _mse_pair_estimates(1, 4096, seed=40)
+    slope = float(est @ true / (true @ true))
+    se = float(np.std(est - slope * true) / math.sqrt(true @ true))
+    assert abs(slope - shrink) < 5 * se + 2e-3, (slope, shrink, se)

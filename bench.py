@@ -76,13 +76,16 @@ def parse_args():
 def key_bytes(w) -> int:
     if w.layout == "unpacked":
         return 2 * w.D + (4 if w.gamma_dtype == "f32" else 2)
+    if w.layout == "mse":                 # code plane + norm, no sign plane
+        return w.D * w.mse_bits // 8 + (4 if w.gamma_dtype == "f32" else 2)
     return w.D * w.mse_bits // 8 + w.D // 8 + (4 if w.gamma_dtype == "f32" else 2)
 
 
 def score_kernel_bytes(w) -> int:
     """Algorithmic bytes of one scoring launch: the compressed cache once, the
-    scores once, A and T once, the codebook."""
-    return (w.P * w.S * key_bytes(w) + 4 * w.P * w.B * w.S + 2 * 4 * w.P * w.B * w.D + 4 * w.C)
+    scores once, A and T once (A only for the MSE-only scorer), the codebook."""
+    n_at = 1 if w.layout == "mse" else 2
+    return (w.P * w.S * key_bytes(w) + 4 * w.P * w.B * w.S + n_at * 4 * w.P * w.B * w.D + 4 * w.C)
 
 
 def fused_kernel_extra_bytes(w) -> int:
@@ -237,6 +240,11 @@ def build_device_workload(w, tq, torch, dev):
     cache = {"gamma": gamma}
     if w.layout == "unpacked":
         cache["idx"], cache["signs"] = idx, sg
+    elif w.layout == "mse":
+        # unit keys: the codes of TurboQuant_prod's MSE stage are the MSE-only codes
+        # (same rotation, codebook and cells) and every stored norm is 1
+        cache = {"idx": tq.pack_indices(idx, w.mse_bits),
+                 "norm": torch.ones((w.P, w.S), dtype=torch.float16, device=dev)}
     else:
         cache["idx"] = tq.pack_indices(idx, w.mse_bits)
         cache["signs"] = tq.pack_signs(sg)
@@ -245,6 +253,8 @@ def build_device_workload(w, tq, torch, dev):
 
 
 def score_call(tq, w, path, A, T, cache, cb, out):
+    if w.layout == "mse":
+        return tq.scores_mse(A, cache["idx"], cache["norm"], cb, w.mse_bits, norm_correction=True, out=out)
     if w.layout == "unpacked":
         return tq.scores(A, T, cache["idx"], cache["signs"], cache["gamma"], cb, path=path, out=out)
     return tq.scores_packed(A, T, cache["idx"], cache["signs"], cache["gamma"], cb, w.mse_bits,
@@ -261,19 +271,26 @@ def oracle_sample(w, n_keys):
     Pi = oracle.haar_rotation(synth.rotation_seed_matrix(w.seed, 0, w.D)).astype(np.float32)
     S_mat = synth.s_matrix(w.seed, 0, w.D)
     keys = synth.unit_keys(w.seed, 0, 0, n_keys, w.D)
-    idx, sg, gamma = oracle.compress_prod(keys, Pi, S_mat, cb, w.gamma_dtype)
     Q = synth.queries(w.seed, 0, w.B, w.D, w.q_dtype)[0]
-    return oracle, (Q, Pi, S_mat, idx, sg, gamma, cb)
+    if w.layout == "mse":
+        idx, nrm = oracle.compress_mse(keys, Pi, cb)
+
+        def run():
+            A, _ = oracle.prepare_queries(Q, Pi, Pi)
+            return oracle.scores_mse(A, idx, nrm, cb, norm_correction=True)
+        return run
+    idx, sg, gamma = oracle.compress_prod(keys, Pi, S_mat, cb, w.gamma_dtype)
+    return lambda: oracle.scores_from_queries(Q, Pi, S_mat, idx, sg, gamma, cb)
 
 
 def time_oracle(w, seconds, n_keys=None):
     """Scores/s of the oracle (query transform + scoring of B queries over a key sample)."""
     n_keys = n_keys or min(w.S, 4096)
-    oracle, args = oracle_sample(w, n_keys)
+    run = oracle_sample(w, n_keys)
     t0 = time.perf_counter()
     reps = 0
     while True:
-        oracle.scores_from_queries(*args)
+        run()
         reps += 1
         el = time.perf_counter() - t0
         if el >= seconds:
@@ -289,12 +306,12 @@ def run_reference(args, w):
     if rank != 0:
         return
     n_keys = min(w.S, 4096)
-    oracle, ins = oracle_sample(w, n_keys)
+    run = oracle_sample(w, n_keys)
     for _ in range(args.warmup):
-        oracle.scores_from_queries(*ins)
+        run()
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.scores_from_queries(*ins)
+        run()
     el = time.perf_counter() - t0
     value = args.steps * w.B * n_keys / el
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
@@ -367,8 +384,12 @@ def main():
                     and 2 * w.P < sms)
 
     def solve_call(cp):
-        # one step = the fused public entry over the whole workload
-        if w.layout == "unpacked":
+        # one step = the fused public entry over the whole workload (for the MSE-only
+        # variant, which has no fused entry: the query transform and the MSE scorer)
+        if w.layout == "mse":
+            tq.prepare_queries(cp["Q"], Pi, Pi, out=(cp["A"], cp["T"]))
+            score_call(tq, w, path, cp["A"], cp["T"], cp["cache"], cb, cp["out"])
+        elif w.layout == "unpacked":
             tq.solve(cp["Q"], cp["cache"]["idx"], cp["cache"]["signs"], cp["cache"]["gamma"], Pi, S_mat, cb,
                      path=path, workspace=cp["ws"], out=cp["out"])
         else:
@@ -464,13 +485,15 @@ def main():
         hostQ = Q0.cpu().pin_memory()
         hcache = {k: v.cpu().pin_memory() for k, v in cache0.items()}
         hPi, hS, hcb = Pi.cpu().pin_memory(), S_mat.cpu().pin_memory(), cb.cpu().pin_memory()
+        mse = w.layout == "mse"            # no S_mat: the MSE-only path needs Pi alone
         hout = torch.empty((w.P, w.B, w.S), dtype=torch.float32).pin_memory()
         dQ, dcache = torch.empty_like(Q0), {k: torch.empty_like(v) for k, v in cache0.items()}
         dPi, dS, dcb = torch.empty_like(Pi), torch.empty_like(S_mat), torch.empty_like(cb)
         dout = torch.empty((w.P, w.B, w.S), device=dev)
         ws = torch.empty(tq.workspace_bytes(w.P, w.B, w.D), dtype=torch.uint8, device=dev)
         h2d = (hostQ.numel() * hostQ.element_size() + sum(v.numel() * v.element_size() for v in hcache.values())
-               + (hPi.numel() + hS.numel() + hcb.numel()) * 4)
+               + (hPi.numel() + (0 if mse else hS.numel()) + hcb.numel()) * 4)
+        dA, dT = torch.empty((w.P, w.B, w.D), device=dev), torch.empty((w.P, w.B, w.D), device=dev)
         d2h = hout.numel() * 4
 
         def e2e_step():
@@ -478,9 +501,14 @@ def main():
             for k in dcache:
                 dcache[k].copy_(hcache[k], non_blocking=True)
             dPi.copy_(hPi, non_blocking=True)
-            dS.copy_(hS, non_blocking=True)
+            if not mse:
+                dS.copy_(hS, non_blocking=True)
             dcb.copy_(hcb, non_blocking=True)
-            if w.layout == "unpacked":
+            if mse:
+                tq.prepare_queries(dQ, dPi, dPi, out=(dA, dT))
+                tq.scores_mse(dA, dcache["idx"], dcache["norm"], dcb, w.mse_bits, norm_correction=True,
+                              out=dout)
+            elif w.layout == "unpacked":
                 tq.solve(dQ, dcache["idx"], dcache["signs"], dcache["gamma"], dPi, dS, dcb, path=path,
                          workspace=ws, out=dout)
             else:

@@ -218,6 +218,20 @@ tq_status tq_solve_packed(const void* Q, tq_qtype qtype, const uint8_t* idx_plan
                     p, stream, true, Y);
 }
 
+tq_status tq_scores_mse(const float* A, const uint8_t* idx_plane, const uint16_t* norm_f16,
+                        const float* codebook, float* scores, int P, int B, int S, int D,
+                        int idx_bits, int norm_correction, cudaStream_t stream) {
+  tq_status st = check_ptrs(A, idx_plane, norm_f16, codebook, scores);
+  if (st != TQ_OK) return st;
+  if (P < 1 || B < 1 || S < 1 || D < 32 || D > 4096) return TQ_ERR_INVALID_VALUE;
+  if (P > kMaxGridYZ || B > kMaxGridYZ || S > INT_MAX - 1024) return TQ_ERR_INVALID_VALUE;
+  if (idx_bits < 1 || idx_bits > 4 || (norm_correction != 0 && norm_correction != 1))
+    return TQ_ERR_INVALID_VALUE;
+  if (D % 32 != 0) return TQ_ERR_UNSUPPORTED;
+  return from_cuda(tq::launch_scores_mse(A, idx_plane, norm_f16, codebook, scores, P, B, S, D,
+                                         idx_bits, norm_correction != 0, stream));
+}
+
 tq_status tq_pack_indices(const uint8_t* K_idx, uint8_t* idx_plane, int64_t n_keys, int D,
                           int bits, cudaStream_t stream) {
   tq_status st = check_ptrs(K_idx, idx_plane);

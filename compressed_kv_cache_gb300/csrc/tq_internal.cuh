@@ -66,6 +66,11 @@ cudaError_t launch_scores_mma(const float* A, const float* T, const uint8_t* idx
                               bool packed, bool after_prepare, cudaStream_t st,
                               const uint16_t* Ybf = nullptr);
 
+// MSE-only scores from A = Pi q, packed codes and fp16 norms (D % 32 == 0, 1-4 bits).
+cudaError_t launch_scores_mse(const float* A, const uint8_t* idx_plane, const uint16_t* norm_f16,
+                              const float* codebook, float* scores, int P, int B, int S, int D,
+                              int idx_bits, bool norm_correction, cudaStream_t st);
+
 cudaError_t launch_pack_indices(const uint8_t* K_idx, uint8_t* plane, int64_t n, int D, int bits,
                                 cudaStream_t st);
 cudaError_t launch_unpack_indices(const uint8_t* plane, uint8_t* K_idx, int64_t n, int D,

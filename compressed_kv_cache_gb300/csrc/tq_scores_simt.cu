@@ -14,6 +14,7 @@
 #include <atomic>
 
 #include "tq_internal.cuh"
+#include "tq_lut.cuh"
 
 namespace tq {
 namespace {
@@ -230,15 +231,6 @@ scores_packed_kernel(const float* __restrict__ A, const float* __restrict__ T,
 // with G = 2 codes per lookup for 2- and 3-bit codes and 4 for 1-bit codes.  A
 // key then costs 64 (1-bit: 32) code lookups and 32 sign lookups per query.
 // ---------------------------------------------------------------------------
-template <int BITS>
-struct LutShape {
-  static constexpr int G = BITS == 1 ? 4 : 2;            // codes per lookup
-  static constexpr int KB = G * BITS;                    // key bits per lookup
-  static constexpr int NV = 1 << KB;                     // entries per code table
-  static constexpr int NPI = 128 / G;                    // code tables per query
-  static constexpr int NPS = 32;                         // sign tables per query (4 signs each)
-  static constexpr int PER_Q = NPI * NV + NPS * 16;      // floats per query
-};
 
 // One key of the packed cache in registers: BITS 16-byte rows of codes, the
 // 16-byte row of signs and the fp16 gamma.
@@ -299,17 +291,6 @@ __device__ __forceinline__ void lut_key_sums(const float* lut, const PackedKey<B
   }
 #pragma unroll
   for (int q = 0; q < QB; ++q) { mm[q] = m[0][q] + m[1][q]; rr[q] = r[0][q] + r[1][q]; }
-}
-
-// Centroids of the table value this thread keeps fixed while it builds tables
-// (value v = thread % NV; code i of v is bits BITS*i .. BITS*i+BITS-1).
-template <int BITS>
-__device__ __forceinline__ void table_centroids(const float* __restrict__ codebook,
-                                                float (&cv)[LutShape<BITS>::G]) {
-  using L = LutShape<BITS>;
-  const int v = threadIdx.x % L::NV;
-#pragma unroll
-  for (int k = 0; k < L::G; ++k) cv[k] = __ldg(codebook + ((v >> (BITS * k)) & ((1 << BITS) - 1)));
 }
 
 // Tables of QB queries from A (a[0..127]) and T (a[128..255]) of each query,

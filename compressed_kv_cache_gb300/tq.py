@@ -41,6 +41,7 @@ _SIGNATURES = {
     "tq_prepare_queries": ([_P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _P], _I),
     "tq_scores": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P], _I),
     "tq_scores_packed": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P], _I),
+    "tq_scores_mse": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P], _I),
     "tq_workspace_bytes": ([_I, _I, _I], _Z),
     "tq_solve": ([_P, _I, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _Z, _I, _P], _I),
     "tq_solve_packed": ([_P, _I, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _Z, _I, _P], _I),
@@ -177,6 +178,22 @@ def scores_packed(A, T, idx_plane, sign_plane, gamma_f16, codebook, idx_bits, pa
         _dev(idx_plane, "idx_plane", (torch.uint8,)), _dev(sign_plane, "sign_plane", (torch.uint8,)),
         _dev(gamma_f16, "gamma_f16", (torch.float16,)), _dev(codebook, "codebook", (torch.float32,)),
         _dev(o, "scores", (torch.float32,)), P, B, S, D, idx_bits, PATHS[path], _stream()))
+    return o if (out is not None or A.dim() == 3) else o.view(B, S)
+
+
+def scores_mse(A, idx_plane, norm_f16, codebook, idx_bits, norm_correction=False, out=None):
+    """MSE-only scores: A = Pi q [P,B,D] fp32, idx_plane uint8 [P,S,D*bits/8] (codes of
+    the rotated unit keys), norm_f16 float16 [P,S] (key lengths)."""
+    P, B, D = _as3(A)
+    S, row = _keys3(idx_plane, P)
+    if row * 8 != D * idx_bits or norm_f16.numel() != P * S:
+        raise ValueError("inconsistent packed key shapes")
+    o = _scores_out(out, P, B, S, A)
+    _check("tq_scores_mse", lib().tq_scores_mse(
+        _dev(A, "A", (torch.float32,)), _dev(idx_plane, "idx_plane", (torch.uint8,)),
+        _dev(norm_f16, "norm_f16", (torch.float16,)), _dev(codebook, "codebook", (torch.float32,)),
+        _dev(o, "scores", (torch.float32,)), P, B, S, D, idx_bits, 1 if norm_correction else 0,
+        _stream()))
     return o if (out is not None or A.dim() == 3) else o.view(B, S)
 
 

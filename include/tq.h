@@ -120,6 +120,32 @@ tq_status tq_scores_packed(const float* A, const float* T, const uint8_t* idx_pl
                            int idx_bits, tq_path path, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
+ * MSE-only variant (TurboQuant-MSE: no residual sketch, one stored norm per key;
+ * kanthi.in "TurboQuant: Rotate-then-Quantize KV Caches at 3 Bits", §3
+ * TurboQuantMSE, §6 on why attention prefers it, §8 "Kernel view: never
+ * un-rotate a key"):
+ *
+ *   score[b,s] = n_s * sum_d A[b,d] c[idx[s,d]]
+ *   score[b,s] = n_s * sum_d A[b,d] c[idx[s,d]] / sqrt(sum_d c[idx[s,d]]^2)
+ *                                           (norm_correction = 1: the codeword
+ *                                            is put back on the unit sphere)
+ *
+ * A         [P,B,D] fp32 = Pi q (the A output of tq_prepare_queries).
+ * idx_plane [P,S,D*idx_bits/8] bytes, the packed code format above, codes
+ *           of the rotated unit key k/||k||.
+ * norm_f16  [P,S] IEEE fp16 key lengths ||k||.
+ * codebook  2^idx_bits fp32 centroids.  scores [P,B,S] fp32.
+ * D % 32 == 0 (32 <= D <= 4096), idx_bits in {1,2,3,4}; fp32 arithmetic
+ * (D = 128 with 1-3 bit codes uses the lookup-table kernel).  Every pointer is
+ * a caller-owned device pointer, 16-byte aligned; nothing is allocated.
+ * Errors: TQ_ERR_INVALID_VALUE (null pointer, size or flag out of range),
+ * TQ_ERR_MISALIGNED, TQ_ERR_UNSUPPORTED (D % 32 != 0), TQ_ERR_LAUNCH.
+ * ---------------------------------------------------------------------- */
+tq_status tq_scores_mse(const float* A, const uint8_t* idx_plane, const uint16_t* norm_f16,
+                        const float* codebook, float* scores, int P, int B, int S, int D,
+                        int idx_bits, int norm_correction, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
  * Fused query transform + scoring: the challenge's `solve` without its
  * per-call cudaMalloc/cudaFree (riteshyadav.xyz, "What the rearrangement
  * saves": its solve "allocates temporary arrays on every call").  The caller

@@ -62,8 +62,9 @@ class Workload:
     S: int
     D: int
     mse_bits: int
-    layout: str          # "unpacked" (uint8 idx + int8 signs) or "packed" (bit planes)
-    gamma_dtype: str     # "f32" or "f16"
+    layout: str          # "unpacked" (uint8 idx + int8 signs), "packed" (bit planes) or
+                         # "mse" (code plane + fp16 norm, the MSE-only variant, no signs)
+    gamma_dtype: str     # "f32" or "f16" (for "mse": the dtype of the stored norm)
     q_dtype: str         # "f32" or "bf16"
 
     @property
@@ -90,6 +91,10 @@ WORKLOADS = {
     # Prefill-chunk scoring over a 4-bit cache (3-bit index + 1-bit sign), bf16 queries.
     "c4": Workload("c4_prefill_B128_S262144_packed4bit", 1004, 1, 1, 128, 262144, 128, 3,
                    "packed", "f16", "bf16"),
+    # MSE-only variant (no sign plane, fp16 norm), single-query decode with 3-bit codes:
+    # 48 + 2 bytes per key, the same as the packed 3-bit cache of c2.
+    "m1": Workload("m1_mse_decode_B1_S131072_3bit", 1005, 1, 1, 1, 131072, 128, 3,
+                   "mse", "f16", "f32"),
 }
 
 

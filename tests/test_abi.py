@@ -92,3 +92,15 @@ def test_binding_refuses_cpu_tensors(L):
     x = torch.zeros(4, 128)
     with pytest.raises(ValueError, match="CUDA"):
         tq.prepare_queries(x, torch.eye(128), torch.eye(128))
+
+
+def test_mse_argument_errors(L):
+    def call(A=FAKE, norm=FAKE, D=128, bits=2, corr=0, S=10):
+        return L.tq_scores_mse(A, FAKE, norm, FAKE, FAKE, 1, 1, S, D, bits, corr, None)
+    assert call(A=None) == 1
+    assert call(norm=ODD) == 3
+    assert call(D=48) == 2                                   # D % 32 != 0
+    assert call(D=16) == 1 and call(D=8192) == 1
+    assert call(bits=0) == 1 and call(bits=5) == 1
+    assert call(corr=2) == 1
+    assert call(S=0) == 1

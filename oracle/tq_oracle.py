@@ -29,6 +29,8 @@ __all__ = [
     "SQRT_HALF_PI",
     "kappa",
     "haar_rotation",
+    "fwht",
+    "hadamard_rotation",
     "lloyd_max_sphere",
     "nearest_cell",
     "compress_prod",
@@ -68,6 +70,37 @@ def haar_rotation(G: np.ndarray) -> np.ndarray:
     Q, R = np.linalg.qr(np.asarray(G, dtype=np.float64))
     col_sign = np.where(np.diag(R) < 0.0, -1.0, 1.0)
     return Q * col_sign[np.newaxis, :]
+
+
+def fwht(x: np.ndarray) -> np.ndarray:
+    """Orthonormal Walsh-Hadamard transform along the last axis (length a power of two),
+    by butterflies ([KB] §2 "randomized Hadamard transform", §3 Hadamard butterfly).
+
+    Stage h = 1, 2, 4, ...: within every block of 2h entries, entry i of the first
+    half and entry i of the second half become (a + b, a - b); the result is divided
+    by sqrt(n), so the transform is its own inverse (Sylvester order).
+    """
+    y = np.array(x, dtype=np.float64, copy=True)
+    n = y.shape[-1]
+    if n < 1 or n & (n - 1):
+        raise ValueError("length must be a power of two")
+    h = 1
+    while h < n:
+        for start in range(0, n, 2 * h):
+            a = y[..., start:start + h].copy()
+            b = y[..., start + h:start + 2 * h].copy()
+            y[..., start:start + h] = a + b
+            y[..., start + h:start + 2 * h] = a - b
+        h *= 2
+    return y / math.sqrt(n)
+
+
+def hadamard_rotation(signs: np.ndarray) -> np.ndarray:
+    """Dense matrix of the randomized Hadamard rotation y = H diag(s) x ([KB] §2-§3
+    RandomizedHadamard): Π[i, j] = H[i, j] s_j with H the orthonormal Walsh-Hadamard
+    matrix, so that Π x = fwht(x * s).  ``signs`` holds +1 / -1."""
+    s = np.asarray(signs, dtype=np.float64)
+    return fwht(np.eye(s.size)).T * s[np.newaxis, :]
 
 
 def nearest_cell(values: np.ndarray, edges: np.ndarray) -> np.ndarray:

@@ -417,3 +417,36 @@ def test_mse_one_bit_shrinkage_closed_form():
     slope = float(est @ true / (true @ true))
     se = float(np.std(est - slope * true) / math.sqrt(true @ true))
     assert abs(slope - shrink) < 5 * se + 2e-3, (slope, shrink, se)
+
+
+# ---------------------------------------------------------------------------
+# randomized Hadamard rotation (kanthi.in §2-§3 RandomizedHadamard)
+# ---------------------------------------------------------------------------
+
+def test_fwht_matches_the_sylvester_matrix():
+    """The butterfly transform equals the Sylvester-order Hadamard matrix of the library
+    routine, scaled to be orthonormal, for every power-of-two length up to 256."""
+    scipy_linalg = pytest.importorskip("scipy.linalg")
+    rng = np.random.default_rng(51)
+    for n in (1, 2, 4, 8, 32, 128, 256):
+        x = rng.standard_normal((3, n))
+        want = x @ (scipy_linalg.hadamard(n).astype(np.float64) / math.sqrt(n)).T
+        assert np.allclose(oracle.fwht(x), want, rtol=1e-12, atol=1e-12)
+    assert np.allclose(oracle.fwht(np.array([1.0, 0.0])), [1 / math.sqrt(2), 1 / math.sqrt(2)])
+    with pytest.raises(ValueError):
+        oracle.fwht(np.ones(6))
+
+
+def test_randomized_hadamard_is_orthogonal_and_inverts_as_printed():
+    """y = H D x is exactly orthogonal, and x = D H y recovers x (the page's inverse)."""
+    rng = np.random.default_rng(52)
+    for n in (8, 64, 128):
+        s = rng.choice([-1.0, 1.0], size=n)
+        Pi = oracle.hadamard_rotation(s)
+        assert np.allclose(Pi @ Pi.T, np.eye(n), atol=1e-12)
+        x = rng.standard_normal(n)
+        y = Pi @ x
+        assert np.allclose(y, oracle.fwht(x * s), atol=1e-12)
+        assert np.allclose(oracle.fwht(y) * s, x, atol=1e-12)
+        # entries are +-1/sqrt(n): every coordinate of y mixes all of x
+        assert np.allclose(np.abs(Pi), 1.0 / math.sqrt(n))

@@ -2,6 +2,7 @@
 // Every check runs on the host before any CUDA call, so an invalid call
 // returns its status without touching the device.
 #include <climits>
+#include <cmath>
 
 #include "tq_internal.cuh"
 
@@ -137,6 +138,30 @@ tq_status tq_prepare_queries(const void* Q, tq_qtype qtype, const float* Pi, con
   if (st != TQ_OK) return st;
   if ((st = check_prepare_sizes(P, H, B, D, qtype)) != TQ_OK) return st;
   return from_cuda(tq::launch_prepare(Q, qtype, Pi, S_mat, A, T, P, H, B, D, stream));
+}
+
+tq_status tq_prepare_queries_hadamard(const void* Q, tq_qtype qtype, const float* hsigns,
+                                      const float* S_mat, float* A, float* T, int P, int H, int B,
+                                      int D, cudaStream_t stream) {
+  tq_status st = check_ptrs(Q, hsigns, S_mat, A, T);
+  if (st != TQ_OK) return st;
+  if ((st = check_prepare_sizes(P, H, B, D, qtype)) != TQ_OK) return st;
+  if (D < 2 || (D & (D - 1)) != 0) return TQ_ERR_INVALID_VALUE;
+  // the dense rows are unused in this mode; S_mat stands in for Pi
+  return from_cuda(tq::launch_prepare(Q, qtype, S_mat, S_mat, A, T, P, H, B, D, stream, nullptr, hsigns));
+}
+
+tq_status tq_hadamard_rotation(const float* signs, int D, float* Pi) {
+  if (signs == nullptr || Pi == nullptr || D < 1 || D > 4096 || (D & (D - 1)) != 0)
+    return TQ_ERR_INVALID_VALUE;
+  // Pi[i][j] = H[i][j] s_j / sqrt(D), H[i][j] = (-1)^popcount(i & j) (Sylvester order)
+  const double scale = 1.0 / std::sqrt(static_cast<double>(D));
+  for (int i = 0; i < D; ++i)
+    for (int j = 0; j < D; ++j) {
+      const double h = (__builtin_popcount(static_cast<unsigned>(i & j)) & 1) ? -scale : scale;
+      Pi[static_cast<size_t>(i) * D + j] = static_cast<float>(h * signs[j]);
+    }
+  return TQ_OK;
 }
 
 tq_status tq_scores(const float* A, const float* T, const uint8_t* K_idx, const int8_t* signs,

@@ -28,9 +28,11 @@ inline size_t mma_y_bytes(int P, int B) {
 }
 
 // Ybf (optional, D == 128 only): also write A and T as the tensor-core query operand.
+// hsigns (optional, [H][D] +-1, D a power of two): A = H diag(s) q by a fast
+// Walsh-Hadamard transform instead of the dense rows of Pi (Pi is then unused).
 cudaError_t launch_prepare(const void* Q, tq_qtype qtype, const float* Pi, const float* S_mat,
                            float* A, float* T, int P, int H, int B, int D, cudaStream_t st,
-                           uint16_t* Ybf = nullptr);
+                           uint16_t* Ybf = nullptr, const float* hsigns = nullptr);
 
 cudaError_t launch_scores_unpacked_fp32(const float* A, const float* T, const uint8_t* K_idx,
                                         const int8_t* signs, const float* gamma,

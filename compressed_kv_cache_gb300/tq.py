@@ -42,6 +42,8 @@ _SIGNATURES = {
     "tq_scores": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P], _I),
     "tq_scores_packed": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P], _I),
     "tq_scores_mse": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P], _I),
+    "tq_prepare_queries_hadamard": ([_P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _P], _I),
+    "tq_hadamard_rotation": ([_P, _I, _P], _I),
     "tq_workspace_bytes": ([_I, _I, _I], _Z),
     "tq_solve": ([_P, _I, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _Z, _I, _P], _I),
     "tq_solve_packed": ([_P, _I, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _Z, _I, _P], _I),
@@ -132,6 +134,35 @@ def prepare_queries(Q, Pi, S_mat, out=None):
     if Q.dim() == 2:
         return A.view(B, D), T.view(B, D)
     return A, T
+
+
+def prepare_queries_hadamard(Q, signs, S_mat, out=None):
+    """A = H diag(s) q (fast Walsh-Hadamard transform) and T = S_mat q.  signs [H,D] (or [D])
+    fp32 +-1; S_mat [H,D,D] (or [D,D]); D a power of two."""
+    P, B, D = _as3(Q)
+    H = 1 if signs.dim() == 1 else signs.shape[0]
+    if signs.shape[-1] != D or tuple(S_mat.shape[-2:]) != (D, D):
+        raise ValueError("signs must be [H,D] and S_mat [H,D,D]")
+    A, T = out if out is not None else (torch.empty((P, B, D), device=Q.device, dtype=torch.float32),
+                                         torch.empty((P, B, D), device=Q.device, dtype=torch.float32))
+    _check("tq_prepare_queries_hadamard", lib().tq_prepare_queries_hadamard(
+        _dev(Q, "Q", QTYPE), QTYPE[Q.dtype], _dev(signs, "signs", (torch.float32,)),
+        _dev(S_mat, "S_mat", (torch.float32,)), _dev(A, "A", (torch.float32,)),
+        _dev(T, "T", (torch.float32,)), P, H, B, D, _stream()))
+    if Q.dim() == 2:
+        return A.view(B, D), T.view(B, D)
+    return A, T
+
+
+def hadamard_rotation(signs):
+    """Dense Pi = H diag(s) as a float32 [D,D] numpy matrix (host computation in libtq), for
+    the compressor and the dense paths."""
+    import numpy as np
+    s = np.ascontiguousarray(signs, dtype=np.float32)
+    D = s.size
+    out = np.empty((D, D), dtype=np.float32)
+    _check("tq_hadamard_rotation", lib().tq_hadamard_rotation(s.ctypes.data, D, out.ctypes.data))
+    return out
 
 
 def _keys3(t: torch.Tensor, P: int):

@@ -89,6 +89,25 @@ tq_status tq_prepare_queries(const void* Q, tq_qtype qtype, const float* Pi, con
                              float* A, float* T, int P, int H, int B, int D, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
+ * The same transform with a randomized-Hadamard rotation Pi = H diag(s)
+ * (kanthi.in §2 "A dense Haar rotation costs O(d^2) ... randomized Hadamard
+ * transform y = H D x", §3 RandomizedHadamard): A = H (s * q) by a fast
+ * Walsh-Hadamard transform in O(D log D), H orthonormal in Sylvester order
+ * (H[i][j] = (-1)^popcount(i & j) / sqrt(D)); T = S_mat q as above.
+ *
+ * hsigns: [H,D] fp32, each +1 or -1 (device).  D a power of two, 2 <= D <= 256.
+ * Other arguments and errors as for tq_prepare_queries.
+ *
+ * tq_hadamard_rotation (HOST pointers): writes the dense fp32 row-major
+ * Pi = H diag(s) for the D signs at `signs`, D a power of two <= 4096, so that
+ * the compressor and every other entry taking Pi use the same rotation.
+ * ---------------------------------------------------------------------- */
+tq_status tq_prepare_queries_hadamard(const void* Q, tq_qtype qtype, const float* hsigns,
+                                      const float* S_mat, float* A, float* T, int P, int H, int B,
+                                      int D, cudaStream_t stream);
+tq_status tq_hadamard_rotation(const float* signs, int D, float* Pi);
+
+/* ------------------------------------------------------------------------
  * Scores from an UNPACKED cache (riteshyadav.xyz, "Two kernels, two jobs",
  * second kernel, and "Full CUDA solution"): one byte per index and per sign.
  *

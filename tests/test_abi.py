@@ -104,3 +104,13 @@ def test_mse_argument_errors(L):
     assert call(bits=0) == 1 and call(bits=5) == 1
     assert call(corr=2) == 1
     assert call(S=0) == 1
+
+
+def test_hadamard_prepare_argument_errors(L):
+    def call(D=128, signs=FAKE, H=1, P=1):
+        return L.tq_prepare_queries_hadamard(FAKE, 0, signs, FAKE, FAKE, FAKE, P, H, 4, D, None)
+    assert call(D=96) == 1 and call(D=1) == 1 and call(D=512) == 1   # a power of two, 2..256
+    assert call(signs=None) == 1
+    assert call(signs=ODD) == 3
+    assert call(H=2) == 1                                              # H > P
+    assert L.tq_hadamard_rotation(None, 8, None) == 1

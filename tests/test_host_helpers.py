@@ -47,3 +47,15 @@ def test_host_helper_argument_errors():
     f = 0x100000
     assert L.tq_compress_keys(f, f, f, f, 4, f, f, f, f, 1, 1, 8, 128, None) == 1   # both gammas
     assert L.tq_compress_keys(f, f, f, f, 4, f, f, f, None, 1, 1, 8, 160, None) == 2  # D > 128
+
+
+def test_hadamard_rotation_matches_oracle():
+    """tq_hadamard_rotation (host) writes H diag(s) in fp32: the oracle's matrix rounded."""
+    import oracle
+    rng = np.random.default_rng(71)
+    for D in (1, 2, 16, 128, 256):
+        s = rng.choice([-1.0, 1.0], size=D).astype(np.float32)
+        got = tq.hadamard_rotation(s)
+        assert np.array_equal(got, oracle.hadamard_rotation(s).astype(np.float32))
+    with pytest.raises(Exception):
+        tq.hadamard_rotation(np.ones(12, dtype=np.float32))

@@ -40,6 +40,7 @@ __all__ = [
     "scores_from_queries",
     "scores_sampled",
     "scores_mse",
+    "decode_mse",
     "pack_indices",
     "unpack_indices",
     "pack_signs",
@@ -293,6 +294,29 @@ def scores_mse(A: np.ndarray, idx: np.ndarray, norm: np.ndarray, codebook: np.nd
     if norm_correction:
         dots = dots / np.sqrt(np.sum(cvals * cvals, axis=1))[np.newaxis, :]
     return dots * np.asarray(norm, dtype=np.float64)[np.newaxis, :]
+
+
+def decode_mse(A: np.ndarray, k_idx: np.ndarray, k_norm: np.ndarray, k_codebook: np.ndarray,
+               v_idx: np.ndarray, v_norm: np.ndarray, v_codebook: np.ndarray, Pi_v: np.ndarray,
+               scale: float) -> np.ndarray:
+    """Attention output over an MSE-quantized key and value cache, computed in the
+    rotated domain ([KB] §8 "Kernel view", the kernel form of tq_rotated_domain):
+
+        s[b, i]  = scale * k_norm[i] * <A[b], c_k[k_idx[i]]>        (A = Pi_k q)
+        p[b, :]  = softmax(s[b, :])                                 (max subtracted)
+        acc[b]   = sum_i p[b, i] v_norm[i] c_v[v_idx[i]]            (stays rotated)
+        out[b]   = Pi_v^T acc[b]                                    (one inverse rotation)
+
+    The page's scale is 1/sqrt(D).  float64 throughout.
+    """
+    A = np.asarray(A, dtype=np.float64)
+    kc = np.asarray(k_codebook, dtype=np.float64)[np.asarray(k_idx, dtype=np.int64)]
+    vc = np.asarray(v_codebook, dtype=np.float64)[np.asarray(v_idx, dtype=np.int64)]
+    s = scale * (A @ kc.T) * np.asarray(k_norm, dtype=np.float64)[np.newaxis, :]
+    p = np.exp(s - s.max(axis=1, keepdims=True))
+    p /= p.sum(axis=1, keepdims=True)
+    acc = (p * np.asarray(v_norm, dtype=np.float64)[np.newaxis, :]) @ vc
+    return acc @ np.asarray(Pi_v, dtype=np.float64)
 
 
 # ---------------------------------------------------------------------------

@@ -450,3 +450,63 @@ def test_randomized_hadamard_is_orthogonal_and_inverts_as_printed():
         assert np.allclose(oracle.fwht(y) * s, x, atol=1e-12)
         # entries are +-1/sqrt(n): every coordinate of y mixes all of x
         assert np.allclose(np.abs(Pi), 1.0 / math.sqrt(n))
+
+
+# ---------------------------------------------------------------------------
+# fused decode over MSE keys and values (kanthi.in §8 "Kernel view")
+# ---------------------------------------------------------------------------
+
+def _decode_case(n, D, seed, kbits=3, vbits=3):
+    rng = np.random.default_rng(seed)
+    K = rng.standard_normal((n, D))
+    V = rng.standard_normal((n, D))
+    q = rng.standard_normal((2, D))
+    Pk = oracle.haar_rotation(rng.standard_normal((D, D))).astype(np.float32)
+    Pv = oracle.haar_rotation(rng.standard_normal((D, D))).astype(np.float32)
+    kcb = codebook(D, kbits)[0].astype(np.float32)
+    vcb = codebook(D, vbits)[0].astype(np.float32)
+    ki, kn = oracle.compress_mse(K, Pk, kcb)
+    vi, vn = oracle.compress_mse(V, Pv, vcb)
+    return q, K, V, Pk, Pv, kcb, vcb, ki, kn, vi, vn
+
+
+def test_decode_equals_dequantize_everything():
+    """The rotated-domain decode equals attention over fully dequantized keys and values
+    (kanthi.in §8 prints both routes agreeing to 1e-15): every key and value is rebuilt
+    as n * Pi^T c_idx, scored against q / sqrt(d), softmaxed, and the values averaged."""
+    D, n = 32, 300
+    q, K, V, Pk, Pv, kcb, vcb, ki, kn, vi, vn = _decode_case(n, D, 61)
+    A = q @ Pk.astype(np.float64).T
+    got = oracle.decode_mse(A, ki, kn, kcb, vi, vn, vcb, Pv, 1.0 / math.sqrt(D))
+    Kh = kn.astype(np.float64)[:, None] * (kcb.astype(np.float64)[ki.astype(np.int64)] @ Pk.astype(np.float64))
+    Vh = vn.astype(np.float64)[:, None] * (vcb.astype(np.float64)[vi.astype(np.int64)] @ Pv.astype(np.float64))
+    for b in range(q.shape[0]):
+        logits = [float(np.dot(Kh[i], q[b])) / math.sqrt(D) for i in range(n)]
+        m = max(logits)
+        w = [math.exp(x - m) for x in logits]
+        tot = sum(w)
+        want = sum(w[i] / tot * Vh[i] for i in range(n))
+        assert np.allclose(got[b], want, rtol=1e-12, atol=1e-12)
+
+
+def test_decode_special_cases():
+    """One key: the output is that value's reconstruction.  A key whose logit exceeds
+    every other by a wide margin takes all the weight.  Keys with equal logits weigh their
+    values equally: the output is the plain mean of the reconstructed values."""
+    D = 16
+    q, K, V, Pk, Pv, kcb, vcb, ki, kn, vi, vn = _decode_case(40, D, 62)
+    A = q @ Pk.astype(np.float64).T
+    Vh = vn.astype(np.float64)[:, None] * (vcb.astype(np.float64)[vi.astype(np.int64)] @ Pv.astype(np.float64))
+    one = oracle.decode_mse(A, ki[:1], kn[:1], kcb, vi[:1], vn[:1], vcb, Pv, 0.25)
+    assert np.allclose(one, np.broadcast_to(Vh[0], one.shape), rtol=1e-12)
+    # key 0's logit for query 0 is s0 = 0.25 * n0 * <A0, c_k0>; a norm of 1e4 with the
+    # sign of <A0, c_k0> puts it far above the others (whose norms are about 4)
+    dot0 = float(A[0] @ kcb.astype(np.float64)[ki[0].astype(np.int64)])
+    big = kn.astype(np.float64).copy()
+    big[0] = math.copysign(1e4, dot0)
+    out = oracle.decode_mse(A[:1], ki, big, kcb, vi, vn, vcb, Pv, 0.25)
+    assert np.allclose(out[0], Vh[0], rtol=1e-9, atol=1e-9)
+    same = np.zeros_like(ki)                          # one code row for every key
+    ones = np.ones(len(kn), dtype=np.float16)
+    o1 = oracle.decode_mse(A, same, ones, kcb, vi, vn, vcb, Pv, 0.25)
+    assert np.allclose(o1, np.broadcast_to(Vh.mean(axis=0), o1.shape), rtol=1e-12, atol=1e-12)

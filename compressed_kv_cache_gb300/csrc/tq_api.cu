@@ -257,6 +257,31 @@ tq_status tq_scores_mse(const float* A, const uint8_t* idx_plane, const uint16_t
                                          idx_bits, norm_correction != 0, stream));
 }
 
+size_t tq_decode_workspace_bytes(int P, int B, int S, int D) {
+  if (P < 1 || B < 1 || S < 1 || D != 128) return 0;
+  return round_up(tq::decode_part_floats(P, B, S) * sizeof(float), 256);
+}
+
+tq_status tq_decode_mse(const float* A, const uint8_t* k_plane, const uint16_t* k_norm,
+                        const float* k_codebook, int k_bits, const uint8_t* v_plane,
+                        const uint16_t* v_norm, const float* v_codebook, int v_bits,
+                        const float* Pi_v, float* out, int P, int H, int B, int S, int D,
+                        float scale, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  tq_status st = check_ptrs(A, k_plane, k_norm, k_codebook, v_plane, v_norm, v_codebook, Pi_v, out);
+  if (st != TQ_OK) return st;
+  if (P < 1 || H < 1 || H > P || B < 1 || S < 1 || D < 1) return TQ_ERR_INVALID_VALUE;
+  if (P > kMaxGridYZ || B > kMaxGridYZ || S > INT_MAX - 4096) return TQ_ERR_INVALID_VALUE;
+  if (k_bits < 1 || k_bits > 3 || v_bits < 1 || v_bits > 3 || !std::isfinite(scale))
+    return TQ_ERR_INVALID_VALUE;
+  if (D != 128) return TQ_ERR_UNSUPPORTED;
+  if (workspace == nullptr) return TQ_ERR_WORKSPACE;
+  if (misaligned(workspace)) return TQ_ERR_MISALIGNED;
+  if (workspace_bytes < tq_decode_workspace_bytes(P, B, S, D)) return TQ_ERR_WORKSPACE;
+  return from_cuda(tq::launch_decode_mse(A, k_plane, k_norm, k_codebook, k_bits, v_plane, v_norm,
+                                         v_codebook, v_bits, Pi_v, out, static_cast<float*>(workspace),
+                                         P, H, B, S, scale, stream));
+}
+
 tq_status tq_pack_indices(const uint8_t* K_idx, uint8_t* idx_plane, int64_t n_keys, int D,
                           int bits, cudaStream_t stream) {
   tq_status st = check_ptrs(K_idx, idx_plane);

@@ -73,6 +73,15 @@ cudaError_t launch_scores_mse(const float* A, const uint8_t* idx_plane, const ui
                               const float* codebook, float* scores, int P, int B, int S, int D,
                               int idx_bits, bool norm_correction, cudaStream_t st);
 
+// Fused decode over MSE keys and values (D = 128, 1-3 bit codes): split-KV partials in
+// `part` (decode_part_floats(P, B, S) floats), then the combine and Pi_v^T.
+size_t decode_part_floats(int P, int B, int S);
+cudaError_t launch_decode_mse(const float* A, const uint8_t* k_plane, const uint16_t* k_norm,
+                              const float* k_cb, int k_bits, const uint8_t* v_plane,
+                              const uint16_t* v_norm, const float* v_cb, int v_bits,
+                              const float* Pi_v, float* out, float* part, int P, int H, int B, int S,
+                              float scale, cudaStream_t st);
+
 cudaError_t launch_pack_indices(const uint8_t* K_idx, uint8_t* plane, int64_t n, int D, int bits,
                                 cudaStream_t st);
 cudaError_t launch_unpack_indices(const uint8_t* plane, uint8_t* K_idx, int64_t n, int D,

@@ -44,6 +44,9 @@ _SIGNATURES = {
     "tq_scores_mse": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P], _I),
     "tq_prepare_queries_hadamard": ([_P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _P], _I),
     "tq_hadamard_rotation": ([_P, _I, _P], _I),
+    "tq_decode_workspace_bytes": ([_I, _I, _I, _I], ctypes.c_size_t),
+    "tq_decode_mse": ([_P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, ctypes.c_float,
+                       _P, ctypes.c_size_t, _P], _I),
     "tq_workspace_bytes": ([_I, _I, _I], _Z),
     "tq_solve": ([_P, _I, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _Z, _I, _P], _I),
     "tq_solve_packed": ([_P, _I, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _Z, _I, _P], _I),
@@ -226,6 +229,33 @@ def scores_mse(A, idx_plane, norm_f16, codebook, idx_bits, norm_correction=False
         _dev(o, "scores", (torch.float32,)), P, B, S, D, idx_bits, 1 if norm_correction else 0,
         _stream()))
     return o if (out is not None or A.dim() == 3) else o.view(B, S)
+
+
+def decode_mse(A, k_plane, k_norm, k_codebook, k_bits, v_plane, v_norm, v_codebook, v_bits, Pi_v,
+               scale=None, workspace=None, out=None):
+    """Attention output over MSE-quantized keys and values (rotated-domain decode).
+    A = Pi_k q [P,B,128]; planes uint8 [P,S,128*bits/8]; norms float16 [P,S];
+    Pi_v [H,128,128] (or [128,128]).  Returns [P,B,128] (or [B,128])."""
+    P, B, D = _as3(A)
+    S, krow = _keys3(k_plane, P)
+    _, vrow = _keys3(v_plane, P)
+    H = 1 if Pi_v.dim() == 2 else Pi_v.shape[0]
+    if krow * 8 != D * k_bits or vrow * 8 != D * v_bits or k_norm.numel() != P * S or v_norm.numel() != P * S:
+        raise ValueError("inconsistent key/value shapes")
+    need = int(lib().tq_decode_workspace_bytes(P, B, S, D))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), device=A.device, dtype=torch.uint8)
+    o = out if out is not None else torch.empty((P, B, D), device=A.device, dtype=torch.float32)
+    if scale is None:
+        scale = 1.0 / float(D) ** 0.5
+    _check("tq_decode_mse", lib().tq_decode_mse(
+        _dev(A, "A", (torch.float32,)), _dev(k_plane, "k_plane", (torch.uint8,)),
+        _dev(k_norm, "k_norm", (torch.float16,)), _dev(k_codebook, "k_codebook", (torch.float32,)), k_bits,
+        _dev(v_plane, "v_plane", (torch.uint8,)), _dev(v_norm, "v_norm", (torch.float16,)),
+        _dev(v_codebook, "v_codebook", (torch.float32,)), v_bits, _dev(Pi_v, "Pi_v", (torch.float32,)),
+        _dev(o, "out", (torch.float32,)), P, H, B, S, D, float(scale),
+        _dev(workspace, "workspace", (torch.uint8,)), workspace.numel(), _stream()))
+    return o if (out is not None or A.dim() == 3) else o.view(B, D)
 
 
 def workspace_bytes(P: int, B: int, D: int) -> int:

@@ -165,6 +165,33 @@ tq_status tq_scores_mse(const float* A, const uint8_t* idx_plane, const uint16_t
                         int idx_bits, int norm_correction, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Fused decode over an MSE-quantized key AND value cache, in the rotated
+ * domain (kanthi.in §8 "Kernel view: never un-rotate a key", the kernel form
+ * of tq_rotated_domain; §7 on values):
+ *
+ *   s[b,i] = scale * nk_i * <A_b, ck[kidx_i]>     A = Pi_k q (tq_prepare_queries)
+ *   p[b,:] = softmax(s[b,:])
+ *   out[b] = Pi_v^T sum_i p[b,i] nv_i cv[vidx_i]  (one inverse rotation per query)
+ *
+ * Keys and values use the tq_scores_mse format: packed code planes
+ * k_plane [P,S,D*k_bits/8] and v_plane [P,S,D*v_bits/8] of the rotated unit
+ * vectors, fp16 lengths k_norm, v_norm [P,S], fp32 codebooks of 2^bits
+ * centroids.  Pi_v: [H,D,D] fp32 (problem p uses head p % H).  out: [P,B,D]
+ * fp32.  scale: the logit scale (1/sqrt(D) on the page).  D == 128,
+ * k_bits, v_bits in {1,2,3}.  Split-KV: the caller passes `workspace` of at
+ * least tq_decode_workspace_bytes(P, B, S, D) bytes (scratch, contents
+ * unspecified on return, not shared by concurrent calls).  fp32 arithmetic.
+ * Errors: TQ_ERR_INVALID_VALUE, TQ_ERR_MISALIGNED, TQ_ERR_UNSUPPORTED (D != 128),
+ * TQ_ERR_WORKSPACE, TQ_ERR_LAUNCH.
+ * ---------------------------------------------------------------------- */
+size_t tq_decode_workspace_bytes(int P, int B, int S, int D);
+tq_status tq_decode_mse(const float* A, const uint8_t* k_plane, const uint16_t* k_norm,
+                        const float* k_codebook, int k_bits, const uint8_t* v_plane,
+                        const uint16_t* v_norm, const float* v_codebook, int v_bits,
+                        const float* Pi_v, float* out, int P, int H, int B, int S, int D,
+                        float scale, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
  * Fused query transform + scoring: the challenge's `solve` without its
  * per-call cudaMalloc/cudaFree (riteshyadav.xyz, "What the rearrangement
  * saves": its solve "allocates temporary arrays on every call").  The caller

@@ -114,3 +114,18 @@ def test_hadamard_prepare_argument_errors(L):
     assert call(signs=ODD) == 3
     assert call(H=2) == 1                                              # H > P
     assert L.tq_hadamard_rotation(None, 8, None) == 1
+
+
+def test_decode_argument_errors(L):
+    assert L.tq_decode_workspace_bytes(1, 1, 131072, 128) >= 4 * 130 * 512
+    assert L.tq_decode_workspace_bytes(1, 1, 10, 64) == 0
+
+    def call(A=FAKE, D=128, kb=3, vb=3, scale=0.1, ws=FAKE, wsb=1 << 20, H=1):
+        return L.tq_decode_mse(A, FAKE, FAKE, FAKE, kb, FAKE, FAKE, FAKE, vb, FAKE, FAKE, 1, H, 2, 100, D,
+                               scale, ws, wsb, None)
+    assert call(A=None) == 1 and call(A=ODD) == 3
+    assert call(D=64) == 2                                    # D must be 128
+    assert call(kb=0) == 1 and call(kb=4) == 1 and call(vb=4) == 1
+    assert call(scale=float("inf")) == 1
+    assert call(H=2) == 1                                     # H > P
+    assert call(ws=None) == 4 and call(wsb=16) == 4 and call(ws=ODD) == 3

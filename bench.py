@@ -78,12 +78,17 @@ def key_bytes(w) -> int:
         return 2 * w.D + (4 if w.gamma_dtype == "f32" else 2)
     if w.layout == "mse":                 # code plane + norm, no sign plane
         return w.D * w.mse_bits // 8 + (4 if w.gamma_dtype == "f32" else 2)
+    if w.layout == "decode":              # the key's and the value's code plane + norm
+        return 2 * (w.D * w.mse_bits // 8 + 2)
     return w.D * w.mse_bits // 8 + w.D // 8 + (4 if w.gamma_dtype == "f32" else 2)
 
 
 def score_kernel_bytes(w) -> int:
     """Algorithmic bytes of one scoring launch: the compressed cache once, the
     scores once, A and T once (A only for the MSE-only scorer), the codebook."""
+    if w.layout == "decode":
+        # cache once, A and the outputs once, Pi_v once, both codebooks
+        return (w.P * w.S * key_bytes(w) + 2 * 4 * w.P * w.B * w.D + 4 * w.H * w.D * w.D + 8 * w.C)
     n_at = 1 if w.layout == "mse" else 2
     return (w.P * w.S * key_bytes(w) + 4 * w.P * w.B * w.S + n_at * 4 * w.P * w.B * w.D + 4 * w.C)
 
@@ -240,11 +245,25 @@ def build_device_workload(w, tq, torch, dev):
     cache = {"gamma": gamma}
     if w.layout == "unpacked":
         cache["idx"], cache["signs"] = idx, sg
-    elif w.layout == "mse":
+    elif w.layout in ("mse", "decode"):
         # unit keys: the codes of TurboQuant_prod's MSE stage are the MSE-only codes
         # (same rotation, codebook and cells) and every stored norm is 1
         cache = {"idx": tq.pack_indices(idx, w.mse_bits),
                  "norm": torch.ones((w.P, w.S), dtype=torch.float16, device=dev)}
+        if w.layout == "decode":
+            # unit values of their own, with their own rotation per head
+            Pi_v = torch.from_numpy(np.stack([tq.haar_rotation(synth.rotation_seed_matrix(w.seed + 1, h, w.D))
+                                              for h in range(w.H)])).to(dev)
+            vidx = torch.empty((w.P, w.S, w.D), dtype=torch.uint8, device=dev)
+            for p in range(w.P):
+                vals = torch.from_numpy(synth.unit_keys(w.seed + 1, p, 0, w.S, w.D).astype(np.float32)).to(dev)
+                vidx[p].copy_(tq.compress_keys(vals, Pi_v[p % w.H], S_mat[p % w.H], cb, gdt)[0])
+            cache.update({"vidx": tq.pack_indices(vidx, w.mse_bits), "Pi_v": Pi_v,
+                          "vnorm": torch.ones((w.P, w.S), dtype=torch.float16, device=dev),
+                          # outputs and split-KV scratch of the decode (not inputs)
+                          "dout": torch.empty((w.P, w.B, w.D), device=dev),
+                          "dws": torch.empty(max(16, int(tq.lib().tq_decode_workspace_bytes(w.P, w.B, w.S, w.D))),
+                                             dtype=torch.uint8, device=dev)})
     else:
         cache["idx"] = tq.pack_indices(idx, w.mse_bits)
         cache["signs"] = tq.pack_signs(sg)
@@ -253,6 +272,9 @@ def build_device_workload(w, tq, torch, dev):
 
 
 def score_call(tq, w, path, A, T, cache, cb, out):
+    if w.layout == "decode":
+        return tq.decode_mse(A, cache["idx"], cache["norm"], cb, w.mse_bits, cache["vidx"], cache["vnorm"], cb,
+                             w.mse_bits, cache["Pi_v"], workspace=cache["dws"], out=cache["dout"])
     if w.layout == "mse":
         return tq.scores_mse(A, cache["idx"], cache["norm"], cb, w.mse_bits, norm_correction=True, out=out)
     if w.layout == "unpacked":
@@ -272,6 +294,15 @@ def oracle_sample(w, n_keys):
     S_mat = synth.s_matrix(w.seed, 0, w.D)
     keys = synth.unit_keys(w.seed, 0, 0, n_keys, w.D)
     Q = synth.queries(w.seed, 0, w.B, w.D, w.q_dtype)[0]
+    if w.layout == "decode":
+        Pi_v = oracle.haar_rotation(synth.rotation_seed_matrix(w.seed + 1, 0, w.D)).astype(np.float32)
+        ki, kn = oracle.compress_mse(keys, Pi, cb)
+        vi, vn = oracle.compress_mse(synth.unit_keys(w.seed + 1, 0, 0, n_keys, w.D), Pi_v, cb)
+
+        def run_decode():
+            A, _ = oracle.prepare_queries(Q, Pi, Pi)
+            return oracle.decode_mse(A, ki, kn, cb, vi, vn, cb, Pi_v, 1.0 / np.sqrt(w.D))
+        return run_decode
     if w.layout == "mse":
         idx, nrm = oracle.compress_mse(keys, Pi, cb)
 
@@ -386,7 +417,7 @@ def main():
     def solve_call(cp):
         # one step = the fused public entry over the whole workload (for the MSE-only
         # variant, which has no fused entry: the query transform and the MSE scorer)
-        if w.layout == "mse":
+        if w.layout in ("mse", "decode"):
             tq.prepare_queries(cp["Q"], Pi, Pi, out=(cp["A"], cp["T"]))
             score_call(tq, w, path, cp["A"], cp["T"], cp["cache"], cb, cp["out"])
         elif w.layout == "unpacked":
@@ -483,11 +514,14 @@ def main():
     # end to end through the public fused API with host buffers
     if True:
         hostQ = Q0.cpu().pin_memory()
-        hcache = {k: v.cpu().pin_memory() for k, v in cache0.items()}
+        scratch = ("dout", "dws")             # decode outputs and workspace: not copied in
+        hcache = {k: v.cpu().pin_memory() for k, v in cache0.items() if k not in scratch}
         hPi, hS, hcb = Pi.cpu().pin_memory(), S_mat.cpu().pin_memory(), cb.cpu().pin_memory()
-        mse = w.layout == "mse"            # no S_mat: the MSE-only path needs Pi alone
+        mse = w.layout in ("mse", "decode")   # no S_mat: the MSE-only paths need Pi alone
         hout = torch.empty((w.P, w.B, w.S), dtype=torch.float32).pin_memory()
         dQ, dcache = torch.empty_like(Q0), {k: torch.empty_like(v) for k, v in cache0.items()}
+        if w.layout == "decode":
+            hout = torch.empty((w.P, w.B, w.D), dtype=torch.float32).pin_memory()
         dPi, dS, dcb = torch.empty_like(Pi), torch.empty_like(S_mat), torch.empty_like(cb)
         dout = torch.empty((w.P, w.B, w.S), device=dev)
         ws = torch.empty(tq.workspace_bytes(w.P, w.B, w.D), dtype=torch.uint8, device=dev)
@@ -498,12 +532,17 @@ def main():
 
         def e2e_step():
             dQ.copy_(hostQ, non_blocking=True)
-            for k in dcache:
+            for k in hcache:
                 dcache[k].copy_(hcache[k], non_blocking=True)
             dPi.copy_(hPi, non_blocking=True)
             if not mse:
                 dS.copy_(hS, non_blocking=True)
             dcb.copy_(hcb, non_blocking=True)
+            if w.layout == "decode":
+                tq.prepare_queries(dQ, dPi, dPi, out=(dA, dT))
+                score_call(tq, w, path, dA, dT, dcache, dcb, None)
+                hout.copy_(dcache["dout"], non_blocking=True)
+                return
             if mse:
                 tq.prepare_queries(dQ, dPi, dPi, out=(dA, dT))
                 tq.scores_mse(dA, dcache["idx"], dcache["norm"], dcb, w.mse_bits, norm_correction=True,
@@ -555,12 +594,14 @@ def main():
         "hbm_gbs": achieved,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "fused transform+scoring kernel" if fused_single else "scoring kernel", "kernel_ms": kernel_ms, "bytes_per_launch": kbytes,
+                     "kernel": ("fused transform+scoring kernel" if fused_single else
+                                "decode split + combine kernels" if w.layout == "decode" else "scoring kernel"),
+                     "kernel_ms": kernel_ms, "bytes_per_launch": kbytes,
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback 6.8 TB/s",
                      "timing": ktiming, "kernel_fingerprint": fp},
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": (1 if fused_single else 2) * args.steps,
+        "gpu_launches": (1 if fused_single else (3 if w.layout == "decode" else 2)) * args.steps,
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)

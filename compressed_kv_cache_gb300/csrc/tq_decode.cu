@@ -8,13 +8,16 @@
 //   out[b]  = Pi_v^T acc[b]                             one inverse rotation per query
 //
 // Split-KV (flash decoding): decode_split_kernel takes one chunk of keys and one tile
-// of QB queries of a problem.  It builds the key lookup tables of the MSE scorer,
-// scores its keys into shared memory (thread per key), reduces the chunk's maximum,
-// turns the logits into exp(s - max) and their sum, then accumulates the weighted value
-// codewords: a warp per key, lane l owning coordinates 4l .. 4l+3, so that each key's
-// value row is read once per warp.  It writes (max, sum, acc[128]) per (query, chunk)
-// to the workspace.  decode_combine_kernel merges the chunks of a query with the
-// usual rescaling by exp(max_c - max) and applies Pi_v^T.  D = 128, 1-3 bit codes.
+// of QB queries of a problem.  Each of its 8 warps owns a contiguous run of the chunk's
+// keys and starts the asynchronous copies of their key and value rows into shared
+// memory, 32 keys to a copy group.  The CTA builds the key lookup tables of the MSE
+// scorer from the rotated queries meanwhile.  Then every warp runs an online softmax
+// over its groups as they land: logits (lane per key), the group maximum, the rescale
+// of the running sum and accumulator by exp(old max - new max), and the weighted value
+// centroids (warp per key, lane l owning coordinates 4l .. 4l+3).  The 8 warps merge
+// in shared memory and write (max, sum, acc[128]) per (query, chunk) to the workspace.
+// decode_combine_kernel merges the chunks of a query with the same rescaling and
+// applies Pi_v^T.  D = 128, 1-3 bit codes.
 #include <atomic>
 
 #include "tq_internal.cuh"
@@ -24,29 +27,10 @@ namespace tq {
 namespace {
 
 constexpr int kD = 128;
-constexpr int kDecThreads = 256;
-constexpr int kMaxChunk = 2048;          // keys per split CTA (shared-memory logits)
-constexpr int kPart = 2 + kD;            // floats per (query, chunk): max, sum, acc
-
-// The centroid of a 1-3 bit code from registers (no dynamic register indexing).
-template <int BITS>
-__device__ __forceinline__ float centroid_of(const float (&c)[1 << BITS], uint32_t code) {
-  if constexpr (BITS == 1) {
-    return (code & 1u) ? c[1] : c[0];
-  } else if constexpr (BITS == 2) {
-    const float lo = (code & 1u) ? c[1] : c[0];
-    const float hi = (code & 1u) ? c[3] : c[2];
-    return (code & 2u) ? hi : lo;
-  } else {
-    const float c01 = (code & 1u) ? c[1] : c[0];
-    const float c23 = (code & 1u) ? c[3] : c[2];
-    const float c45 = (code & 1u) ? c[5] : c[4];
-    const float c67 = (code & 1u) ? c[7] : c[6];
-    const float lo = (code & 2u) ? c23 : c01;
-    const float hi = (code & 2u) ? c67 : c45;
-    return (code & 4u) ? hi : lo;
-  }
-}
+constexpr int kDecThreads = 512;
+constexpr int kMaxChunk = 1024;          // keys per split CTA (rows staged in shared memory)
+constexpr int kAcc = 4;                  // acc offset in a partial row (16-byte aligned)
+constexpr int kPart = kAcc + kD;         // floats per (query, chunk): max, sum, 2 pad, acc
 
 __device__ __forceinline__ float warp_max(float x) {
 #pragma unroll
@@ -59,11 +43,44 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
-// Shared memory: lut [QB][NPI*NV] | logits [QB][chunk] | red [8 warps][QB][128]
-template <int KBITS, int QB>
-constexpr size_t split_smem_floats(int chunk) {
-  return static_cast<size_t>(QB) * LutShape<KBITS>::NPI * LutShape<KBITS>::NV +
-         static_cast<size_t>(QB) * chunk + static_cast<size_t>(kDecThreads / 32) * QB * kD;
+// One bulk copy global -> shared through the copy engine, completing on a local mbarrier.
+__device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void expect_bytes(uint32_t bar, uint32_t bytes) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(bar),
+               "r"(bytes)
+               : "memory");
+}
+// Bounded wait for phase 0 of a local mbarrier (about a second at most); false if it
+// gave up.
+__device__ __forceinline__ bool wait_phase0(uint32_t bar) {
+  for (uint32_t it = 0; it < (1u << 22); ++it) {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(bar)
+                 : "memory");
+    if (ok) return true;
+  }
+  return false;
+}
+
+// Shared memory: key rows [chunk][16 KBITS B] | value rows [chunk][16 VBITS B] |
+// copy barriers [warps][steps] | lut [QB][NPI*NV] | rotated queries [QB][128] |
+// warp acc [warps][QB][128] | warp max and sum [warps][QB] each | value centroids [8]
+constexpr int kDecWarps = kDecThreads / 32;
+constexpr int kStep = 32;                                  // keys per warp step (lane per key)
+constexpr int kMaxSteps = kMaxChunk / kDecWarps / kStep;   // warp steps, at most
+
+template <int KBITS, int VBITS, int QB>
+constexpr size_t split_smem_bytes(int chunk) {
+  return static_cast<size_t>(chunk) * 16 * (KBITS + VBITS) + 8 * kDecWarps * kMaxSteps +
+         sizeof(float) * (static_cast<size_t>(QB) * LutShape<KBITS>::NPI * LutShape<KBITS>::NV +
+                          static_cast<size_t>(QB) * kD + static_cast<size_t>(kDecWarps) * QB * (kD + 2) + 8);
 }
 
 template <int KBITS, int VBITS, int QB>
@@ -74,184 +91,328 @@ decode_split_kernel(const float* __restrict__ A, const uint8_t* __restrict__ k_p
                     const float* __restrict__ v_cb, float* __restrict__ part, int B, int S,
                     int chunk, int nchunks, float scale) {
   using L = LutShape<KBITS>;
-  constexpr int kW = kDecThreads / 32;
-  extern __shared__ __align__(16) float smem[];
-  float* lut = smem;
-  float* logit = lut + QB * L::NPI * L::NV;
-  float* red = logit + QB * chunk;
+  constexpr int kW = kDecWarps;
+  constexpr int kKRow = 16 * KBITS, kVRow = 16 * VBITS;   // bytes of one key / value row
+  constexpr int kBlk = kStep;
+  constexpr int kMaxBlk = kMaxSteps;
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  uint8_t* kst = smem_raw;
+  uint8_t* vst = kst + static_cast<size_t>(chunk) * kKRow;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(vst + static_cast<size_t>(chunk) * kVRow);
+  float* lut = reinterpret_cast<float*>(bars + kW * kMaxBlk);
+  float* sA = lut + QB * L::NPI * L::NV;
+  float* racc = sA + QB * kD;
+  float* rmax = racc + kW * QB * kD;
+  float* rsum = rmax + kW * QB;
+  float* vtab = rsum + kW * QB;
   const int c = blockIdx.x, p = blockIdx.z, b0 = blockIdx.y * QB;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int k0 = c * chunk;
-  const int n = min(chunk, S - k0);
+  const int n = min(chunk, S - k0);                        // >= 1
   const size_t kbase = static_cast<size_t>(p) * S + k0;
+  // the merge kernel behind this grid may launch now; it reads the partials only after
+  // this grid has completed
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
+  // rotated queries into registers first (stored once the copies are under way)
+  constexpr int kAPer = (QB * kD + kDecThreads - 1) / kDecThreads;
+  float av[kAPer];
+#pragma unroll
+  for (int j = 0; j < kAPer; ++j) {
+    const int e = tid + j * kDecThreads, q = e / kD;
+    av[j] = e < QB * kD && b0 + q < B ? __ldg(A + (static_cast<size_t>(p) * B + b0 + q) * kD + (e % kD)) : 0.f;
+  }
+  const float vt = tid < (1 << VBITS) ? __ldg(v_cb + tid) : 0.f;
+  float cv[L::G];
+  table_centroids<KBITS>(k_cb, cv);
+
+  // this warp's keys [w0, w1) of the chunk, in steps of 32: per step one bulk copy of
+  // the key rows and one of the value rows, both completing on the step's barrier
+  const int per = (n + kW - 1) / kW;
+  const int w0 = min(n, warp * per), w1 = min(n, w0 + per);
+  const int nsteps = (w1 - w0 + kBlk - 1) / kBlk;
+  const uint32_t bar0 = static_cast<uint32_t>(__cvta_generic_to_shared(bars + warp * kMaxBlk));
+  if (lane == 0) {
+    for (int t = 0; t < nsteps; ++t)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar0 + 8 * t) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    for (int t = 0; t < nsteps; ++t) {
+      const int r0 = w0 + t * kBlk, rows = min(kBlk, w1 - r0);
+      const uint32_t bar = bar0 + 8 * t;
+      expect_bytes(bar, static_cast<uint32_t>(rows * (kKRow + kVRow)));
+      bulk_copy(kst + static_cast<size_t>(r0) * kKRow, k_plane + (kbase + r0) * kKRow,
+                static_cast<uint32_t>(rows * kKRow), bar);
+      bulk_copy(vst + static_cast<size_t>(r0) * kVRow, v_plane + (kbase + r0) * kVRow,
+                static_cast<uint32_t>(rows * kVRow), bar);
+    }
+  }
+  __syncwarp();
+  // norms of this lane's keys w0 + 32 t + lane
+  float nk[kMaxBlk], nv[kMaxBlk];
+#pragma unroll
+  for (int t = 0; t < kMaxBlk; ++t) {
+    const int i = w0 + t * kBlk + lane;
+    nk[t] = i < w1 ? __half2float(__ushort_as_half(__ldg(k_norm + kbase + i))) : 0.f;
+    nv[t] = i < w1 ? __half2float(__ushort_as_half(__ldg(v_norm + kbase + i))) : 0.f;
+  }
+
+#pragma unroll
+  for (int j = 0; j < kAPer; ++j) {
+    const int e = tid + j * kDecThreads;
+    if (e < QB * kD) sA[e] = av[j];
+  }
+  if (tid < (1 << VBITS)) vtab[tid] = vt;
   // key tables of the query tile (rows past B give zero tables)
+  __syncthreads();
   {
-    float cv[L::G];
-    table_centroids<KBITS>(k_cb, cv);
     const int v = tid % L::NV;
     for (int q = 0; q < QB; ++q) {
-      const bool live = b0 + q < B;
-      const float* a = A + (static_cast<size_t>(p) * B + (live ? b0 + q : b0)) * kD;
+      const float* a = sA + q * kD;
       float* tq = lut + q * L::NPI * L::NV;
       for (int g = tid / L::NV; g < L::NPI; g += kDecThreads / L::NV) {
         float acc = 0.f;
 #pragma unroll
-        for (int k = 0; k < L::G; ++k) acc = fmaf(__ldg(a + g * L::G + k), cv[k], acc);
-        tq[g * L::NV + v] = live ? acc : 0.f;
+        for (int k = 0; k < L::G; ++k) acc = fmaf(a[g * L::G + k], cv[k], acc);
+        tq[g * L::NV + v] = acc;
       }
     }
   }
   __syncthreads();
 
-  // logits, thread per key
-  float mx[QB];
-#pragma unroll
-  for (int q = 0; q < QB; ++q) mx[q] = -INFINITY;
-  for (int i = tid; i < n; i += kDecThreads) {
-    const uint4* kp = reinterpret_cast<const uint4*>(k_plane + (kbase + i) * (16 * KBITS));
-    uint32_t wd[4 * KBITS + 1];
-#pragma unroll
-    for (int r = 0; r < KBITS; ++r) {
-      const uint4 x = __ldg(kp + r);
-      wd[4 * r] = x.x; wd[4 * r + 1] = x.y; wd[4 * r + 2] = x.z; wd[4 * r + 3] = x.w;
-    }
-    wd[4 * KBITS] = 0u;
-    const float nk = __half2float(__ushort_as_half(__ldg(k_norm + kbase + i)));
-    float m[2][QB];
-#pragma unroll
-    for (int q = 0; q < QB; ++q) m[0][q] = m[1][q] = 0.f;
-#pragma unroll
-    for (int gi = 0; gi < L::NPI; ++gi) {
-      const int off = L::KB * gi;
-      const int wi = off >> 5, sh = off & 31;
-      const uint32_t val = (sh + L::KB <= 32) ? (wd[wi] >> sh) & (L::NV - 1)
-                                              : __funnelshift_r(wd[wi], wd[wi + 1], sh) & (L::NV - 1);
-#pragma unroll
-      for (int q = 0; q < QB; ++q) m[gi & 1][q] += lut[(q * L::NPI + gi) * L::NV + val];
-    }
-#pragma unroll
-    for (int q = 0; q < QB; ++q) {
-      const float s = scale * nk * (m[0][q] + m[1][q]);
-      logit[q * chunk + i] = s;
-      mx[q] = fmaxf(mx[q], s);
-    }
-  }
-  // chunk maximum per query
-#pragma unroll
-  for (int q = 0; q < QB; ++q) {
-    mx[q] = warp_max(mx[q]);
-    if (lane == 0) red[warp * QB + q] = mx[q];
-  }
-  __syncthreads();
-  float M[QB];
-#pragma unroll
-  for (int q = 0; q < QB; ++q) {
-    M[q] = red[q];
-    for (int w = 1; w < kW; ++w) M[q] = fmaxf(M[q], red[w * QB + q]);
-  }
-  __syncthreads();
-  // weights exp(s - max) in place, and their sum per query
-  float sum[QB];
-#pragma unroll
-  for (int q = 0; q < QB; ++q) sum[q] = 0.f;
-  for (int i = tid; i < n; i += kDecThreads) {
-#pragma unroll
-    for (int q = 0; q < QB; ++q) {
-      const float e = expf(logit[q * chunk + i] - M[q]);
-      logit[q * chunk + i] = e;
-      sum[q] += e;
-    }
-  }
-#pragma unroll
-  for (int q = 0; q < QB; ++q) {
-    sum[q] = warp_sum(sum[q]);
-    if (lane == 0) red[warp * QB + q] = sum[q];
-  }
-  __syncthreads();
-  float Ls[QB];
-#pragma unroll
-  for (int q = 0; q < QB; ++q) {
-    Ls[q] = 0.f;
-    for (int w = 0; w < kW; ++w) Ls[q] += red[w * QB + q];
-  }
-  __syncthreads();
-
-  // weighted value codewords, warp per key; lane l owns coordinates 4l .. 4l+3, whose
-  // codes are bits 4*VBITS*l .. 4*VBITS*l + 4*VBITS-1 of the key's value row
-  float vc[1 << VBITS];
-#pragma unroll
-  for (int k = 0; k < (1 << VBITS); ++k) vc[k] = __ldg(v_cb + k);
-  constexpr int kVW = 4 * VBITS;          // 32-bit words of one value row
-  const int bit0 = 4 * VBITS * lane;
+  // online softmax over the warp's steps: logits (lane per key), the step maximum, the
+  // rescale of what came before, then the weighted value centroids.  Values: KPI keys
+  // at a time, LPK = 32 / KPI lanes per key, lane sub = lane % LPK owning CPL = 128 / LPK
+  // coordinates CPL*sub .. CPL*sub + CPL-1, whose codes are the bits from VBITS*CPL*sub
+  // on of the value row; a code becomes its centroid by one read of the shared table.
+  // Four keys at a time (8 lanes per key) for up to two queries, else one.
+  constexpr int KPI = QB <= 2 ? 4 : 1;
+  constexpr int LPK = 32 / KPI, CPL = kD / LPK, NB = VBITS * CPL;
+  constexpr uint32_t kMask = (1u << VBITS) - 1u;
+  const int slot = lane / LPK, sub = lane % LPK;
+  const int bit0 = NB * sub;
   const int wlo = bit0 >> 5, bsh = bit0 & 31;
-  float acc[QB][4];
-#pragma unroll
-  for (int q = 0; q < QB; ++q) acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0.f;
-  for (int i = warp; i < n; i += kW) {
-    const uint32_t* vr = reinterpret_cast<const uint32_t*>(v_plane + (kbase + i) * (16 * VBITS));
-    const uint32_t word = lane < kVW ? __ldg(vr + lane) : 0u;
-    const uint32_t lo = __shfl_sync(0xffffffffu, word, wlo);
-    const uint32_t hi = __shfl_sync(0xffffffffu, word, wlo + 1);
-    const uint32_t codes = __funnelshift_r(lo, hi, bsh);
-    const float nv = __half2float(__ushort_as_half(__ldg(v_norm + kbase + i)));
-    float cw[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) cw[j] = nv * centroid_of<VBITS>(vc, (codes >> (VBITS * j)) & ((1u << VBITS) - 1u));
-#pragma unroll
-    for (int q = 0; q < QB; ++q) {
-      const float wq = logit[q * chunk + i];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) acc[q][j] = fmaf(wq, cw[j], acc[q][j]);
-    }
-  }
+  const bool two = bsh + NB > 32;          // the lane's codes straddle two words
+  bool landed = true;
+  float M[QB], Lp[QB], acc[QB][CPL];
 #pragma unroll
   for (int q = 0; q < QB; ++q) {
+    M[q] = -INFINITY;
+    Lp[q] = 0.f;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) red[(warp * QB + q) * kD + 4 * lane + j] = acc[q][j];
+    for (int j = 0; j < CPL; ++j) acc[q][j] = 0.f;
+  }
+#pragma unroll
+  for (int t = 0; t < kMaxBlk; ++t) {
+    if (t < nsteps) {
+      landed &= wait_phase0(bar0 + 8 * t);
+      const int r0 = w0 + t * kBlk;
+      const int i = r0 + lane;
+      float sc[QB];
+#pragma unroll
+      for (int q = 0; q < QB; ++q) sc[q] = -INFINITY;
+      if (i < w1) {
+        const uint4* kp = reinterpret_cast<const uint4*>(kst + static_cast<size_t>(i) * kKRow);
+        uint32_t wd[4 * KBITS + 1];
+#pragma unroll
+        for (int r = 0; r < KBITS; ++r) {
+          const uint4 x = kp[r];
+          wd[4 * r] = x.x; wd[4 * r + 1] = x.y; wd[4 * r + 2] = x.z; wd[4 * r + 3] = x.w;
+        }
+        wd[4 * KBITS] = 0u;
+        float m[2][QB];
+#pragma unroll
+        for (int q = 0; q < QB; ++q) m[0][q] = m[1][q] = 0.f;
+#pragma unroll
+        for (int gi = 0; gi < L::NPI; ++gi) {
+          const int off = L::KB * gi;
+          const int wi = off >> 5, sh = off & 31;
+          const uint32_t val = (sh + L::KB <= 32) ? (wd[wi] >> sh) & (L::NV - 1)
+                                                  : __funnelshift_r(wd[wi], wd[wi + 1], sh) & (L::NV - 1);
+#pragma unroll
+          for (int q = 0; q < QB; ++q) m[gi & 1][q] += lut[(q * L::NPI + gi) * L::NV + val];
+        }
+#pragma unroll
+        for (int q = 0; q < QB; ++q) sc[q] = scale * nk[t] * (m[0][q] + m[1][q]);
+      }
+      float w[QB];
+#pragma unroll
+      for (int q = 0; q < QB; ++q) {
+        const float mn = fmaxf(M[q], warp_max(sc[q]));     // finite: the step has a key
+        const float r = expf(M[q] - mn);                    // 0 on the first step
+        const float e = i < w1 ? expf(sc[q] - mn) : 0.f;
+        Lp[q] = fmaf(Lp[q], r, e);
+        w[q] = e * nv[t];
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) acc[q][j] *= r;
+        M[q] = mn;
+      }
+      const int cnt = min(kBlk, w1 - r0);
+#pragma unroll 2
+      for (int k = 0; k < cnt; k += KPI) {
+        const int kk = k + slot;                            // this lane's key of the step
+        const uint32_t* vr =
+            reinterpret_cast<const uint32_t*>(vst + static_cast<size_t>(r0 + min(kk, cnt - 1)) * kVRow);
+        const uint32_t lo = vr[wlo];
+        const uint32_t hi = two ? vr[wlo + 1] : 0u;
+        const uint32_t c0 = __funnelshift_r(lo, hi, bsh);  // code bits 0..31 of the lane
+        const uint32_t c1 = hi >> bsh;                      // code bits 32..63
+        float cw[CPL];
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) {
+          const int pj = VBITS * j;
+          const uint32_t code = pj + VBITS <= 32 ? (c0 >> pj) & kMask
+                                : pj >= 32       ? (c1 >> (pj - 32)) & kMask
+                                                 : __funnelshift_r(c0, c1, pj) & kMask;
+          cw[j] = vtab[code];
+        }
+#pragma unroll
+        for (int q = 0; q < QB; ++q) {
+          const float wsh = __shfl_sync(0xffffffffu, w[q], kk & 31);
+          const float wq = kk < cnt ? wsh : 0.f;
+#pragma unroll
+          for (int j = 0; j < CPL; ++j) acc[q][j] = fmaf(wq, cw[j], acc[q][j]);
+        }
+      }
+    }
+  }
+  // the key slots of a lane group hold partial sums of the same coordinates
+#pragma unroll
+  for (int o = LPK; o < 32; o <<= 1) {
+#pragma unroll
+    for (int q = 0; q < QB; ++q) {
+#pragma unroll
+      for (int j = 0; j < CPL; ++j) acc[q][j] += __shfl_xor_sync(0xffffffffu, acc[q][j], o);
+    }
+  }
+
+  // merge the warps: max, rescaled sums and accumulators, to the workspace
+  landed = __all_sync(0xffffffffu, landed);
+#pragma unroll
+  for (int q = 0; q < QB; ++q) {
+    const float ls = warp_sum(Lp[q]);
+    if (lane == 0) {
+      rmax[warp * QB + q] = M[q];                            // -inf for a warp without keys
+      rsum[warp * QB + q] = landed ? ls : __int_as_float(0x7fc00000);   // NaN: rows never landed
+    }
+    if (slot == 0) {
+#pragma unroll
+      for (int j = 0; j < CPL; ++j) racc[(warp * QB + q) * kD + CPL * sub + j] = acc[q][j];
+    }
   }
   __syncthreads();
   for (int e = tid; e < QB * kD; e += kDecThreads) {
     const int q = e / kD, d = e % kD;
     if (b0 + q >= B) continue;
-    float s = 0.f;
-    for (int w = 0; w < kW; ++w) s += red[(w * QB + q) * kD + d];
-    part[((static_cast<size_t>(p) * B + b0 + q) * nchunks + c) * kPart + 2 + d] = s;
-  }
-  if (tid < QB && b0 + tid < B) {
-    float* pp = part + ((static_cast<size_t>(p) * B + b0 + tid) * nchunks + c) * kPart;
-#pragma unroll
-    for (int q = 0; q < QB; ++q) {
-      if (q == tid) {
-        pp[0] = M[q];
-        pp[1] = Ls[q];
-      }
+    float mx = rmax[q];
+    for (int w = 1; w < kW; ++w) mx = fmaxf(mx, rmax[w * QB + q]);
+    float s = 0.f, ls = 0.f;
+    for (int w = 0; w < kW; ++w) {
+      const float f = expf(rmax[w * QB + q] - mx);
+      s = fmaf(racc[(w * QB + q) * kD + d], f, s);
+      ls = fmaf(rsum[w * QB + q], f, ls);
+    }
+    float* pp = part + ((static_cast<size_t>(p) * B + b0 + q) * nchunks + c) * kPart;
+    pp[kAcc + d] = s;
+    if (d == 0) {
+      pp[0] = mx;
+      pp[1] = ls;
     }
   }
 }
 
 // One query: merge the chunks (rescale by exp(max_c - max)), normalise, out = acc Pi_v.
-__global__ void __launch_bounds__(kD)
+// 512 threads.  Thread t first holds rows 32g .. 32g+31 of column d of Pi_v (g = t / 128,
+// d = t % 128), loaded before the wait on the split grid so that they overlap it.  Warp
+// w then takes the chunks w, w + 16, ..., ten at a time with all their loads in flight
+// at once (lane l: the chunk's max and sum, and acc coordinates 4l .. 4l+3), and keeps
+// a running (max, sum, acc) with the usual rescaling.  The 16 warps merge in shared
+// memory, the result is normalised, and thread (g, d) sums its 32 terms of out[d].
+constexpr int kCombThreads = 512;
+constexpr int kCombWarps = kCombThreads / 32;
+constexpr int kCombSlots = 10;            // chunks per warp and round
+
+__global__ void __launch_bounds__(kCombThreads)
 decode_combine_kernel(const float* __restrict__ part, const float* __restrict__ Pi_v,
                       float* __restrict__ out, int H, int B, int nchunks) {
-  __shared__ float sacc[kD];
-  const int b = blockIdx.x, p = blockIdx.y, h = p % H, d = threadIdx.x;
+  constexpr int kGroups = kCombThreads / kD;
+  constexpr int kRows = kD / kGroups;
+  __shared__ float wmax[kCombWarps];
+  __shared__ float wsum[kCombWarps];
+  __shared__ __align__(16) float wacc[kCombWarps][kD];
+  __shared__ float snorm[kD];
+  const int b = blockIdx.x, p = blockIdx.y, h = p % H, tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  const int d = tid & (kD - 1), g = tid / kD;
+  const float* Pv = Pi_v + static_cast<size_t>(h) * kD * kD + static_cast<size_t>(g) * kRows * kD + d;
+  float pv[kRows];
+#pragma unroll
+  for (int k = 0; k < kRows; ++k) pv[k] = __ldg(Pv + k * kD);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const float* pp = part + (static_cast<size_t>(p) * B + b) * nchunks * kPart;
-  float M = -INFINITY;
-  for (int c = 0; c < nchunks; ++c) M = fmaxf(M, pp[c * kPart]);
-  float Lsum = 0.f, a = 0.f;
-  for (int c = 0; c < nchunks; ++c) {
-    const float e = expf(pp[c * kPart] - M);
-    Lsum = fmaf(pp[c * kPart + 1], e, Lsum);
-    a = fmaf(pp[c * kPart + 2 + d], e, a);
+  float Mw = -INFINITY, Lw = 0.f;
+  float a[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int c0 = warp; c0 < nchunks; c0 += kCombWarps * kCombSlots) {
+    float2 ml[kCombSlots];
+    float4 x[kCombSlots];
+#pragma unroll
+    for (int j = 0; j < kCombSlots; ++j) {
+      const int c = c0 + j * kCombWarps;
+      if (c < nchunks) {
+        const float* pc = pp + static_cast<size_t>(c) * kPart;
+        ml[j] = *reinterpret_cast<const float2*>(pc);
+        x[j] = *reinterpret_cast<const float4*>(pc + kAcc + 4 * lane);
+      } else {
+        ml[j] = make_float2(-INFINITY, 0.f);
+        x[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    float mb = Mw;
+#pragma unroll
+    for (int j = 0; j < kCombSlots; ++j) mb = fmaxf(mb, ml[j].x);   // finite: chunk c0 exists
+    const float r = expf(Mw - mb);                                     // 0 on the first round
+    Lw *= r;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) a[k] *= r;
+#pragma unroll
+    for (int j = 0; j < kCombSlots; ++j) {
+      const float e = expf(ml[j].x - mb);
+      Lw = fmaf(ml[j].y, e, Lw);
+      a[0] = fmaf(x[j].x, e, a[0]);
+      a[1] = fmaf(x[j].y, e, a[1]);
+      a[2] = fmaf(x[j].z, e, a[2]);
+      a[3] = fmaf(x[j].w, e, a[3]);
+    }
+    Mw = mb;
   }
-  sacc[d] = a / Lsum;
+  if (lane == 0) {
+    wmax[warp] = Mw;                      // -inf for a warp without chunks
+    wsum[warp] = Lw;
+  }
+  *reinterpret_cast<float4*>(&wacc[warp][4 * lane]) = make_float4(a[0], a[1], a[2], a[3]);
   __syncthreads();
-  const float* Pv = Pi_v + static_cast<size_t>(h) * kD * kD;
+  if (tid < kD) {
+    float M = wmax[0];
+    for (int w = 1; w < kCombWarps; ++w) M = fmaxf(M, wmax[w]);
+    float t = 0.f, l = 0.f;
+    for (int w = 0; w < kCombWarps; ++w) {
+      const float f = expf(wmax[w] - M);
+      t = fmaf(wacc[w][tid], f, t);
+      l = fmaf(wsum[w], f, l);
+    }
+    snorm[tid] = t / l;
+  }
+  __syncthreads();
   float o = 0.f;
-#pragma unroll 8
-  for (int k = 0; k < kD; ++k) o = fmaf(sacc[k], __ldg(Pv + k * kD + d), o);
-  out[(static_cast<size_t>(p) * B + b) * kD + d] = o;
+#pragma unroll
+  for (int k = 0; k < kRows; ++k) o = fmaf(snorm[g * kRows + k], pv[k], o);
+  wacc[g][d] = o;
+  __syncthreads();
+  if (g == 0) {
+    float t = 0.f;
+#pragma unroll
+    for (int j = 0; j < kGroups; ++j) t += wacc[j][d];
+    out[(static_cast<size_t>(p) * B + b) * kD + d] = t;
+  }
 }
 
 template <int KBITS, int VBITS, int QB>
@@ -274,25 +435,36 @@ cudaError_t launch_decode_qb(const float* A, const uint8_t* k_plane, const uint1
   const uint64_t bit = 1ull << (dev & 63);
   if (!(configured.load(std::memory_order_acquire) & bit)) {
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(split_smem_floats<KBITS, QB>(kMaxChunk) * sizeof(float)));
+                             static_cast<int>(split_smem_bytes<KBITS, VBITS, QB>(kMaxChunk)));
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit, std::memory_order_acq_rel);
   }
-  // chunks of 256..2048 keys (a multiple of 256), enough of them for about two CTAs per SM
+  // chunks of 256..1024 keys, as many as give every SM one CTA (equal chunks, so that
+  // no SM gets more keys than another)
   const int qtiles = ceil_div(B, QB);
   const int64_t units = static_cast<int64_t>(P) * qtiles;
-  const int64_t per_unit = (2LL * sms + units - 1) / units;
+  const int64_t per_unit = (static_cast<int64_t>(sms) + units - 1) / units;
   int chunk = ceil_div(S, per_unit < 1 ? 1 : per_unit);
-  chunk = (chunk + 255) / 256 * 256;
   chunk = chunk < 256 ? 256 : (chunk > kMaxChunk ? kMaxChunk : chunk);
   const int nchunks = ceil_div(S, chunk);
-  const size_t smem = split_smem_floats<KBITS, QB>(chunk) * sizeof(float);
+  const size_t smem = split_smem_bytes<KBITS, VBITS, QB>(chunk);
   dim3 grid(nchunks, qtiles, P);
   kernel<<<grid, kDecThreads, smem, st>>>(A, k_plane, k_norm, k_cb, v_plane, v_norm, v_cb, part, B, S,
                                           chunk, nchunks, scale);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  decode_combine_kernel<<<dim3(B, P), kD, 0, st>>>(part, Pi_v, out, H, B, nchunks);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(B, P);
+  cfg.blockDim = dim3(kCombThreads);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, decode_combine_kernel, static_cast<const float*>(part), Pi_v, out, H, B,
+                         nchunks);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

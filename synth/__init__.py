@@ -63,7 +63,8 @@ class Workload:
     D: int
     mse_bits: int
     layout: str          # "unpacked" (uint8 idx + int8 signs), "packed" (bit planes) or
-                         # "mse" (code plane + fp16 norm, the MSE-only variant, no signs)
+                         # "mse" (code plane + fp16 norm, the MSE-only variant, no signs) or
+                         # "decode" (MSE keys and MSE values, for the fused decode)
     gamma_dtype: str     # "f32" or "f16" (for "mse": the dtype of the stored norm)
     q_dtype: str         # "f32" or "bf16"
 
@@ -95,6 +96,9 @@ WORKLOADS = {
     # 48 + 2 bytes per key, the same as the packed 3-bit cache of c2.
     "m1": Workload("m1_mse_decode_B1_S131072_3bit", 1005, 1, 1, 1, 131072, 128, 3,
                    "mse", "f16", "f32"),
+    # Fused decode (softmax and values) over MSE keys and values, 3-bit codes each.
+    "d1": Workload("d1_fused_decode_B1_S131072_k3v3", 1006, 1, 1, 1, 131072, 128, 3,
+                   "decode", "f16", "f32"),
 }
 
 

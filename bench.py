@@ -44,14 +44,17 @@ METRIC = "scores/sec and achieved HBM GB/s (fraction of ~8 TB/s) at 1 GB300"
 FALLBACK_HBM_GBS = 6800.0
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the scoring kernel, from
-# the ncu captures summarised under profiles/, keyed by (workload, path, kernel source
-# fingerprint).  A changed kernel source makes the figure stale and it is reported null.
+# the ncu captures summarised under profiles/, keyed by (workload, path, fingerprint of
+# that kernel's sources).  A changed kernel source makes the figure stale: it is
+# reported null.
 # Writes that were still in L2 when the kernel ended are not in the figure.
 NCU_TRAFFIC = {
-    ("c1", "bf16_mma", "7ce1b9e87f60"): 8849152,      # scores_mma_kernel, unpacked, lite
-    ("c2", "fp32", "7ce1b9e87f60"): 6705920,          # solve_packed_lut_kernel, cluster of 8
-    ("c3", "fp32", "7ce1b9e87f60"): 256595968,        # scores_packed_lut_kernel, stream-K
-    ("c4", "bf16_mma", "7ce1b9e87f60"): 89685760,     # scores_mma_kernel, packed 3-bit, full
+    ("c1", "bf16_mma", "66e6aa6293ca"): 8580864,      # scores_mma_kernel, unpacked, lite
+    ("c2", "fp32", "5f6326e46e87"): 6705408,          # solve_packed_lut_kernel, cluster of 8
+    ("c3", "fp32", "5f6326e46e87"): 256021760,        # scores_packed_lut_kernel, stream-K
+    ("c4", "bf16_mma", "66e6aa6293ca"): 88979456,     # scores_mma_kernel, packed 3-bit, full
+    ("m1", "fp32", "b3d769f43720"): 6573056,          # scores_mse_lut_kernel, stream-K
+    ("d1", "fp32", "b60bb5d59927"): 13316608,         # decode_split_kernel + decode_combine_kernel
 }
 
 
@@ -130,10 +133,26 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_fingerprint() -> str:
+# The sources each kind of dominant kernel is built from: a traffic figure goes stale
+# only when one of its own kernel's sources changes.
+KERNEL_SOURCES = {
+    "mma": ("tq_scores_mma.cu", "tq_internal.cuh"),
+    "simt": ("tq_scores_simt.cu", "tq_lut.cuh", "tq_internal.cuh"),
+    "mse": ("tq_scores_mse.cu", "tq_lut.cuh", "tq_internal.cuh"),
+    "decode": ("tq_decode.cu", "tq_lut.cuh", "tq_internal.cuh"),
+}
+
+
+def kernel_family(w, path) -> str:
+    if w.layout in ("mse", "decode"):
+        return w.layout
+    return "mma" if path == "bf16_mma" else "simt"
+
+
+def kernel_fingerprint(family: str) -> str:
     import hashlib
     h = hashlib.sha1()
-    for name in sorted(os.listdir(os.path.join(ROOT, "compressed_kv_cache_gb300", "csrc"))):
+    for name in KERNEL_SOURCES[family]:
         with open(os.path.join(ROOT, "compressed_kv_cache_gb300", "csrc", name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
@@ -508,7 +527,7 @@ def main():
     peak, peak_src = hbm_peak()
     kbytes = score_kernel_bytes(w) + (fused_kernel_extra_bytes(w) if fused_single else 0)
     achieved = kbytes / (kernel_ms / 1e3) / 1e9
-    fp = kernel_fingerprint()
+    fp = kernel_fingerprint(kernel_family(w, path))
     traffic = NCU_TRAFFIC.get((args.config, path, fp))
 
     # end to end through the public fused API with host buffers

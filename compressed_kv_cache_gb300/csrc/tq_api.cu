@@ -208,7 +208,8 @@ tq_status tq_solve(const void* Q, tq_qtype qtype, const uint8_t* K_idx, const in
   uint16_t* Y = (p == TQ_PATH_BF16_MMA && y_bytes(P, B, D) > 0)
                     ? reinterpret_cast<uint16_t*>(static_cast<char*>(workspace) + 2 * at_bytes(P, B, D))
                     : nullptr;
-  if ((st = from_cuda(tq::launch_prepare(Q, qtype, Pi, S_mat, A, T, P, H, B, D, stream, Y))) != TQ_OK)
+  if ((st = from_cuda(tq::launch_prepare(Q, qtype, Pi, S_mat, A, T, P, H, B, D, stream, Y, nullptr,
+                                         Y != nullptr && tq::mma_shares_sm(P, B, S)))) != TQ_OK)
     return st;
   return run_unpacked(A, T, K_idx, signs, gamma, codebook, scores, P, B, S, D, C, p, stream, true, Y);
 }
@@ -237,7 +238,8 @@ tq_status tq_solve_packed(const void* Q, tq_qtype qtype, const uint8_t* idx_plan
   uint16_t* Y = (p == TQ_PATH_BF16_MMA && y_bytes(P, B, D) > 0)
                     ? reinterpret_cast<uint16_t*>(static_cast<char*>(workspace) + 2 * at_bytes(P, B, D))
                     : nullptr;
-  if ((st = from_cuda(tq::launch_prepare(Q, qtype, Pi, S_mat, A, T, P, H, B, D, stream, Y))) != TQ_OK)
+  if ((st = from_cuda(tq::launch_prepare(Q, qtype, Pi, S_mat, A, T, P, H, B, D, stream, Y, nullptr,
+                                         Y != nullptr && tq::mma_shares_sm(P, B, S)))) != TQ_OK)
     return st;
   return run_packed(A, T, idx_plane, sign_plane, gamma_f16, codebook, scores, P, B, S, D, idx_bits,
                     p, stream, true, Y);

@@ -437,8 +437,13 @@ cudaError_t launch_decode_qb(const float* A, const uint8_t* k_plane, const uint1
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(split_smem_bytes<KBITS, VBITS, QB>(kMaxChunk)));
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e != cudaSuccess) return e;
     configured.fetch_or(bit, std::memory_order_acq_rel);
   }
+  static std::atomic<uint64_t> carve_combine{0};
+  e = prefer_max_shared(decode_combine_kernel, carve_combine);
+  if (e != cudaSuccess) return e;
   // chunks of 256..1024 keys, as many as give every SM one CTA (equal chunks, so that
   // no SM gets more keys than another)
   const int qtiles = ceil_div(B, QB);

@@ -1,6 +1,8 @@
 // Internal declarations shared by the libtq translation units (not part of the ABI).
 #pragma once
 
+#include <atomic>
+
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
 #include <cuda_bf16.h>
@@ -19,6 +21,22 @@ inline float qjl_scale(int D) { return kSqrtHalfPi / static_cast<float>(D); }
 // ---- launchers (return the CUDA error of the launch, cudaSuccess otherwise) ----
 
 // Query tile of the tensor-core path: NT = min(B, 128) rounded up to 16, ceil(B/NT) tiles.
+// A kernel launched as a programmatic dependent shares SMs with the grid before it only
+// when both run under the same L1 / shared-memory split, so every kernel of such a pair
+// asks for the largest shared-memory carveout.  Set once per device and kernel.
+template <typename Kernel>
+inline cudaError_t prefer_max_shared(Kernel kernel, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  if (e != cudaSuccess) return e;
+  done.fetch_or(bit, std::memory_order_acq_rel);
+  return cudaSuccess;
+}
+
 inline int mma_query_tile(int B) { const int n = B < 128 ? B : 128; return (n + 15) / 16 * 16; }
 inline int mma_query_tiles(int B) { const int nt = mma_query_tile(B); return (B + nt - 1) / nt; }
 // Bytes of the bf16 query operand of the tensor-core path for P problems (D = 128):
@@ -30,9 +48,12 @@ inline size_t mma_y_bytes(int P, int B) {
 // Ybf (optional, D == 128 only): also write A and T as the tensor-core query operand.
 // hsigns (optional, [H][D] +-1, D a power of two): A = H diag(s) q by a fast
 // Walsh-Hadamard transform instead of the dense rows of Pi (Pi is then unused).
+// share_sm: the scorer launched next shares SMs with the transform (the two-CTA tensor-core
+// configuration, mma_shares_sm).
 cudaError_t launch_prepare(const void* Q, tq_qtype qtype, const float* Pi, const float* S_mat,
                            float* A, float* T, int P, int H, int B, int D, cudaStream_t st,
-                           uint16_t* Ybf = nullptr, const float* hsigns = nullptr);
+                           uint16_t* Ybf = nullptr, const float* hsigns = nullptr,
+                           bool share_sm = false);
 
 cudaError_t launch_scores_unpacked_fp32(const float* A, const float* T, const uint8_t* K_idx,
                                         const int8_t* signs, const float* gamma,
@@ -62,6 +83,10 @@ cudaError_t launch_solve_packed_fused(const void* Q, tq_qtype qtype, const float
 // transform grid has completed.  Ybf: the query operand prepared by that transform
 // (one bulk copy per CTA instead of converting A and T).
 bool mma_path_available();
+// Whether the tensor-core scorer runs in its two-CTA-per-SM configuration for this shape
+// (and so can share SMs with the query transform launched before it).
+bool mma_shares_sm(int P, int B, int S);
+
 cudaError_t launch_scores_mma(const float* A, const float* T, const uint8_t* idx,
                               const void* signs, const void* gamma, const float* codebook,
                               float* scores, int P, int B, int S, int C, int idx_bits,

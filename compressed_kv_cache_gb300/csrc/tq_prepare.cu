@@ -32,7 +32,9 @@ __device__ __forceinline__ float load_q(const __nv_bfloat16* q, size_t i) {
   return __bfloat162float(q[i]);
 }
 
-template <typename QT>
+// kShareSm only makes a second copy of the kernel, the one that runs ahead of a scorer
+// that shares its SMs (it carries the largest shared-memory carveout; see launch_prepare).
+template <typename QT, bool kShareSm>
 __global__ void __launch_bounds__(kWarps * 32)
 prepare_kernel(const QT* __restrict__ Q, const float* __restrict__ Pi,
                const float* __restrict__ Sm, float* __restrict__ A, float* __restrict__ T,
@@ -47,8 +49,36 @@ prepare_kernel(const QT* __restrict__ Q, const float* __restrict__ Pi,
   const int h = p % H;
   const int nq = min(kQ, B - b0);
   const size_t qbase = (static_cast<size_t>(p) * B + b0) * D;
-  for (int e = threadIdx.x; e < kQ * D; e += blockDim.x) {
-    sQ[e] = (e / D) < nq ? load_q(Q, qbase + e) : 0.f;
+  const int lane = threadIdx.x & 31;
+  const bool hadamard_slice = hsigns != nullptr && blockIdx.z == 0;
+  const int row = (hsigns != nullptr ? D + (static_cast<int>(blockIdx.z) - 1) * kWarps
+                                     : static_cast<int>(blockIdx.z) * kWarps) + (threadIdx.x >> 5);
+  const bool has_row = !hadamard_slice && row < 2 * D;
+  const bool is_t = row >= D;
+  const int d = is_t ? row - D : row;
+  const float* mrow = (is_t ? Sm : Pi) + (static_cast<size_t>(h) * D + (has_row ? d : 0)) * D;
+  // The warp's row of [Pi ; S_mat] (its first 128 columns) and the query tile are
+  // requested together, four query loads a thread in flight: one memory round trip.
+  constexpr int kPre = 4;
+  float mpre[kPre];
+#pragma unroll
+  for (int i = 0; i < kPre; ++i) {
+    const int j = lane + 32 * i;
+    mpre[i] = has_row && j < D ? __ldg(mrow + j) : 0.f;
+  }
+  constexpr int kU = 4;
+  for (int e0 = threadIdx.x; e0 < kQ * D; e0 += blockDim.x * kU) {
+    float v[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int e = e0 + u * static_cast<int>(blockDim.x);
+      v[u] = e < kQ * D && (e / D) < nq ? load_q(Q, qbase + e) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int e = e0 + u * static_cast<int>(blockDim.x);
+      if (e < kQ * D) sQ[e] = v[u];
+    }
   }
   // one output: A or T of query b0 + q, coordinate d (and its tensor-core operand copy)
   auto put = [&](bool is_t, int q, int d, float v) {
@@ -63,7 +93,7 @@ prepare_kernel(const QT* __restrict__ Q, const float* __restrict__ Pi,
       Ybf[off] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
     }
   };
-  if (hsigns != nullptr && blockIdx.z == 0) {
+  if (hadamard_slice) {
     const float* sg = hsigns + static_cast<size_t>(h) * D;
     for (int e = threadIdx.x; e < kQ * D; e += blockDim.x) sQ[e] *= __ldg(sg + e % D);
     const int half = D >> 1;
@@ -83,18 +113,21 @@ prepare_kernel(const QT* __restrict__ Q, const float* __restrict__ Pi,
     return;
   }
   __syncthreads();
-  const int lane = threadIdx.x & 31;
-  const int row = (hsigns != nullptr ? D + (blockIdx.z - 1) * kWarps : blockIdx.z * kWarps) + (threadIdx.x >> 5);
-  if (row >= 2 * D) return;
-  const bool is_t = row >= D;
-  const int d = is_t ? row - D : row;
-  const float* mrow = (is_t ? Sm : Pi) + (static_cast<size_t>(h) * D + d) * D;
+  if (!has_row) return;
 
   float acc[kQ];
 #pragma unroll
   for (int q = 0; q < kQ; ++q) acc[q] = 0.f;
+#pragma unroll
+  for (int i = 0; i < kPre; ++i) {
+    const int j = lane + 32 * i;
+    if (j < D) {
+#pragma unroll
+      for (int q = 0; q < kQ; ++q) acc[q] = fmaf(mpre[i], sQ[q * D + j], acc[q]);
+    }
+  }
 #pragma unroll 4
-  for (int j = lane; j < D; j += 32) {
+  for (int j = lane + 32 * kPre; j < D; j += 32) {
     const float m = __ldg(mrow + j);
 #pragma unroll
     for (int q = 0; q < kQ; ++q) acc[q] = fmaf(m, sQ[q * D + j], acc[q]);
@@ -113,25 +146,43 @@ prepare_kernel(const QT* __restrict__ Q, const float* __restrict__ Pi,
   }
 }
 
-}  // namespace
-
-cudaError_t launch_prepare(const void* Q, tq_qtype qtype, const float* Pi, const float* S_mat,
-                           float* A, float* T, int P, int H, int B, int D, cudaStream_t st,
-                           uint16_t* Ybf, const float* hsigns) {
+template <typename QT, bool kShareSm>
+cudaError_t launch_prepare_t(const QT* Q, const float* Pi, const float* S_mat, float* A, float* T,
+                             int P, int H, int B, int D, cudaStream_t st, uint16_t* Ybf,
+                             const float* hsigns) {
+  // A scorer launched behind this grid as a programmatic dependent shares its SMs only
+  // when both kernels run under the same L1 / shared-memory split.  The copy of the
+  // transform that runs ahead of such a scorer takes the largest carveout, as the scorer
+  // does; the other copy keeps the default, which suits kernels that cannot share an SM
+  // with it anyway.
+  if constexpr (kShareSm) {
+    static std::atomic<uint64_t> carve{0};
+    cudaError_t e = prefer_max_shared(prepare_kernel<QT, true>, carve);
+    if (e != cudaSuccess) return e;
+  }
   // dense: 2D output rows in slices of kWarps; Hadamard: slice 0 for A, then the D rows of T
   dim3 grid(ceil_div(B, kQ), P, hsigns != nullptr ? 1 + ceil_div(D, kWarps) : ceil_div(2 * D, kWarps));
   const size_t smem = static_cast<size_t>(kQ) * D * sizeof(float);
   const int NT = mma_query_tile(B), qtiles = mma_query_tiles(B);
+  prepare_kernel<QT, kShareSm><<<grid, kWarps * 32, smem, st>>>(Q, Pi, S_mat, A, T, H, B, D, Ybf, NT, qtiles,
+                                                                hsigns);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prepare(const void* Q, tq_qtype qtype, const float* Pi, const float* S_mat,
+                           float* A, float* T, int P, int H, int B, int D, cudaStream_t st,
+                           uint16_t* Ybf, const float* hsigns, bool share_sm) {
   if (D != 128) Ybf = nullptr;
   if (qtype == TQ_Q_BF16) {
-    prepare_kernel<__nv_bfloat16><<<grid, kWarps * 32, smem, st>>>(
-        static_cast<const __nv_bfloat16*>(Q), Pi, S_mat, A, T, H, B, D, Ybf, NT, qtiles, hsigns);
-  } else {
-    prepare_kernel<float><<<grid, kWarps * 32, smem, st>>>(static_cast<const float*>(Q), Pi,
-                                                           S_mat, A, T, H, B, D, Ybf, NT, qtiles,
-                                                           hsigns);
+    const auto* q = static_cast<const __nv_bfloat16*>(Q);
+    return share_sm ? launch_prepare_t<__nv_bfloat16, true>(q, Pi, S_mat, A, T, P, H, B, D, st, Ybf, hsigns)
+                    : launch_prepare_t<__nv_bfloat16, false>(q, Pi, S_mat, A, T, P, H, B, D, st, Ybf, hsigns);
   }
-  return cudaGetLastError();
+  const auto* q = static_cast<const float*>(Q);
+  return share_sm ? launch_prepare_t<float, true>(q, Pi, S_mat, A, T, P, H, B, D, st, Ybf, hsigns)
+                  : launch_prepare_t<float, false>(q, Pi, S_mat, A, T, P, H, B, D, st, Ybf, hsigns);
 }
 
 }  // namespace tq

@@ -377,7 +377,10 @@ __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.w
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 template <int LAYOUT, int EPIW, int XS>
-__global__ void __launch_bounds__(Cfg<EPIW>::kThreads, (EPIW == 4 ? 2 : 1))
+// The lite configuration keeps to 64 registers a thread: two of its CTAs then fit on an
+// SM next to a CTA of the query transform, so that none of them waits for the transform's
+// CTAs to leave before it can start (programmatic dependent launch).
+__global__ void __launch_bounds__(Cfg<EPIW>::kThreads) __maxnreg__(EPIW == 4 ? 64 : 72)
 scores_mma_kernel(const __grid_constant__ Params prm) {
   constexpr int kEpilogueThreads = Cfg<EPIW>::kEpilogueThreads;
   constexpr int kMmaWarp = Cfg<EPIW>::kMmaWarp;
@@ -464,6 +467,9 @@ scores_mma_kernel(const __grid_constant__ Params prm) {
       for (int j = 0; j < kRawStages && static_cast<int>(blockIdx.x) + j * gx < prm.key_tiles; ++j) issue_rows(j);
     }
   }
+  // The codebook (independent of the transform) is requested first, ahead of the key rows.
+  const int C = prm.C;
+  const float cval = tid < C ? __ldg(prm.codebook + tid) : 0.f;
   // With the query operand prepared by the transform (one bulk copy), producers request
   // their first tile's rows before the rest of the set-up, so the loads are in flight
   // while the transform finishes and TMEM is prepared.  Without it, the rows are
@@ -480,27 +486,17 @@ scores_mma_kernel(const __grid_constant__ Params prm) {
 
   // --- set-up: TMEM, barriers, tables, the query operand ---
   if (warp == kMmaWarp) tmem_alloc(smem_u32(tslot), prm.tmem_cols);
-  // When launched right behind the query transform of the same call (programmatic
-  // dependent launch), everything above ran while the transform was still going;
-  // A and T are read only after this wait, which returns once that grid is complete.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  // One round trip for every global input of the set-up: each thread requests its
-  // codebook entry and its chunks of A/T, then converts and stores them.
-  const int C = prm.C;
-  const float cval = tid < C ? __ldg(prm.codebook + tid) : 0.f;
   const uint32_t ybytes = static_cast<uint32_t>(NT) * 512u;
-  if (prm.Ybf != nullptr) {
-    // the transform already wrote this tile of the query operand: one bulk copy
-    if (tid == 0) {
-      asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(y_bar),
-                   "r"(ybytes)
-                   : "memory");
-      const uint16_t* src = prm.Ybf + (static_cast<size_t>(p) * gridDim.y + blockIdx.y) * NT * 256;
-      asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_u32(Yp)),
-                   "l"(src), "r"(ybytes), "r"(y_bar)
-                   : "memory");
-    }
-  } else {  // Y: query n (row) x 256 K, bf16, core-matrix layout; queries past B are zero
+  // With the query operand prepared by the transform, only the MMA issuer reads what the
+  // transform wrote: it alone waits for that grid (below), and the set-up and the
+  // producers' first tiles proceed while the transform is still running.
+  if (prm.Ybf == nullptr) {
+    // A and T are read after this wait, which returns once a transform launched right
+    // before this grid (programmatic dependent launch) is complete.  One round trip for
+    // the set-up's global inputs: each thread requests its chunks of A/T, then converts
+    // and stores them.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // Y: query n (row) x 256 K, bf16, core-matrix layout; queries past B are zero
     const uint32_t ybase = smem_u32(Yp);
     const int ngroups = NT / 8;
     // pairs of float4 in flight per thread (fewer next to the larger unpacked key registers)
@@ -700,6 +696,18 @@ scores_mma_kernel(const __grid_constant__ Params prm) {
     // -------------------------------- MMA ----------------------------------
     if (lane == 0) {
       const uint32_t yaddr = smem_u32(Yp);
+      if (prm.Ybf != nullptr) {
+        // the transform wrote this tile of the query operand: wait for that grid, then
+        // one bulk copy
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(y_bar),
+                     "r"(ybytes)
+                     : "memory");
+        const uint16_t* src = prm.Ybf + (static_cast<size_t>(p) * gridDim.y + blockIdx.y) * NT * 256;
+        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_u32(Yp)),
+                     "l"(src), "r"(ybytes), "r"(y_bar)
+                     : "memory");
+      }
       bool y_ready = prm.Ybf == nullptr || wait_or_abort(y_bar, 0, abort_v);
       const uint32_t idesc = idesc_bf16(kM, NT);
       const uint32_t ylbo = (NT / 8) * 128;
@@ -819,15 +827,17 @@ cudaError_t launch_cfg(const Params& prm, int P, int qtiles, bool after_prepare,
   return cudaGetLastError();
 }
 
+// At most two tiles per SM: two lighter CTAs per SM run every tile at once.
+bool lite_layout(int NT, int64_t tiles, int sms) { return NT <= 64 && tiles <= 2LL * sms; }
+
 template <int LAYOUT>
 cudaError_t launch_layout(const Params& prm, int P, int qtiles, bool after_prepare, cudaStream_t st) {
   int dev = 0, sms = 148;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  // at most two tiles per SM: two lighter CTAs per SM run every tile at once
   const int64_t tiles = static_cast<int64_t>(prm.key_tiles) * qtiles * P;
-  if (prm.NT <= 64 && tiles <= 2LL * sms) return launch_cfg<LAYOUT, 4, 1>(prm, P, qtiles, after_prepare, sms, st);
+  if (lite_layout(prm.NT, tiles, sms)) return launch_cfg<LAYOUT, 4, 1>(prm, P, qtiles, after_prepare, sms, st);
   return launch_cfg<LAYOUT, 16, 1>(prm, P, qtiles, after_prepare, sms, st);
 }
 
@@ -865,6 +875,14 @@ bool encode_scores_map(CUtensorMap* map, float* scores, int P, int B, int S) {
 }  // namespace
 
 bool mma_path_available() { return true; }
+
+bool mma_shares_sm(int P, int B, int S) {
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t tiles = static_cast<int64_t>((S + kM - 1) / kM) * mma_query_tiles(B) * P;
+  return lite_layout(mma_query_tile(B), tiles, sms);
+}
 
 cudaError_t launch_scores_mma(const float* A, const float* T, const uint8_t* idx,
                               const void* signs, const void* gamma, const float* codebook,

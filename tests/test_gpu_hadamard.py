@@ -33,7 +33,7 @@ def assert_fp32(got, want):
 
 
 @pytest.mark.parametrize("D", [2, 8, 32, 64, 128, 256])
-@pytest.mark.parametrize("B", [1, 5, 8, 13])
+@pytest.mark.parametrize("B", [1, 5, 8, 13, 40])
 @pytest.mark.parametrize("qdt", ["f32", "bf16"])
 def test_prepare_hadamard(tq, D, B, qdt):
     P, H = 3, 2

@@ -493,13 +493,15 @@ __host__ __device__ constexpr int fused_threads() { return QB <= 2 ? 512 : 256; 
 template <int QB>
 __host__ __device__ constexpr int fused_min_blocks() { return 2; }
 
-// Shared memory of the fused kernel: the CTA's rows of [Pi; S_mat], two mbarriers,
-// its slice of A/T, all of A/T and the tables.
+// Shared memory of the fused kernel: the CTA's rows of [Pi; S_mat], three mbarriers,
+// its slice of A/T, all of A/T and the tables; then, when its key range is staged, the
+// range's code rows and sign rows.
 template <int BITS, int QB, int CS>
 constexpr size_t fused_smem_bytes() {
-  return (256 / CS) * 128 * sizeof(float) + 16 +
+  return (256 / CS) * 128 * sizeof(float) + 32 +
          ((256 / CS) * QB + QB * 256 + QB * LutShape<BITS>::PER_Q) * sizeof(float);
 }
+constexpr int kFusedStageMax = 48 * 1024;   // the largest key range staged in shared memory (bytes)
 
 // Bounded wait for the given phase parity of a local mbarrier (about a second at most).
 __device__ __forceinline__ bool wait_parity(uint32_t bar, uint32_t parity) {
@@ -578,17 +580,18 @@ solve_packed_lut_kernel(const QT* __restrict__ Q, const float* __restrict__ Pi,
                         const uint8_t* __restrict__ sign_plane,
                         const uint16_t* __restrict__ gamma_f16,
                         const float* __restrict__ codebook, float* __restrict__ scores, int B,
-                        int S, float kappa) {
+                        int S, float kappa, int staged) {
   constexpr int D = 128;
   constexpr int kT = fused_threads<QB>();
   constexpr int R = 256 / CS;                             // rows of [Pi; S_mat] per CTA
   static_assert(R % 8 == 0 && CS <= 32, "transform split");
   extern __shared__ __align__(16) float smem[];
   float* sRows = smem;                                    // [R][128]
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sRows + R * D);   // [0]: rows, [1]: A/T
-  float* sMine = reinterpret_cast<float*>(bar + 2);       // [R][QB]: this CTA's rows of A/T
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sRows + R * D);   // [0]: rows, [1]: A/T, [2]: keys
+  float* sMine = reinterpret_cast<float*>(bar + 4);       // [R][QB]: this CTA's rows of A/T
   float* sAT = sMine + R * QB;                            // [256][QB]: rows of A, then of T
   float* lut = sAT + QB * 256;                            // [QB][PER_Q]
+  uint8_t* sKidx = reinterpret_cast<uint8_t*>(lut + QB * LutShape<BITS>::PER_Q);   // [range][16 BITS]
   const int p = blockIdx.z;
   const int h = p % H;
   const int b0 = blockIdx.y * QB;
@@ -599,15 +602,21 @@ solve_packed_lut_kernel(const QT* __restrict__ Q, const float* __restrict__ Pi,
   const int k_begin = static_cast<int>(min(static_cast<int64_t>(blockIdx.x) * chunk, static_cast<int64_t>(S)));
   const int k_end = k_begin + chunk < S ? k_begin + chunk : S;
   const int first = k_begin + tid;
+  // staged: the whole key range comes into shared memory by two bulk copies
+  const int nkeys = k_end - k_begin;
+  const bool stage = staged != 0 && nkeys > 0;
+  uint8_t* sKsg = sKidx + static_cast<size_t>(chunk) * (16 * BITS);                  // [range][16]
   const uint32_t rank = cluster_ctarank();
   const int row0 = static_cast<int>(rank) * R;
 
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const uint32_t bar_rows = static_cast<uint32_t>(__cvta_generic_to_shared(bar));
   const uint32_t bar_at = bar_rows + 8;
+  const uint32_t bar_keys = bar_rows + 16;
   if (tid == 0) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar_rows) : "memory");
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar_at) : "memory");
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar_keys) : "memory");
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     expect_bytes(bar_at, 256 * QB * 4);
   }
@@ -627,7 +636,7 @@ solve_packed_lut_kernel(const QT* __restrict__ Q, const float* __restrict__ Pi,
     // a short range of key rows (up to 64 KB) starts streaming from HBM into L2
     // now, through the copy engine rather than the load pipe, so the prologue's own
     // reads are not held up
-    if (k_end > k_begin && (k_end - k_begin) * (16 * BITS + 16) <= 65536) {
+    if (!stage && k_end > k_begin && (k_end - k_begin) * (16 * BITS + 16) <= 65536) {
       const size_t key0 = static_cast<size_t>(p) * S + k_begin;
       const uint32_t n = static_cast<uint32_t>(k_end - k_begin);
       asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(idx_plane + key0 * (16 * BITS)),
@@ -639,6 +648,9 @@ solve_packed_lut_kernel(const QT* __restrict__ Q, const float* __restrict__ Pi,
   }
   float cv[LutShape<BITS>::G];
   table_centroids<BITS>(codebook, cv);
+  // gamma of this thread's first key (staged ranges)
+  const float g_first =
+      stage && first < k_end ? __half2float(__ushort_as_half(__ldg(gamma_f16 + static_cast<size_t>(p) * S + first))) : 0.f;
   // rows of A/T: warp w takes groups of 8 rows; lane l reads coordinates 4l .. 4l+3
   // of each row (one conflict-free 512-byte row a warp) and the warp sums them.  Each
   // group goes to every CTA of the cluster by its own bulk copies, completing bytes
@@ -654,6 +666,20 @@ solve_packed_lut_kernel(const QT* __restrict__ Q, const float* __restrict__ Pi,
     }
   }
   const bool landed = wait_parity(bar_rows, 0);
+  // the query and the rows are in: the key range may stream in now, during the
+  // transform, the exchange and the tables
+  if (stage && tid == 0) {
+    const size_t key0 = static_cast<size_t>(p) * S + k_begin;
+    expect_bytes(bar_keys, static_cast<uint32_t>(nkeys * (16 * BITS + 16)));
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     static_cast<uint32_t>(__cvta_generic_to_shared(sKidx))),
+                 "l"(idx_plane + key0 * (16 * BITS)), "r"(static_cast<uint32_t>(nkeys * (16 * BITS))), "r"(bar_keys)
+                 : "memory");
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     static_cast<uint32_t>(__cvta_generic_to_shared(sKsg))),
+                 "l"(sign_plane + key0 * 16), "r"(static_cast<uint32_t>(nkeys * 16)), "r"(bar_keys)
+                 : "memory");
+  }
   if (warp < R / 8) {
     for (int g = warp; g < R / 8; g += kT / 32) {
       float part[QB][8];
@@ -685,7 +711,7 @@ solve_packed_lut_kernel(const QT* __restrict__ Q, const float* __restrict__ Pi,
   }
   // the first two keys of every thread, in flight during the exchange and the tables
   PackedKey<BITS> k0, k1;
-  prefetch_two_keys<BITS>(k0, k1, idx_plane, sign_plane, gamma_f16, p, first, kT, k_end, S);
+  if (!stage) prefetch_two_keys<BITS>(k0, k1, idx_plane, sign_plane, gamma_f16, p, first, kT, k_end, S);
   // every copy into this CTA has completed (so every peer is done reading the slices
   // it sent here); the cluster barrier below keeps each CTA alive until all have
   const bool have_at = wait_parity(bar_at, 0);
@@ -693,8 +719,30 @@ solve_packed_lut_kernel(const QT* __restrict__ Q, const float* __restrict__ Pi,
   build_luts<BITS, QB, kT>(
       [&](int q, int e) { return have_at ? sAT[e * QB + q] : __int_as_float(0x7fc00000); }, lut, cv);
   __syncthreads();
-  lut_score_keys<BITS, QB>(lut, idx_plane, sign_plane, gamma_f16, scores, k0, k1, first, kT, k_end,
-                           p, b0, B, S, kappa);
+  if (stage) {
+    // keys from the staged range; a range that never landed scores NaN
+    const bool have_keys = wait_parity(bar_keys, 0);
+    for (int s = first; s < k_end; s += kT) {
+      const int i = s - k_begin;
+      PackedKey<BITS> k;
+#pragma unroll
+      for (int r = 0; r < BITS; ++r)
+        k.idx[r] = *reinterpret_cast<const uint4*>(sKidx + static_cast<size_t>(i) * (16 * BITS) + 16 * r);
+      k.sg = *reinterpret_cast<const uint4*>(sKsg + static_cast<size_t>(i) * 16);
+      const float g = s == first ? g_first
+                                 : __half2float(__ushort_as_half(__ldg(gamma_f16 + static_cast<size_t>(p) * S + s)));
+      float mm[QB], rr[QB];
+      lut_key_sums<BITS, QB>(lut, k, mm, rr);
+      if (!have_keys) {
+#pragma unroll
+        for (int q = 0; q < QB; ++q) mm[q] = __int_as_float(0x7fc00000);
+      }
+      store_scores<QB>(scores, mm, rr, kappa * g, p, b0, B, S, s);
+    }
+  } else {
+    lut_score_keys<BITS, QB>(lut, idx_plane, sign_plane, gamma_f16, scores, k0, k1, first, kT, k_end,
+                             p, b0, B, S, kappa);
+  }
   cluster_wait();
 }
 
@@ -707,7 +755,8 @@ cudaError_t launch_fused_cs(const QT* Q, const float* Pi, const float* S_mat, in
                             const uint16_t* gamma_f16, const float* codebook, float* scores,
                             int P, int B, int S, cudaStream_t st) {
   constexpr int kT = fused_threads<QB>();
-  constexpr size_t smem = fused_smem_bytes<BITS, QB, CS>();
+  constexpr size_t smem_base = fused_smem_bytes<BITS, QB, CS>();
+  constexpr size_t smem_max = smem_base + kFusedStageMax;
   auto kernel = solve_packed_lut_kernel<BITS, QB, CS, QT>;
   static std::atomic<uint64_t> configured{0};
   static std::atomic<int> capacity[64];                   // co-resident clusters per device
@@ -724,11 +773,11 @@ cudaError_t launch_fused_cs(const QT* Q, const float* Pi, const float* S_mat, in
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.blockDim = dim3(kT);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = smem_max;          // the capacity below holds for any staged range
   cfg.stream = st;
   cfg.attrs = attr;
   if (!(configured.load(std::memory_order_acquire) & bit)) {
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_max));
     if (e != cudaSuccess) return e;
     int n = 0;
     cfg.gridDim = dim3(CS);
@@ -743,10 +792,16 @@ cudaError_t launch_fused_cs(const QT* Q, const float* Pi, const float* S_mat, in
   const int fill = static_cast<int>(capacity[dev & 63].load(std::memory_order_relaxed) / units);
   const int most = ceil_div(S, 64 * CS);                  // at least 64 keys a CTA on average
   const int clusters = fill < most ? fill : most;
-  cfg.gridDim = dim3((clusters < 1 ? 1 : clusters) * CS, qtiles, P);
+  const int gx = (clusters < 1 ? 1 : clusters) * CS;
+  cfg.gridDim = dim3(gx, qtiles, P);
   cfg.numAttrs = 2;
+  // the key range of a CTA (as the kernel cuts it) is staged when it fits
+  const int64_t chunk = (static_cast<int64_t>(S) + gx - 1) / gx;
+  const int64_t stage_bytes = chunk * (16 * BITS + 16);
+  const int staged = stage_bytes <= kFusedStageMax ? 1 : 0;
+  cfg.dynamicSmemBytes = smem_base + (staged ? static_cast<size_t>(stage_bytes) : 0);
   e = cudaLaunchKernelEx(&cfg, kernel, Q, Pi, S_mat, H, idx_plane, sign_plane, gamma_f16, codebook,
-                         scores, B, S, qjl_scale(128));
+                         scores, B, S, qjl_scale(128), staged);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

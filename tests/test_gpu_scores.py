@@ -237,6 +237,18 @@ def test_fused_solve_many_keys_per_thread(tq):
     assert_fp32(out[p, b, s], c.expected_sampled(p, b, s))
 
 
+@pytest.mark.parametrize("bits,S", [(2, 172_801), (3, 161_281)])
+def test_fused_solve_staged_range_two_keys_per_thread(tq, bits, S):
+    """Key ranges that the fused kernel stages in shared memory (up to 48 KB a CTA) yet
+    that hold more keys than its 512 threads: some threads score two staged keys.  The
+    last range is ragged."""
+    c = Case(1, 1, 2, S, 128, bits, seed=93 + bits, gamma_dtype="f16")
+    ip, sp = c.packed()
+    out = tq.solve_packed(q_tensor(c), dev(ip), dev(sp), f16(c.gamma), dev(c.Pi), dev(c.S_mat), dev(c.cb),
+                          c.bits, path="fp32").cpu().numpy()
+    assert_fp32(out, c.expected())
+
+
 def test_stream_k_ranges_cross_problems(tq):
     """Enough problems for the transform + stream-K scorer: CTA key ranges start and end
     inside problems, S is not a multiple of the block, and heads repeat every 4 problems."""

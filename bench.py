@@ -530,65 +530,79 @@ def main():
     fp = kernel_fingerprint(kernel_family(w, path))
     traffic = NCU_TRAFFIC.get((args.config, path, fp))
 
-    # end to end through the public fused API with host buffers
+    # end to end through the public fused API with host buffers: every step copies its
+    # inputs in from pinned host memory and its result out.  Steps alternate between two
+    # streams with their own device buffers, so one step's device-to-host read overlaps
+    # the next step's host-to-device copies (the two directions use separate engines).
     if True:
         hostQ = Q0.cpu().pin_memory()
         scratch = ("dout", "dws")             # decode outputs and workspace: not copied in
         hcache = {k: v.cpu().pin_memory() for k, v in cache0.items() if k not in scratch}
         hPi, hS, hcb = Pi.cpu().pin_memory(), S_mat.cpu().pin_memory(), cb.cpu().pin_memory()
         mse = w.layout in ("mse", "decode")   # no S_mat: the MSE-only paths need Pi alone
-        hout = torch.empty((w.P, w.B, w.S), dtype=torch.float32).pin_memory()
-        dQ, dcache = torch.empty_like(Q0), {k: torch.empty_like(v) for k, v in cache0.items()}
-        if w.layout == "decode":
-            hout = torch.empty((w.P, w.B, w.D), dtype=torch.float32).pin_memory()
-        dPi, dS, dcb = torch.empty_like(Pi), torch.empty_like(S_mat), torch.empty_like(cb)
-        dout = torch.empty((w.P, w.B, w.S), device=dev)
-        ws = torch.empty(tq.workspace_bytes(w.P, w.B, w.D), dtype=torch.uint8, device=dev)
+        out_shape = (w.P, w.B, w.D) if w.layout == "decode" else (w.P, w.B, w.S)
         h2d = (hostQ.numel() * hostQ.element_size() + sum(v.numel() * v.element_size() for v in hcache.values())
                + (hPi.numel() + (0 if mse else hS.numel()) + hcb.numel()) * 4)
-        dA, dT = torch.empty((w.P, w.B, w.D), device=dev), torch.empty((w.P, w.B, w.D), device=dev)
-        d2h = hout.numel() * 4
+        d2h = int(np.prod(out_shape)) * 4
+        e_streams = [stream, torch.cuda.Stream(device=dev)]
 
-        def e2e_step():
-            dQ.copy_(hostQ, non_blocking=True)
-            for k in hcache:
-                dcache[k].copy_(hcache[k], non_blocking=True)
-            dPi.copy_(hPi, non_blocking=True)
-            if not mse:
-                dS.copy_(hS, non_blocking=True)
-            dcb.copy_(hcb, non_blocking=True)
-            if w.layout == "decode":
-                tq.prepare_queries(dQ, dPi, dPi, out=(dA, dT))
-                score_call(tq, w, path, dA, dT, dcache, dcb, None)
-                hout.copy_(dcache["dout"], non_blocking=True)
-                return
-            if mse:
-                tq.prepare_queries(dQ, dPi, dPi, out=(dA, dT))
-                tq.scores_mse(dA, dcache["idx"], dcache["norm"], dcb, w.mse_bits, norm_correction=True,
-                              out=dout)
-            elif w.layout == "unpacked":
-                tq.solve(dQ, dcache["idx"], dcache["signs"], dcache["gamma"], dPi, dS, dcb, path=path,
-                         workspace=ws, out=dout)
-            else:
-                tq.solve_packed(dQ, dcache["idx"], dcache["signs"], dcache["gamma"], dPi, dS, dcb,
-                                w.mse_bits, path=path, workspace=ws, out=dout)
-            hout.copy_(dout, non_blocking=True)
+        def e2e_buffers():
+            return {"Q": torch.empty_like(Q0), "cache": {k: torch.empty_like(v) for k, v in cache0.items()},
+                    "Pi": torch.empty_like(Pi), "S": torch.empty_like(S_mat), "cb": torch.empty_like(cb),
+                    "out": torch.empty((w.P, w.B, w.S), device=dev),
+                    "ws": torch.empty(tq.workspace_bytes(w.P, w.B, w.D), dtype=torch.uint8, device=dev),
+                    "A": torch.empty((w.P, w.B, w.D), device=dev), "T": torch.empty((w.P, w.B, w.D), device=dev),
+                    "hout": torch.empty(out_shape, dtype=torch.float32).pin_memory()}
+        e_bufs = [e2e_buffers(), e2e_buffers()]
+
+        def e2e_step(k):
+            eb = e_bufs[k % 2]
+            with torch.cuda.stream(e_streams[k % 2]):
+                eb["Q"].copy_(hostQ, non_blocking=True)
+                for key in hcache:
+                    eb["cache"][key].copy_(hcache[key], non_blocking=True)
+                eb["Pi"].copy_(hPi, non_blocking=True)
+                if not mse:
+                    eb["S"].copy_(hS, non_blocking=True)
+                eb["cb"].copy_(hcb, non_blocking=True)
+                dc, dA, dT, dout = eb["cache"], eb["A"], eb["T"], eb["out"]
+                if w.layout == "decode":
+                    tq.prepare_queries(eb["Q"], eb["Pi"], eb["Pi"], out=(dA, dT))
+                    score_call(tq, w, path, dA, dT, dc, eb["cb"], None)
+                    eb["hout"].copy_(dc["dout"], non_blocking=True)
+                    return
+                if mse:
+                    tq.prepare_queries(eb["Q"], eb["Pi"], eb["Pi"], out=(dA, dT))
+                    tq.scores_mse(dA, dc["idx"], dc["norm"], eb["cb"], w.mse_bits, norm_correction=True,
+                                  out=dout)
+                elif w.layout == "unpacked":
+                    tq.solve(eb["Q"], dc["idx"], dc["signs"], dc["gamma"], eb["Pi"], eb["S"], eb["cb"],
+                             path=path, workspace=eb["ws"], out=dout)
+                else:
+                    tq.solve_packed(eb["Q"], dc["idx"], dc["signs"], dc["gamma"], eb["Pi"], eb["S"],
+                                    eb["cb"], w.mse_bits, path=path, workspace=eb["ws"], out=dout)
+                eb["hout"].copy_(dout, non_blocking=True)
+
+        def e2e_run(n):
+            # both streams start after the start event and the first waits for the second
+            es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            es.record(e_streams[0])
+            e_streams[1].wait_event(es)
+            for k in range(n):
+                e2e_step(k)
+            e_streams[0].wait_stream(e_streams[1])
+            ee.record(e_streams[0])
+            return es, ee
 
         e_steps = max(3, min(args.steps, 50))
-        with torch.cuda.stream(stream):
-            for _ in range(args.warmup):
-                e2e_step()
+        e2e_run(args.warmup)
         torch.cuda.synchronize(dev)
-        es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            es.record()
-            for _ in range(e_steps):
-                e2e_step()
-            ee.record()
+        es, ee = e2e_run(e_steps)
         torch.cuda.synchronize(dev)
         e_ms = es.elapsed_time(ee)
         e2e = {"value": scores_per_step * e_steps / (e_ms / 1e3), "unit": "scores/s",
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": e_steps}
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": e_steps,
+               "streams": 2}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -49,12 +49,12 @@ FALLBACK_HBM_GBS = 6800.0
 # reported null.
 # Writes that were still in L2 when the kernel ended are not in the figure.
 NCU_TRAFFIC = {
-    ("c1", "bf16_mma", "66e6aa6293ca"): 8580864,      # scores_mma_kernel, unpacked, lite
-    ("c2", "fp32", "5f6326e46e87"): 6705408,          # solve_packed_lut_kernel, cluster of 8
-    ("c3", "fp32", "5f6326e46e87"): 256021760,        # scores_packed_lut_kernel, stream-K
-    ("c4", "bf16_mma", "66e6aa6293ca"): 88979456,     # scores_mma_kernel, packed 3-bit, full
-    ("m1", "fp32", "b3d769f43720"): 6573056,          # scores_mse_lut_kernel, stream-K
-    ("d1", "fp32", "b60bb5d59927"): 13316608,         # decode_split_kernel + decode_combine_kernel
+    ("c1", "bf16_mma", "21322bf8f55c"): 8582144,      # scores_mma_kernel, unpacked, lite
+    ("c2", "fp32", "6978d1d8832c"): 6712832,          # solve_packed_lut_kernel, cluster of 8, staged keys
+    ("c3", "fp32", "6978d1d8832c"): 256041728,        # scores_packed_lut_kernel, stream-K
+    ("c4", "bf16_mma", "21322bf8f55c"): 89145600,     # scores_mma_kernel, packed 3-bit, full
+    ("m1", "fp32", "f5f64543fc36"): 6573312,          # scores_mse_lut_kernel, stream-K
+    ("d1", "fp32", "d664c21c33df"): 13317120,         # decode_split_kernel + decode_combine_kernel
 }
 
 

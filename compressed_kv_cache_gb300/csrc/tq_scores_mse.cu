@@ -52,7 +52,8 @@ __device__ __forceinline__ void store_mse(float* __restrict__ scores, const floa
 }
 
 // D = 128.  lut: [QB][NPI][NV] code tables; sq: [NV] sums of squared centroids of a
-// table value (the same for every position and query).
+// table value (the same for every position and query); sA: [QB][128] the segment's
+// rotated queries (one load round trip, requested ahead of the segment's keys).
 template <int BITS, int QB>
 __global__ void __launch_bounds__(256, 2)
 scores_mse_lut_kernel(const float* __restrict__ A, const uint8_t* __restrict__ idx_plane,
@@ -62,6 +63,7 @@ scores_mse_lut_kernel(const float* __restrict__ A, const uint8_t* __restrict__ i
   extern __shared__ __align__(16) float smem[];
   float* lut = smem;
   float* sq = lut + QB * L::NPI * L::NV;
+  float* sA = sq + L::NV;
   const int tid = threadIdx.x;
   const int v = tid % L::NV;
   float cv[L::G];
@@ -82,21 +84,34 @@ scores_mse_lut_kernel(const float* __restrict__ A, const uint8_t* __restrict__ i
     const int p = u / qtiles;
     const int b0 = (u - p * qtiles) * QB;
     const size_t base = static_cast<size_t>(p) * S;
-    // the segment's first two keys are requested before its tables are built
+    // the segment's rotated queries, then its first two keys, are requested before its
+    // tables are built (queries past B read as zero)
+    constexpr int kAP = (QB * 128 + 255) / 256;
+    float av[kAP];
+#pragma unroll
+    for (int j = 0; j < kAP; ++j) {
+      const int e = tid + 256 * j, q = e >> 7;
+      av[j] = e < QB * 128 && b0 + q < B ? __ldg(A + (static_cast<size_t>(p) * B + b0 + q) * 128 + (e & 127)) : 0.f;
+    }
     MseKey<BITS> k0, k1;
     const int first = sb + tid;
     if (first < se) load_mse_key<BITS>(k0, idx_plane, norm_f16, base + first);
     if (first + 256 < se) load_mse_key<BITS>(k1, idx_plane, norm_f16, base + first + 256);
     __syncthreads();                      // the previous segment's tables are no longer read
+#pragma unroll
+    for (int j = 0; j < kAP; ++j) {
+      const int e = tid + 256 * j;
+      if (e < QB * 128) sA[e] = av[j];
+    }
+    __syncthreads();
     for (int q = 0; q < QB; ++q) {
-      const bool live = b0 + q < B;
-      const float* a = A + (static_cast<size_t>(p) * B + (live ? b0 + q : b0)) * 128;
+      const float* a = sA + q * 128;
       float* tq = lut + q * L::NPI * L::NV;
       for (int g = tid / L::NV; g < L::NPI; g += 256 / L::NV) {
         float acc = 0.f;
 #pragma unroll
-        for (int k = 0; k < L::G; ++k) acc = fmaf(__ldg(a + g * L::G + k), cv[k], acc);
-        tq[g * L::NV + v] = live ? acc : 0.f;
+        for (int k = 0; k < L::G; ++k) acc = fmaf(a[g * L::G + k], cv[k], acc);
+        tq[g * L::NV + v] = acc;
       }
     }
     __syncthreads();
@@ -187,7 +202,7 @@ cudaError_t launch_mse_lut_qb(const float* A, const uint8_t* idx_plane, const ui
                               const float* codebook, float* scores, int P, int B, int S, bool corr,
                               cudaStream_t st) {
   using L = LutShape<BITS>;
-  const size_t smem = (static_cast<size_t>(QB) * L::NPI * L::NV + L::NV) * sizeof(float);
+  const size_t smem = (static_cast<size_t>(QB) * L::NPI * L::NV + L::NV + QB * 128) * sizeof(float);
   auto kernel = scores_mse_lut_kernel<BITS, QB>;
   static std::atomic<int> slots[64];      // co-resident CTAs per device
   int dev = 0;

@@ -359,7 +359,7 @@ __device__ __forceinline__ void prefetch_two_keys(PackedKey<BITS>& k0, PackedKey
 // end to end (unit-major), are cut into one equal contiguous range per CTA, so every
 // SM gets the same number of keys however the units divide.  A range crosses unit
 // boundaries at most a few times; at each one the CTA rebuilds its tables from that
-// unit's A and T (read through L1).  When launched right behind the query transform
+// unit's A and T (staged in shared memory).  When launched right behind the query transform
 // (programmatic dependent launch), the first keys and the codebook are requested
 // before griddepcontrol.wait and A and T after it.
 template <int BITS, int QB>
@@ -372,6 +372,7 @@ scores_packed_lut_kernel(const float* __restrict__ A, const float* __restrict__ 
                          int S, int qtiles, int64_t total, float kappa) {
   extern __shared__ __align__(16) float smem[];
   float* lut = smem;                      // [QB][NPI*NV + NPS*16]
+  float* sAT = lut + QB * LutShape<BITS>::PER_Q;   // [QB][256]: the unit's A, then T
   const int64_t per = (total + gridDim.x - 1) / gridDim.x;
   int64_t w = min(static_cast<int64_t>(blockIdx.x) * per, total);
   const int64_t wend = min(w + per, total);
@@ -392,15 +393,20 @@ scores_packed_lut_kernel(const float* __restrict__ A, const float* __restrict__ 
       asm volatile("griddepcontrol.wait;" ::: "memory");
       waited = true;
     }
+    // the unit's A and T rows: one load round trip (QB values a thread), staged in
+    // shared memory for the table build; queries past B read as zero
+    float at[QB];
+#pragma unroll
+    for (int j = 0; j < QB; ++j) {
+      const int e = static_cast<int>(threadIdx.x) + 256 * j, q = e >> 8, x = e & 255;
+      const size_t row = (static_cast<size_t>(p) * B + b0 + q) * 128;
+      at[j] = b0 + q < B ? (x < 128 ? __ldg(A + row + x) : __ldg(T + row + x - 128)) : 0.f;
+    }
     __syncthreads();                      // the previous segment's tables are no longer read
-    build_luts<BITS, QB, 256>(
-        [&](int q, int e) {
-          const bool live = b0 + q < B;
-          const size_t row = (static_cast<size_t>(p) * B + (live ? b0 + q : b0)) * 128;
-          const float x = e < 128 ? __ldg(A + row + e) : __ldg(T + row + e - 128);
-          return live ? x : 0.f;
-        },
-        lut, cv);
+#pragma unroll
+    for (int j = 0; j < QB; ++j) sAT[threadIdx.x + 256 * j] = at[j];
+    __syncthreads();
+    build_luts<BITS, QB, 256>([&](int q, int e) { return sAT[q * 256 + e]; }, lut, cv);
     __syncthreads();
     lut_score_keys<BITS, QB>(lut, idx_plane, sign_plane, gamma_f16, scores, k0, k1, first, 256, se,
                              p, b0, B, S, kappa);
@@ -414,7 +420,7 @@ cudaError_t launch_lut_qb(const float* A, const float* T, const uint8_t* idx_pla
                           const float* codebook, float* scores, int P, int B, int S,
                           bool after_prepare, cudaStream_t st) {
   using L = LutShape<BITS>;
-  const size_t smem = static_cast<size_t>(QB) * L::PER_Q * sizeof(float);
+  const size_t smem = static_cast<size_t>(QB) * (L::PER_Q + 256) * sizeof(float);
   auto kernel = scores_packed_lut_kernel<BITS, QB>;
   static std::atomic<int> slots[64];      // co-resident CTAs per device
   int dev = 0;

@@ -34,7 +34,8 @@ __device__ __forceinline__ float load_q(const __nv_bfloat16* q, size_t i) {
 
 // kShareSm only makes a second copy of the kernel, the one that runs ahead of a scorer
 // that shares its SMs (it carries the largest shared-memory carveout; see launch_prepare).
-template <typename QT, bool kShareSm>
+// kR: output rows per warp (4 for grids of many problems, so that they fit in one wave).
+template <typename QT, bool kShareSm, int kR>
 __global__ void __launch_bounds__(kWarps * 32)
 prepare_kernel(const QT* __restrict__ Q, const float* __restrict__ Pi,
                const float* __restrict__ Sm, float* __restrict__ A, float* __restrict__ T,
@@ -51,20 +52,27 @@ prepare_kernel(const QT* __restrict__ Q, const float* __restrict__ Pi,
   const size_t qbase = (static_cast<size_t>(p) * B + b0) * D;
   const int lane = threadIdx.x & 31;
   const bool hadamard_slice = hsigns != nullptr && blockIdx.z == 0;
-  const int row = (hsigns != nullptr ? D + (static_cast<int>(blockIdx.z) - 1) * kWarps
-                                     : static_cast<int>(blockIdx.z) * kWarps) + (threadIdx.x >> 5);
-  const bool has_row = !hadamard_slice && row < 2 * D;
-  const bool is_t = row >= D;
-  const int d = is_t ? row - D : row;
-  const float* mrow = (is_t ? Sm : Pi) + (static_cast<size_t>(h) * D + (has_row ? d : 0)) * D;
-  // The warp's row of [Pi ; S_mat] (its first 128 columns) and the query tile are
+  const int row0 = (hsigns != nullptr ? D + (static_cast<int>(blockIdx.z) - 1) * kWarps * kR
+                                      : static_cast<int>(blockIdx.z) * kWarps * kR) +
+                   (threadIdx.x >> 5) * kR;
+  auto row_ptr = [&](int row) {
+    const bool is_t = row >= D;
+    return (is_t ? Sm : Pi) + (static_cast<size_t>(h) * D + (is_t ? row - D : row)) * D;
+  };
+  // The warp's rows of [Pi ; S_mat] (their first 128 columns) and the query tile are
   // requested together, four query loads a thread in flight: one memory round trip.
   constexpr int kPre = 4;
-  float mpre[kPre];
+  float mpre[kR][kPre];
 #pragma unroll
-  for (int i = 0; i < kPre; ++i) {
-    const int j = lane + 32 * i;
-    mpre[i] = has_row && j < D ? __ldg(mrow + j) : 0.f;
+  for (int r = 0; r < kR; ++r) {
+    const int row = row0 + r;
+    const bool has = !hadamard_slice && row < 2 * D;
+    const float* mrow = row_ptr(has ? row : 0);
+#pragma unroll
+    for (int i = 0; i < kPre; ++i) {
+      const int j = lane + 32 * i;
+      mpre[r][i] = has && j < D ? __ldg(mrow + j) : 0.f;
+    }
   }
   constexpr int kU = 4;
   for (int e0 = threadIdx.x; e0 < kQ * D; e0 += blockDim.x * kU) {
@@ -113,40 +121,47 @@ prepare_kernel(const QT* __restrict__ Q, const float* __restrict__ Pi,
     return;
   }
   __syncthreads();
-  if (!has_row) return;
 
-  float acc[kQ];
 #pragma unroll
-  for (int q = 0; q < kQ; ++q) acc[q] = 0.f;
+  for (int r = 0; r < kR; ++r) {
+    const int row = row0 + r;
+    if (row >= 2 * D) break;                  // the same for the whole warp
+    const bool is_t = row >= D;
+    const int d = is_t ? row - D : row;
+    const float* mrow = row_ptr(row);
+    float acc[kQ];
 #pragma unroll
-  for (int i = 0; i < kPre; ++i) {
-    const int j = lane + 32 * i;
-    if (j < D) {
+    for (int q = 0; q < kQ; ++q) acc[q] = 0.f;
 #pragma unroll
-      for (int q = 0; q < kQ; ++q) acc[q] = fmaf(mpre[i], sQ[q * D + j], acc[q]);
+    for (int i = 0; i < kPre; ++i) {
+      const int j = lane + 32 * i;
+      if (j < D) {
+#pragma unroll
+        for (int q = 0; q < kQ; ++q) acc[q] = fmaf(mpre[r][i], sQ[q * D + j], acc[q]);
+      }
     }
-  }
 #pragma unroll 4
-  for (int j = lane + 32 * kPre; j < D; j += 32) {
-    const float m = __ldg(mrow + j);
+    for (int j = lane + 32 * kPre; j < D; j += 32) {
+      const float m = __ldg(mrow + j);
 #pragma unroll
-    for (int q = 0; q < kQ; ++q) acc[q] = fmaf(m, sQ[q * D + j], acc[q]);
-  }
+      for (int q = 0; q < kQ; ++q) acc[q] = fmaf(m, sQ[q * D + j], acc[q]);
+    }
 #pragma unroll
-  for (int q = 0; q < kQ; ++q) {
+    for (int q = 0; q < kQ; ++q) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc[q] += __shfl_xor_sync(0xffffffffu, acc[q], o);
-  }
-  if (lane < nq) {
-    float v = acc[0];
+      for (int o = 16; o > 0; o >>= 1) acc[q] += __shfl_xor_sync(0xffffffffu, acc[q], o);
+    }
+    if (lane < nq) {
+      float v = acc[0];
 #pragma unroll
-    for (int q = 1; q < kQ; ++q)
-      if (lane == q) v = acc[q];
-    put(is_t, lane, d, v);
+      for (int q = 1; q < kQ; ++q)
+        if (lane == q) v = acc[q];
+      put(is_t, lane, d, v);
+    }
   }
 }
 
-template <typename QT, bool kShareSm>
+template <typename QT, bool kShareSm, int kR>
 cudaError_t launch_prepare_t(const QT* Q, const float* Pi, const float* S_mat, float* A, float* T,
                              int P, int H, int B, int D, cudaStream_t st, uint16_t* Ybf,
                              const float* hsigns) {
@@ -157,15 +172,17 @@ cudaError_t launch_prepare_t(const QT* Q, const float* Pi, const float* S_mat, f
   // with it anyway.
   if constexpr (kShareSm) {
     static std::atomic<uint64_t> carve{0};
-    cudaError_t e = prefer_max_shared(prepare_kernel<QT, true>, carve);
+    cudaError_t e = prefer_max_shared(prepare_kernel<QT, true, kR>, carve);
     if (e != cudaSuccess) return e;
   }
-  // dense: 2D output rows in slices of kWarps; Hadamard: slice 0 for A, then the D rows of T
-  dim3 grid(ceil_div(B, kQ), P, hsigns != nullptr ? 1 + ceil_div(D, kWarps) : ceil_div(2 * D, kWarps));
+  // dense: 2D output rows in slices of kWarps * kR; Hadamard: slice 0 for A, then the D
+  // rows of T
+  dim3 grid(ceil_div(B, kQ), P,
+            hsigns != nullptr ? 1 + ceil_div(D, kWarps * kR) : ceil_div(2 * D, kWarps * kR));
   const size_t smem = static_cast<size_t>(kQ) * D * sizeof(float);
   const int NT = mma_query_tile(B), qtiles = mma_query_tiles(B);
-  prepare_kernel<QT, kShareSm><<<grid, kWarps * 32, smem, st>>>(Q, Pi, S_mat, A, T, H, B, D, Ybf, NT, qtiles,
-                                                                hsigns);
+  prepare_kernel<QT, kShareSm, kR><<<grid, kWarps * 32, smem, st>>>(Q, Pi, S_mat, A, T, H, B, D, Ybf, NT,
+                                                                    qtiles, hsigns);
   return cudaGetLastError();
 }
 
@@ -175,14 +192,30 @@ cudaError_t launch_prepare(const void* Q, tq_qtype qtype, const float* Pi, const
                            float* A, float* T, int P, int H, int B, int D, cudaStream_t st,
                            uint16_t* Ybf, const float* hsigns, bool share_sm) {
   if (D != 128) Ybf = nullptr;
+  // Four rows a warp once one row a warp would take more than two waves of CTAs (about
+  // eight 256-thread CTAs an SM): many problems, as in a GQA decode batch.
+  static std::atomic<int> sms_cache[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  int sms = sms_cache[dev & 63].load(std::memory_order_relaxed);
+  if (sms == 0) {
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    sms_cache[dev & 63].store(sms, std::memory_order_relaxed);
+  }
+  const int64_t ctas = static_cast<int64_t>(ceil_div(B, kQ)) * P * ceil_div(2 * D, kWarps);
+  const bool four = !share_sm && ctas > 2LL * 8 * sms;
   if (qtype == TQ_Q_BF16) {
     const auto* q = static_cast<const __nv_bfloat16*>(Q);
-    return share_sm ? launch_prepare_t<__nv_bfloat16, true>(q, Pi, S_mat, A, T, P, H, B, D, st, Ybf, hsigns)
-                    : launch_prepare_t<__nv_bfloat16, false>(q, Pi, S_mat, A, T, P, H, B, D, st, Ybf, hsigns);
+    if (share_sm) return launch_prepare_t<__nv_bfloat16, true, 1>(q, Pi, S_mat, A, T, P, H, B, D, st, Ybf, hsigns);
+    if (four) return launch_prepare_t<__nv_bfloat16, false, 4>(q, Pi, S_mat, A, T, P, H, B, D, st, Ybf, hsigns);
+    return launch_prepare_t<__nv_bfloat16, false, 1>(q, Pi, S_mat, A, T, P, H, B, D, st, Ybf, hsigns);
   }
   const auto* q = static_cast<const float*>(Q);
-  return share_sm ? launch_prepare_t<float, true>(q, Pi, S_mat, A, T, P, H, B, D, st, Ybf, hsigns)
-                  : launch_prepare_t<float, false>(q, Pi, S_mat, A, T, P, H, B, D, st, Ybf, hsigns);
+  if (share_sm) return launch_prepare_t<float, true, 1>(q, Pi, S_mat, A, T, P, H, B, D, st, Ybf, hsigns);
+  if (four) return launch_prepare_t<float, false, 4>(q, Pi, S_mat, A, T, P, H, B, D, st, Ybf, hsigns);
+  return launch_prepare_t<float, false, 1>(q, Pi, S_mat, A, T, P, H, B, D, st, Ybf, hsigns);
 }
 
 }  // namespace tq

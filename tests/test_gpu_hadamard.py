@@ -53,6 +53,23 @@ def test_prepare_hadamard(tq, D, B, qdt):
         assert_fp32(T[p].cpu().numpy(), q @ S_mat[h].astype(np.float64).T)
 
 
+@pytest.mark.parametrize("P,D", [(200, 64), (130, 128)])
+def test_prepare_hadamard_many_problems(tq, P, D):
+    """Enough problems that every warp of the transform takes four rows of S_mat."""
+    H, B = 4, 3
+    rng = np.random.default_rng(800 + P + D)
+    signs = rng.choice([-1.0, 1.0], size=(H, D)).astype(np.float32)
+    S_mat = rng.standard_normal((H, D, D)).astype(np.float32)
+    Q = rng.standard_normal((P, B, D)).astype(np.float32)
+    A, T = tq.prepare_queries_hadamard(dev(Q), dev(signs), dev(S_mat))
+    A, T = A.cpu().numpy(), T.cpu().numpy()
+    for p in range(P):
+        h = p % H
+        q = Q[p].astype(np.float64)
+        assert_fp32(A[p], oracle.fwht(q * signs[h]))
+        assert_fp32(T[p], q @ S_mat[h].astype(np.float64).T)
+
+
 def test_hadamard_rotation_through_the_whole_path(tq):
     """Keys compressed on the GPU with the dense H diag(s), queries transformed by the fast
     transform, packed fp32 scorer: the oracle's scores for the same rotation."""

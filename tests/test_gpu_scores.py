@@ -75,7 +75,9 @@ def test_worked_example(tq):
 
 @pytest.mark.parametrize("P,H,B,D", [(1, 1, 1, 2), (3, 2, 5, 37), (2, 2, 9, 128), (4, 4, 3, 256), (8, 8, 4, 128),
                                      # 32 queries per CTA from B = 32 on (D <= 256), ragged last tile
-                                     (2, 1, 37, 128), (1, 1, 64, 256), (2, 2, 33, 37), (1, 1, 96, 200)])
+                                     (2, 1, 37, 128), (1, 1, 64, 256), (2, 2, 33, 37), (1, 1, 96, 200),
+                                     # many problems: four rows a warp, ragged last slice at D = 37
+                                     (100, 4, 3, 128), (300, 3, 2, 37)])
 @pytest.mark.parametrize("qdt", ["f32", "bf16"])
 def test_prepare_queries(tq, P, H, B, D, qdt):
     c = Case(P, H, B, 1, D, 2, seed=50 + P + D, q_dtype=qdt, random_codebook=True)

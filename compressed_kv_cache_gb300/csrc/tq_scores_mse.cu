@@ -65,6 +65,10 @@ scores_mse_lut_kernel(const float* __restrict__ A, const uint8_t* __restrict__ i
   float* sq = lut + QB * L::NPI * L::NV;
   float* sA = sq + L::NV;
   const int tid = threadIdx.x;
+  // Launched as a programmatic dependent of whatever ran before it on the stream (the
+  // query transform, typically): every global read follows this wait, so the launch
+  // overlaps that kernel's tail and nothing else.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int v = tid % L::NV;
   float cv[L::G];
   table_centroids<BITS>(codebook, cv);
@@ -226,8 +230,19 @@ cudaError_t launch_mse_lut_qb(const float* A, const uint8_t* idx_plane, const ui
   const int64_t total = static_cast<int64_t>(P) * qtiles * S;
   const int64_t want = (total + 255) / 256;
   const unsigned grid = static_cast<unsigned>(want < n ? want : n);
-  kernel<<<grid, 256, smem, st>>>(A, idx_plane, norm_f16, codebook, scores, B, S, qtiles, total,
-                                  corr ? 1 : 0);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kernel, A, idx_plane, norm_f16, codebook, scores, B, S, qtiles, total,
+                         corr ? 1 : 0);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -53,7 +53,7 @@ NCU_TRAFFIC = {
     ("c2", "fp32", "2bf1566ae994"): 6713088,          # solve_packed_lut_kernel, cluster of 8, staged keys
     ("c3", "fp32", "2bf1566ae994"): 256231424,        # scores_packed_lut_kernel, stream-K
     ("c4", "bf16_mma", "21322bf8f55c"): 89145600,     # scores_mma_kernel, packed 3-bit, full
-    ("m1", "fp32", "d7f82160880c"): 6572544,          # scores_mse_lut_kernel, stream-K
+    ("m1", "fp32", "62ab8eab09d4"): 6573312,          # scores_mse_lut_kernel, stream-K
     ("d1", "fp32", "d664c21c33df"): 13317120,         # decode_split_kernel + decode_combine_kernel
 }
 

@@ -92,10 +92,10 @@ def workload_case(key: str) -> Case:
 
 
 def fp32_tol(expected):
-    """Spec bound of the fp32 path: 1e-5 (1 + |score|)."""
+    """Parity bound of the fp32 path: 1e-5 (1 + |score|)."""
     return 1e-5 * (1.0 + np.abs(expected))
 
 
 def bf16_tol(qnorm_b):
-    """Spec bound of the bf16 tensor-core path: 2e-3 ||q_b||_2."""
+    """Parity bound of the bf16 tensor-core path: 2e-3 ||q_b||_2."""
     return 2e-3 * qnorm_b

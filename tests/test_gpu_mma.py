@@ -1,6 +1,6 @@
 """GPU parity of the bf16 tensor-core path (tcgen05) against the CPU oracle.
 
-Bound (the benchmark spec): max |err| <= 2e-3 ||q_b||_2 against the float64 oracle on the
+Parity bound: max |err| <= 2e-3 ||q_b||_2 against the float64 oracle on the
 original queries.  The path rounds A, T and the centroids to bf16 (signs are exact)
 and sums in fp32.
 """

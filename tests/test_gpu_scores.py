@@ -1,6 +1,6 @@
 """GPU parity: every kernel of libtq against the CPU oracle, through the C ABI.
 
-Tolerances are the benchmark spec's bounds: fp32 path max |err| <= 1e-5 (1 + |score|);
+Tolerances are the parity bounds: fp32 path max |err| <= 1e-5 (1 + |score|);
 bf16 tensor-core path max |err| <= 2e-3 ||q_b||_2; packing bit-exact.
 """
 import numpy as np

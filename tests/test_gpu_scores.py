@@ -266,6 +266,59 @@ def test_stream_k_ranges_cross_problems(tq):
 
 
 # ---------------------------------------------------------------------------
+# degenerate inputs, on every scoring path
+# ---------------------------------------------------------------------------
+
+DEGENERATE_PATHS = ["unpacked_fp32", "unpacked_bf16_mma", "packed_fused", "packed_stream_k"]
+
+
+@pytest.mark.parametrize("path", DEGENERATE_PATHS)
+@pytest.mark.parametrize("case", ["zero_queries", "zero_gamma", "constant_codes"])
+def test_degenerate_inputs(tq, path, case):
+    """Zero queries score exactly 0; zero gamma leaves only the codebook term; one code and
+    one sign everywhere make every key the same vector.  S is ragged (300 keys)."""
+    D, S, bits = 128, 300, 2
+    B = {"unpacked_fp32": 3, "unpacked_bf16_mma": 16, "packed_fused": 1, "packed_stream_k": 4}[path]
+    rng = np.random.default_rng(1234 + DEGENERATE_PATHS.index(path))
+    from conftest import codebook
+    cb = codebook(D, bits)[0].astype(np.float32)
+    Pi = oracle.haar_rotation(rng.standard_normal((D, D))).astype(np.float32)
+    Sm = rng.standard_normal((D, D)).astype(np.float32)
+    Q = rng.standard_normal((B, D)).astype(np.float32)
+    idx = rng.integers(0, 1 << bits, (S, D)).astype(np.uint8)
+    sg = rng.choice(np.array([-1, 1], np.int8), (S, D))
+    gm = (0.1 + rng.random(S)).astype(np.float32)
+    if case == "zero_queries":
+        Q[:] = 0.0
+    elif case == "zero_gamma":
+        gm[:] = 0.0
+    else:
+        idx[:] = (1 << bits) - 1
+        sg[:] = 1
+    packed = path.startswith("packed")
+    if packed:
+        gm = gm.astype(np.float16)
+    want = oracle.scores_from_queries(Q, Pi, Sm, idx, sg, gm, cb)
+    if path == "unpacked_fp32" or path == "unpacked_bf16_mma":
+        got = tq.solve(dev(Q), dev(idx), dev(sg), dev(gm), dev(Pi), dev(Sm), dev(cb),
+                       path="fp32" if path == "unpacked_fp32" else "bf16_mma")
+    else:
+        ip, sp = dev(oracle.pack_indices(idx, bits)), dev(oracle.pack_signs(sg))
+        if path == "packed_fused":
+            got = tq.solve_packed(dev(Q), ip, sp, dev(gm), dev(Pi), dev(Sm), dev(cb), bits, path="fp32")
+        else:
+            A, T = tq.prepare_queries(dev(Q), dev(Pi), dev(Sm))
+            got = tq.scores_packed(A, T, ip, sp, dev(gm), dev(cb), bits, path="fp32")
+    got = got.cpu().numpy()
+    if case == "zero_queries":
+        assert (got == 0).all()
+    elif path == "unpacked_bf16_mma":
+        assert_bf16(got, want, np.linalg.norm(Q.astype(np.float64), axis=1)[:, np.newaxis])
+    else:
+        assert_fp32(got, want)
+
+
+# ---------------------------------------------------------------------------
 # properties
 # ---------------------------------------------------------------------------
 

@@ -45,7 +45,6 @@ __all__ = [
     "unpack_indices",
     "pack_signs",
     "unpack_signs",
-    "f16_round",
 ]
 
 SQRT_HALF_PI = math.sqrt(math.pi / 2.0)
@@ -74,26 +73,27 @@ def haar_rotation(G: np.ndarray) -> np.ndarray:
 
 
 def fwht(x: np.ndarray) -> np.ndarray:
-    """Orthonormal Walsh-Hadamard transform along the last axis (length a power of two),
-    by butterflies ([KB] §2 "randomized Hadamard transform", §3 Hadamard butterfly).
+    """Orthonormal Walsh-Hadamard transform along the last axis ([KB] §2 "randomized
+    Hadamard transform"; the length n must be a power of two).
 
-    Stage h = 1, 2, 4, ...: within every block of 2h entries, entry i of the first
-    half and entry i of the second half become (a + b, a - b); the result is divided
-    by sqrt(n), so the transform is its own inverse (Sylvester order).
+    The n x n Walsh-Hadamard matrix in Sylvester order is the k-fold Kronecker
+    power of H_2 = [[1, 1], [1, -1]] / sqrt(2) (n = 2^k), so its entry (i, j) is
+    (-1)^popcount(i & j) / sqrt(n).  Viewing the last axis as k axes of length 2
+    (index bits, most significant first), the transform applies H_2 along each of
+    those axes in turn.  The result is orthonormal and its own inverse.
     """
     y = np.array(x, dtype=np.float64, copy=True)
     n = y.shape[-1]
     if n < 1 or n & (n - 1):
         raise ValueError("length must be a power of two")
-    h = 1
-    while h < n:
-        for start in range(0, n, 2 * h):
-            a = y[..., start:start + h].copy()
-            b = y[..., start + h:start + 2 * h].copy()
-            y[..., start:start + h] = a + b
-            y[..., start + h:start + 2 * h] = a - b
-        h *= 2
-    return y / math.sqrt(n)
+    k = n.bit_length() - 1
+    lead = y.shape[:-1]
+    h2 = np.array([[1.0, 1.0], [1.0, -1.0]]) / math.sqrt(2.0)
+    t = y.reshape(lead + (2,) * k)
+    for axis in range(len(lead), len(lead) + k):
+        # contract H_2 with this bit axis, then put the new axis back in its place
+        t = np.moveaxis(np.tensordot(t, h2, axes=([axis], [1])), -1, axis)
+    return t.reshape(lead + (n,))
 
 
 def hadamard_rotation(signs: np.ndarray) -> np.ndarray:
@@ -118,49 +118,86 @@ def nearest_cell(values: np.ndarray, edges: np.ndarray) -> np.ndarray:
     return out
 
 
-def lloyd_max_sphere(d: int, mse_bits: int, grid: int = 400_001, iters: int = 300):
-    """Lloyd-Max codebook for one coordinate of a uniform unit vector in R^d ([KB] §3-§4).
+def _sphere_coordinate_moments(d: int):
+    """Exact cell moments of one coordinate x of a uniform unit vector in R^d.
 
-    The coordinate has density proportional to (1 - x^2)^((d-3)/2) on [-1, 1]
-    ([KB] §2 fact 1).  The density is sampled on ``grid`` evenly spaced points
-    and normalised to unit mass; the 2^b centroids start evenly spaced on
-    [-2/sqrt(d), 2/sqrt(d)]; each of ``iters`` rounds sets the cell edges to
-    the midpoints of the current centroids and then every centroid to the
-    mean of its cell under the density.
+    Its density is f(x) = (1 - x^2)^m / Z on [-1, 1] with m = (d - 3) / 2 ([KB] §2,
+    fact 1).  Substituting t = (1 + x) / 2 turns the mass below x into the
+    regularised incomplete beta function I_t(m + 1, m + 1).  The first moment has
+    the antiderivative -(1 - x^2)^(m+1) / (2 (m + 1)), and x^2 = 1 - (1 - x^2) writes
+    the second moment through the density of exponent m + 1, whose normaliser is
+    Z_{m+1} = Z_m (d - 1) / d (so that E[x^2] = 1 / d).  Returns three functions of
+    the cell edges (a, b): mass, first moment and second moment.
+    """
+    from scipy import special
+
+    m = (d - 3) / 2.0
+    log_z = (2.0 * m + 1.0) * math.log(2.0) + special.betaln(m + 1.0, m + 1.0)
+
+    def cdf(x, e):
+        t = np.clip((1.0 + np.asarray(x, dtype=np.float64)) / 2.0, 0.0, 1.0)
+        return special.betainc(e + 1.0, e + 1.0, t)
+
+    def mass(a, b):
+        return cdf(b, m) - cdf(a, m)
+
+    def first(a, b):
+        g = lambda x: np.clip(1.0 - np.asarray(x, dtype=np.float64) ** 2, 0.0, None) ** (m + 1.0)
+        return (g(a) - g(b)) / (2.0 * (m + 1.0)) / math.exp(log_z)
+
+    def second(a, b):
+        return mass(a, b) - (d - 1.0) / d * (cdf(b, m + 1.0) - cdf(a, m + 1.0))
+
+    return mass, first, second
+
+
+def lloyd_max_sphere(d: int, mse_bits: int, tol: float = 1e-13, max_rounds: int = 200_000):
+    """Lloyd-Max codebook for one coordinate of a uniform unit vector in R^d ([KB] §2-§4).
+
+    The codebook is the fixed point of Lloyd's two conditions for the density
+    (1 - x^2)^((d-3)/2) on [-1, 1]: every cell edge is the midpoint of its two
+    centroids, and every centroid is the mean of its cell.  Cell masses and
+    moments are evaluated exactly (:func:`_sphere_coordinate_moments`), not on a
+    grid.  The 2^b centroids start at the medians of 2^b equal-probability cells;
+    rounds of "edges from centroids, then centroids from edges" repeat until no
+    centroid moves by more than ``tol`` times the largest one (the float64 cell
+    moments carry about 1e-15 of rounding noise, so ``tol`` stays above it).  The
+    density is log-concave, so the fixed point is unique and the start does not
+    matter.
 
     Returns ``(centroids, edges, d_mse)`` in float64, where ``d_mse`` is
     d * E[(x - Q(x))^2], the expected squared error of a unit vector.
     """
     if d < 3:
         raise ValueError("the sphere-coordinate density needs d >= 3")
+    from scipy import special
+
+    mass, first, second = _sphere_coordinate_moments(d)
     C = 1 << mse_bits
-    x = np.linspace(-1.0, 1.0, grid)
-    dens = np.clip(1.0 - x * x, 0.0, None) ** ((d - 3) / 2.0)
-    dens = dens / dens.sum()
-    centroids = np.linspace(-2.0, 2.0, C) / math.sqrt(d)
-    for _ in range(iters):
+    m = (d - 3) / 2.0
+    probs = (np.arange(C) + 0.5) / C
+    centroids = 2.0 * special.betaincinv(m + 1.0, m + 1.0, probs) - 1.0
+    for _ in range(max_rounds):
         edges = 0.5 * (centroids[1:] + centroids[:-1])
-        cell = nearest_cell(x, edges)
-        new = np.empty(C)
-        for k in range(C):
-            member = cell == k
-            mass = dens[member].sum()
-            new[k] = (dens[member] * x[member]).sum() / mass
+        lo = np.concatenate(([-1.0], edges))
+        hi = np.concatenate((edges, [1.0]))
+        new = first(lo, hi) / mass(lo, hi)
+        moved = float(np.max(np.abs(new - centroids)))
         centroids = new
+        if moved <= tol * float(np.max(np.abs(centroids))):
+            break
+    else:
+        raise RuntimeError("Lloyd-Max rounds did not converge")
     edges = 0.5 * (centroids[1:] + centroids[:-1])
-    err = x - centroids[nearest_cell(x, edges)]
-    d_mse = d * float(np.sum(dens * err * err))
-    return centroids, edges, d_mse
+    lo = np.concatenate(([-1.0], edges))
+    hi = np.concatenate((edges, [1.0]))
+    err = second(lo, hi) - 2.0 * centroids * first(lo, hi) + centroids ** 2 * mass(lo, hi)
+    return centroids, edges, d * float(np.sum(err))
 
 
 # ---------------------------------------------------------------------------
 # Compressor: TurboQuant_prod on unit-norm keys
 # ---------------------------------------------------------------------------
-
-def f16_round(x: np.ndarray) -> np.ndarray:
-    """IEEE binary16 round-to-nearest-even of float64 values, returned as float64."""
-    return np.asarray(x, dtype=np.float64).astype(np.float16).astype(np.float64)
-
 
 def compress_prod(keys: np.ndarray, Pi: np.ndarray, S_mat: np.ndarray, codebook: np.ndarray,
                   gamma_dtype: str = "f32"):

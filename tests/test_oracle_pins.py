@@ -131,32 +131,48 @@ def test_codebook_gaussian_closed_forms():
 def test_one_bit_codebook_exact_closed_form():
     """1 bit: the cell edge is 0 and each centroid is E|x| = Gamma(d/2) / (sqrt(pi) Gamma((d+1)/2));
     the distortion is 1 - d c^2 because E[x^2] = 1/d on the sphere."""
-    for d in (16, 64, 128):
-        c, edges, dm = codebook(d, 1) if d == 128 else oracle.lloyd_max_sphere(d, 1, iters=60)
+    for d in (4, 16, 64, 128):
+        c, edges, dm = codebook(d, 1) if d == 128 else oracle.lloyd_max_sphere(d, 1)
         exact = math.exp(math.lgamma(d / 2) - math.lgamma((d + 1) / 2)) / math.sqrt(math.pi)
-        np.testing.assert_allclose([-c[0], c[1]], [exact, exact], rtol=1e-4)
-        # the grid point at exactly 0 joins the lower cell (left-sided search), so the
-        # edge can sit off 0 by at most about one grid step 2/(grid-1)
-        assert abs(edges[0]) < 2.0 / 400_000
-        assert dm == pytest.approx(1.0 - d * exact * exact, rel=2e-4)
+        np.testing.assert_allclose([-c[0], c[1]], [exact, exact], rtol=1e-12)
+        assert abs(edges[0]) < 1e-15
+        assert dm == pytest.approx(1.0 - d * exact * exact, rel=1e-10)
+
+
+def test_uniform_density_at_d3():
+    """d = 3 makes the coordinate uniform on [-1, 1] (Archimedes): the Lloyd-Max codebook is the
+    uniform quantizer, centroids -1 + (2k + 1)/C, and the distortion is 3 * (2/C)^2 / 12."""
+    for b in (1, 2, 3):
+        C = 1 << b
+        c, edges, dm = oracle.lloyd_max_sphere(3, b)
+        np.testing.assert_allclose(c, -1.0 + (2.0 * np.arange(C) + 1.0) / C, atol=1e-13)
+        np.testing.assert_allclose(edges, -1.0 + 2.0 * np.arange(1, C) / C, atol=1e-13)
+        assert dm == pytest.approx(3.0 * (2.0 / C) ** 2 / 12.0, rel=1e-12)
 
 
 def test_codebook_is_a_lloyd_fixed_point_under_quadrature():
-    """Each centroid is the conditional mean of its cell under the exact density, checked with
-    adaptive quadrature (scipy) instead of the grid the oracle sums over."""
+    """Each centroid is the conditional mean of its cell under the exact density and the
+    distortion is the integral of the squared error, both checked with adaptive quadrature
+    (scipy.integrate.quad) instead of the oracle's incomplete-beta moments."""
     integrate = pytest.importorskip("scipy.integrate")
-    d = 128
-    for b in (2, 3):
-        c, edges, _ = codebook(d, b)
-        f = lambda x: (1.0 - x * x) ** ((d - 3) / 2.0)
-        lims = [-1.0] + list(edges) + [1.0]
-        for k in range(len(c)):
-            mass = integrate.quad(f, lims[k], lims[k + 1], epsabs=0, epsrel=1e-12, limit=200)[0]
-            mom = integrate.quad(lambda x: x * f(x), lims[k], lims[k + 1], epsabs=0, epsrel=1e-12, limit=200)[0]
-            # 300 Lloyd rounds leave ~3e-5 relative; a wrong density exponent moves centroids ~1e-2
-            assert c[k] == pytest.approx(mom / mass, rel=1e-4)
-        # symmetry of a symmetric density: c_k = -c_{C-1-k}
-        np.testing.assert_allclose(c, -c[::-1], atol=1e-5)
+    for d in (16, 128):
+        for b in (2, 3, 4):
+            c, edges, dm = codebook(d, b) if d == 128 else oracle.lloyd_max_sphere(d, b)
+            f = lambda x: (1.0 - x * x) ** ((d - 3) / 2.0)
+            z = integrate.quad(f, -1.0, 1.0, epsabs=0, epsrel=1e-13, limit=200)[0]
+            lims = [-1.0] + list(edges) + [1.0]
+            sq = 0.0
+            for k in range(len(c)):
+                a, e = lims[k], lims[k + 1]
+                mass = integrate.quad(f, a, e, epsabs=0, epsrel=1e-13, limit=200)[0]
+                mom = integrate.quad(lambda x: x * f(x), a, e, epsabs=0, epsrel=1e-13, limit=200)[0]
+                sq += integrate.quad(lambda x: (x - c[k]) ** 2 * f(x), a, e, epsabs=0, epsrel=1e-13,
+                                     limit=200)[0]
+                # converged to the fixed point; a wrong density exponent moves centroids ~1e-2
+                assert c[k] == pytest.approx(mom / mass, rel=1e-9)
+            assert dm == pytest.approx(d * sq / z, rel=1e-8)
+            # symmetry of a symmetric density: c_k = -c_{C-1-k}
+            np.testing.assert_allclose(c, -c[::-1], atol=1e-13)
 
 
 # ---------------------------------------------------------------------------
@@ -194,7 +210,7 @@ def test_compressor_bruteforce_properties():
     keys /= np.linalg.norm(keys, axis=1, keepdims=True)
     Pi = oracle.haar_rotation(rng.standard_normal((D, D))).astype(np.float32)
     Smat = rng.standard_normal((D, D)).astype(np.float32)
-    cb = (oracle.lloyd_max_sphere(D, 2, iters=60)[0]).astype(np.float32)
+    cb = (oracle.lloyd_max_sphere(D, 2)[0]).astype(np.float32)
     idx, sg, gamma = oracle.compress_prod(keys, Pi, Smat, cb, "f32")
     P64, S64, c64 = Pi.astype(float), Smat.astype(float), cb.astype(float)
     for s in range(S):
@@ -510,3 +526,18 @@ def test_decode_special_cases():
     ones = np.ones(len(kn), dtype=np.float16)
     o1 = oracle.decode_mse(A, same, ones, kcb, vi, vn, vcb, Pv, 0.25)
     assert np.allclose(o1, np.broadcast_to(Vh.mean(axis=0), o1.shape), rtol=1e-12, atol=1e-12)
+
+
+def test_nearest_cell_is_a_left_sided_search():
+    """The cell rule equals NumPy's left-sided binary search over the sorted midpoints
+    (a value on a midpoint takes the lower cell), on random values and on the edges."""
+    rng = np.random.default_rng(5)
+    edges = np.sort(rng.standard_normal(7))
+    vals = np.concatenate([rng.standard_normal(500), edges, [-np.inf, np.inf]])
+    assert np.array_equal(oracle.nearest_cell(vals, edges), np.searchsorted(edges, vals, side="left"))
+
+
+def test_qjl_constant_is_the_half_normal_mean():
+    """sqrt(pi/2) = 1 / E|g| for g ~ N(0, 1), and E|g| = sqrt(2) / Gamma(1/2)."""
+    assert oracle.SQRT_HALF_PI == pytest.approx(math.gamma(0.5) / math.sqrt(2.0), rel=1e-15)
+    assert oracle.kappa(128) == pytest.approx(oracle.SQRT_HALF_PI / 128, rel=1e-15)

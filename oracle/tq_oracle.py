@@ -41,6 +41,7 @@ __all__ = [
     "scores_sampled",
     "scores_mse",
     "decode_mse",
+    "decode_prod",
     "pack_indices",
     "unpack_indices",
     "pack_signs",
@@ -352,6 +353,30 @@ def decode_mse(A: np.ndarray, k_idx: np.ndarray, k_norm: np.ndarray, k_codebook:
     s = scale * (A @ kc.T) * np.asarray(k_norm, dtype=np.float64)[np.newaxis, :]
     p = np.exp(s - s.max(axis=1, keepdims=True))
     p /= p.sum(axis=1, keepdims=True)
+    acc = (p * np.asarray(v_norm, dtype=np.float64)[np.newaxis, :]) @ vc
+    return acc @ np.asarray(Pi_v, dtype=np.float64)
+
+
+def decode_prod(A: np.ndarray, T: np.ndarray, k_idx: np.ndarray, k_signs: np.ndarray,
+                k_gamma: np.ndarray, k_codebook: np.ndarray, v_idx: np.ndarray, v_norm: np.ndarray,
+                v_codebook: np.ndarray, Pi_v: np.ndarray, scale: float) -> np.ndarray:
+    """Attention output over a TurboQuant_prod key cache and an MSE-quantized value cache
+    ([ZT] "The Optimization Journey", v2 kernel 3 and v6 "Fused hybrid Triton kernel":
+    per compressed block the TQ score, the value dequantization and the accumulation;
+    the score is the paper's <y, x_mse> + ||r|| sqrt(pi/2)/d <S y, qjl>, [ZT] "Relevance
+    to v6"):
+
+        s[b, i]  = scale * score[b, i]        (score: :func:`scores`, from A = Pi q, T = S_mat q)
+        p[b, :]  = softmax(s[b, :])           (max subtracted)
+        acc[b]   = sum_i p[b, i] v_norm[i] c_v[v_idx[i]]          (rotated value basis)
+        out[b]   = Pi_v^T acc[b]
+
+    Values as in :func:`decode_mse`.  float64 throughout.
+    """
+    s = scale * scores(A, T, k_idx, k_signs, k_gamma, k_codebook)
+    p = np.exp(s - s.max(axis=1, keepdims=True))
+    p /= p.sum(axis=1, keepdims=True)
+    vc = np.asarray(v_codebook, dtype=np.float64)[np.asarray(v_idx, dtype=np.int64)]
     acc = (p * np.asarray(v_norm, dtype=np.float64)[np.newaxis, :]) @ vc
     return acc @ np.asarray(Pi_v, dtype=np.float64)
 

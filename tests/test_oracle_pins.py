@@ -541,3 +541,74 @@ def test_qjl_constant_is_the_half_normal_mean():
     """sqrt(pi/2) = 1 / E|g| for g ~ N(0, 1), and E|g| = sqrt(2) / Gamma(1/2)."""
     assert oracle.SQRT_HALF_PI == pytest.approx(math.gamma(0.5) / math.sqrt(2.0), rel=1e-15)
     assert oracle.kappa(128) == pytest.approx(oracle.SQRT_HALF_PI / 128, rel=1e-15)
+
+
+def _prod_decode_case(n, D, seed, kbits=3, vbits=3):
+    """Unit keys compressed by TurboQuant_prod (b = kbits: (kbits-1)-bit codes + signs),
+    values by TurboQuant-MSE; two queries."""
+    rng = np.random.default_rng(seed)
+    K = rng.standard_normal((n, D))
+    K /= np.linalg.norm(K, axis=1, keepdims=True)
+    V = rng.standard_normal((n, D))
+    q = rng.standard_normal((2, D))
+    Pk = oracle.haar_rotation(rng.standard_normal((D, D))).astype(np.float32)
+    Sm = rng.standard_normal((D, D)).astype(np.float32)
+    Pv = oracle.haar_rotation(rng.standard_normal((D, D))).astype(np.float32)
+    kcb = codebook(D, kbits - 1)[0].astype(np.float32)
+    vcb = codebook(D, vbits)[0].astype(np.float32)
+    ki, ks, kg = oracle.compress_prod(K, Pk, Sm, kcb, "f16")
+    vi, vn = oracle.compress_mse(V, Pv, vcb)
+    return q, Pk, Sm, Pv, kcb, vcb, ki, ks, kg, vi, vn
+
+
+def _prod_reconstructions(D, Pk, Sm, Pv, kcb, vcb, ki, ks, kg, vi, vn):
+    """Keys and values rebuilt in the original basis, as the page's first version does
+    before any matrix product (zededa.com v1: unpack, centroids, rotate back; the QJL part
+    sqrt(pi/2)/d * gamma * S^T sigma, kanthi.in §3 TurboQuantProd.dequantize)."""
+    P = Pk.astype(np.float64)
+    Kh = kcb.astype(np.float64)[ki.astype(np.int64)] @ P
+    Kh += (math.sqrt(math.pi / 2) / D) * kg.astype(np.float64)[:, None] * (ks.astype(np.float64) @ Sm.astype(np.float64))
+    Vh = vn.astype(np.float64)[:, None] * (vcb.astype(np.float64)[vi.astype(np.int64)] @ Pv.astype(np.float64))
+    return Kh, Vh
+
+
+def test_prod_decode_equals_dequantize_everything():
+    """Attention over the product cache equals softmax(scale <q, k_hat>) weights on the
+    rebuilt values, with every key rebuilt in the original basis and scored from q itself
+    (no A, no T), one pair at a time."""
+    for D, n, kb, vb in ((8, 13, 3, 2), (32, 200, 3, 3), (16, 64, 4, 1)):
+        q, Pk, Sm, Pv, kcb, vcb, ki, ks, kg, vi, vn = _prod_decode_case(n, D, 71 + D, kb, vb)
+        A, T = oracle.prepare_queries(q, Pk, Sm)
+        got = oracle.decode_prod(A, T, ki, ks, kg, kcb, vi, vn, vcb, Pv, 1.0 / math.sqrt(D))
+        Kh, Vh = _prod_reconstructions(D, Pk, Sm, Pv, kcb, vcb, ki, ks, kg, vi, vn)
+        for b in range(q.shape[0]):
+            logits = [float(np.dot(Kh[i], q[b])) / math.sqrt(D) for i in range(n)]
+            m = max(logits)
+            w = [math.exp(x - m) for x in logits]
+            tot = sum(w)
+            want = sum(w[i] / tot * Vh[i] for i in range(n))
+            assert np.allclose(got[b], want, rtol=1e-11, atol=1e-12)
+
+
+def test_prod_decode_special_cases():
+    """One key: the output is that value's reconstruction.  A dominant key (its logit far
+    above every other) takes all the weight.  Equal logits (q = 0) weigh the values
+    equally: the output is the plain mean of the rebuilt values."""
+    D = 16
+    q, Pk, Sm, Pv, kcb, vcb, ki, ks, kg, vi, vn = _prod_decode_case(40, D, 81)
+    A, T = oracle.prepare_queries(q, Pk, Sm)
+    _, Vh = _prod_reconstructions(D, Pk, Sm, Pv, kcb, vcb, ki, ks, kg, vi, vn)
+    one = oracle.decode_prod(A, T, ki[:1], ks[:1], kg[:1], kcb, vi[:1], vn[:1], vcb, Pv, 0.25)
+    assert np.allclose(one, np.broadcast_to(Vh[0], one.shape), rtol=1e-12)
+    # the query along key 7's reconstruction, scaled up: its logit exceeds the rest by
+    # far more than log(n / eps)
+    Kh, _ = _prod_reconstructions(D, Pk, Sm, Pv, kcb, vcb, ki, ks, kg, vi, vn)
+    qd = 400.0 * Kh[7:8] / np.linalg.norm(Kh[7])
+    Ad, Td = oracle.prepare_queries(qd, Pk, Sm)
+    logits = (Kh @ qd[0])
+    assert logits[7] - np.delete(logits, 7).max() > 50.0
+    out = oracle.decode_prod(Ad, Td, ki, ks, kg, kcb, vi, vn, vcb, Pv, 1.0)
+    assert np.allclose(out[0], Vh[7], rtol=1e-12, atol=1e-12)
+    z = np.zeros_like(A)
+    o0 = oracle.decode_prod(z, z, ki, ks, kg, kcb, vi, vn, vcb, Pv, 0.25)
+    assert np.allclose(o0, np.broadcast_to(Vh.mean(axis=0), o0.shape), rtol=1e-12, atol=1e-12)

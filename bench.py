@@ -1,8 +1,9 @@
 #!/usr/bin/env python
 """Throughput of the TurboQuant_prod score path (query transform + scoring) on GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--config c1] [--path auto]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config c2] [--path auto]
     python bench.py --impl reference ...      # the CPU oracle on the host cores
+    python bench.py --config c2 --s-sweep 32768,131072,524288,2097152   # fixed + per-key fit
 
 One step = one pass of the whole hot path over one workload through the fused
 public entry (tq_solve / tq_solve_packed): the query transform A = Pi q,
@@ -11,9 +12,12 @@ cache.  Inputs are synthetic (the ``synth`` draws), compressed on the GPU by
 libtq's own compressor before timing starts; nothing on the timed path touches
 the CPU oracle.  Prints one JSON line (rank 0).
 
+The default workload is c2, single-query decode over 131072 bit-packed 3-bit keys.
+
 Timing: the timed region replays CUDA graphs that hold 8 consecutive steps each
 (one graph per step for a remainder), exactly K steps, bracketed by CUDA events
-on the launching stream.  Steps rotate over enough independent input/output
+on the launching stream; the region is repeated (at least 5 times and for at least
+half a second, so the clock sampler sees it) and the median repeat is reported.  Steps rotate over enough independent input/output
 copies that their union is more than twice the L2, so every step reads its
 cache from HBM.  The roofline's kernel time is the mean of back-to-back
 launches of the dominant kernel (the scoring kernel, or the single fused
@@ -64,11 +68,15 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", choices=sorted(synth.WORKLOADS), default="c1")
+    ap.add_argument("--config", choices=sorted(synth.WORKLOADS), default="c2")
     ap.add_argument("--path", choices=["auto", "fp32", "bf16_mma"], default="auto")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="approximate CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--oracle-one-core", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--s-sweep", default="",
+                    help="comma-separated key counts: time the step of this workload at each S "
+                         "(keys tiled from the workload's own cache) and fit fixed + S x per-key")
     return ap.parse_args()
 
 
@@ -351,6 +359,27 @@ def time_oracle(w, seconds, n_keys=None):
                       f"{el:.1f} s, float64 NumPy (BLAS threads = host cores)"}
 
 
+def time_oracle_one_core(config, seconds):
+    """The same oracle timing in a child process pinned to one core with one BLAS thread
+    (the variables must be set before NumPy loads its BLAS).  Returns scores/s or None."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               BLIS_NUM_THREADS="1", VECLIB_MAXIMUM_THREADS="1", NUMEXPR_NUM_THREADS="1")
+    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-one-core", "--config", config,
+           "--cpu-seconds", str(seconds)]
+    try:
+        res = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=10 * seconds + 120)
+        return json.loads(res.stdout.strip().splitlines()[-1])["value"]
+    except (subprocess.SubprocessError, ValueError, IndexError, KeyError):
+        return None
+
+
+def oracle_one_core_child(args, w):
+    if hasattr(os, "sched_setaffinity"):
+        cpu = min(os.sched_getaffinity(0))
+        os.sched_setaffinity(0, {cpu})
+    print(json.dumps(time_oracle(w, args.cpu_seconds)), flush=True)
+
+
 def run_reference(args, w):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -379,12 +408,92 @@ def run_reference(args, w):
 
 
 # ---------------------------------------------------------------------------
+# S-sweep: the per-call time of one workload as the cache grows
+# ---------------------------------------------------------------------------
+
+def run_s_sweep(args, w, tq, torch, dev, path):
+    """Times one step (the fused public entry) of workload `w` at each S of --s-sweep and
+    fits t(S) = fixed + S * per_key by least squares.  The cache at each S repeats the
+    workload's own compressed keys; every launch reads its inputs from HBM (rotating
+    copies larger than twice the L2).  Prints one JSON line."""
+    Q0, Pi, S_mat, cb, cache0 = build_device_workload(w, tq, torch, dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    stream = torch.cuda.Stream(dev)
+    rows = []
+    for S in [int(x) for x in args.s_sweep.split(",") if x]:
+        reps_ = -(-S // w.S)
+        cache = {k: v.repeat_interleave(1, dim=0).repeat(*([1, reps_] + [1] * (v.dim() - 2)))[:, :S].contiguous()
+                 for k, v in cache0.items()}
+        ws = dataclasses_replace(w, S=S)
+        per_copy = score_kernel_bytes(ws)
+        R = max(2, min(64, math.ceil(2.2 * l2 / per_copy)))
+        copies = [{"cache": {k: v.clone() for k, v in cache.items()}, "Q": Q0.clone(),
+                   "out": torch.empty((w.P, w.B, S), device=dev),
+                   "ws": torch.empty(tq.workspace_bytes(w.P, w.B, w.D), dtype=torch.uint8, device=dev)}
+                  for _ in range(R)]
+        del cache
+
+        def call(cp):
+            c = cp["cache"]
+            if w.layout == "unpacked":
+                tq.solve(cp["Q"], c["idx"], c["signs"], c["gamma"], Pi, S_mat, cb, path=path,
+                         workspace=cp["ws"], out=cp["out"])
+            else:
+                tq.solve_packed(cp["Q"], c["idx"], c["signs"], c["gamma"], Pi, S_mat, cb, w.mse_bits,
+                                path=path, workspace=cp["ws"], out=cp["out"])
+        with torch.cuda.stream(stream):
+            for cp in copies:
+                call(cp)
+        torch.cuda.synchronize(dev)
+        n = max(R, 32)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for k in range(n):
+                call(copies[k % R])
+        times = []
+        for _ in range(6):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                e0.record()
+                g.replay()
+                e1.record()
+            torch.cuda.synchronize(dev)
+            times.append(e0.elapsed_time(e1) / n)
+        ms = statistics.median(times[1:])
+        nbytes = score_kernel_bytes(ws) + fused_kernel_extra_bytes(ws)
+        rows.append({"S": S, "ms_per_call": ms, "bytes": nbytes, "gbs": nbytes / (ms / 1e3) / 1e9,
+                     "copies": R})
+        del copies, g
+        torch.cuda.empty_cache()
+    xs = np.array([r["S"] for r in rows], dtype=np.float64)
+    ys = np.array([r["ms_per_call"] for r in rows], dtype=np.float64)
+    fit = None
+    if len(rows) >= 2:
+        slope, icpt = np.polyfit(xs, ys, 1)
+        per_key_bytes = key_bytes(w) + 4 * w.B
+        fit = {"fixed_us": icpt * 1e3, "per_key_ns": slope * 1e6,
+               "streaming_gbs": per_key_bytes / (slope * 1e-3) / 1e9 if slope > 0 else None}
+    peak, _ = hbm_peak()
+    for r in rows:
+        r["frac"] = r["gbs"] / peak
+    print(json.dumps({"sweep": w.name, "path": path, "peak_gbs": peak, "rows": rows, "fit": fit}), flush=True)
+
+
+def dataclasses_replace(w, **kw):
+    import dataclasses
+    return dataclasses.replace(w, **kw)
+
+
+# ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
 
 def main():
     args = parse_args()
     w = synth.WORKLOADS[args.config]
+    if args.oracle_one_core:
+        oracle_one_core_child(args, w)
+        return
     if args.impl == "reference":
         run_reference(args, w)
         return
@@ -407,6 +516,9 @@ def main():
 
     tq.lib()
     path = args.path if args.path != "auto" else tq.auto_path(w.B, w.D)
+    if args.s_sweep:
+        run_s_sweep(args, w, tq, torch, dev, path)
+        return
     Q0, Pi, S_mat, cb, cache0 = build_device_workload(w, tq, torch, dev)
 
     # rotating copies: their union exceeds twice the L2 so that every step reads HBM;
@@ -473,24 +585,34 @@ def main():
     if dist:
         dist.barrier()
     torch.cuda.synchronize(dev)
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    def timed_region():
+        """Exactly K steps on the launching stream between two CUDA events (ms)."""
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            start.record()
+            k = 0
+            while k < args.steps:                 # exactly K steps; step k uses copy k mod R
+                if k % nG == 0 and k + nG <= args.steps:
+                    chunk[(k % R) // nG].replay()
+                    k += nG
+                else:
+                    single[k % R].replay()
+                    k += 1
+            end.record()
+        torch.cuda.synchronize(dev)
+        return start.elapsed_time(end)
+
+    # The K-step region is repeated (at least 5 times and for at least half a second, so
+    # that the clock sampler sees it) and the median repeat is reported.
     t_wall0 = time.time()
-    with torch.cuda.stream(stream):
-        start.record()
-        k = 0
-        while k < args.steps:                 # exactly K steps; step k uses copy k mod R
-            if k % nG == 0 and k + nG <= args.steps:
-                chunk[(k % R) // nG].replay()
-                k += nG
-            else:
-                single[k % R].replay()
-                k += 1
-        end.record()
-    torch.cuda.synchronize(dev)
+    regions = [timed_region()]
+    n_rep = int(min(500, max(5, math.ceil(500.0 / max(regions[0], 1e-3)))))
+    while len(regions) < n_rep:
+        regions.append(timed_region())
     t_wall1 = time.time()
     if dist:
         dist.barrier()
-    elapsed_ms = max_over_ranks(start.elapsed_time(end), dist, dev)
+    elapsed_ms = max_over_ranks(statistics.median(regions), dist, dev)
     clk = clocks.stop((t_wall0, t_wall1))
 
     # Dominant-kernel duration: the mean of back-to-back launches in one graph over the
@@ -521,6 +643,31 @@ def main():
     kernel_ms = ks.elapsed_time(ke) / (3 * reps)
     ktiming = (f"mean of {3 * reps} back-to-back launches in one graph over the {R} rotating copies "
                f"(CUDA events on the launching stream)")
+
+    def graph_ms(fn):
+        """Mean time of one call of fn(copy) over back-to-back launches in one graph."""
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for k in range(reps):
+                fn(copies[k % R])
+        with torch.cuda.stream(stream):
+            g.replay()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record()
+            for _ in range(3):
+                g.replay()
+            e1.record()
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / (3 * reps)
+
+    # the query transform alone, the scoring alone (from precomputed A and T) and the
+    # fused call, each as back-to-back launches over the rotating copies
+    split_ms = {"prepare_ms": graph_ms(lambda cp: tq.prepare_queries(cp["Q"], Pi, S_mat, out=(cp["A"], cp["T"]))),
+                "score_only_ms": graph_ms(lambda cp: score_call(tq, w, path, cp["A"], cp["T"], cp["cache"], cb,
+                                                                cp["out"])),
+                "fused_ms": graph_ms(solve_call)}
 
     scores_per_step = w.P * w.B * w.S
     value = world * scores_per_step * args.steps / (elapsed_ms / 1e3)
@@ -607,6 +754,9 @@ def main():
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = time_oracle(w, args.cpu_seconds)
+        cpu["hardware_concurrency"] = os.cpu_count()
+        cpu["value_1core"] = time_oracle_one_core(args.config, max(2.0, args.cpu_seconds / 3))
+        cpu["sample"] += "; value_1core: the same sample on one pinned core, one BLAS thread"
 
     if dist:
         dist.barrier()
@@ -632,6 +782,9 @@ def main():
                      "kernel_ms": kernel_ms, "bytes_per_launch": kbytes,
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback 6.8 TB/s",
                      "timing": ktiming, "kernel_fingerprint": fp},
+        "split_ms": split_ms,
+        "timed_region": {"repeats": len(regions), "median_ms": statistics.median(regions),
+                         "min_ms": min(regions), "max_ms": max(regions)},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": (1 if fused_single else (3 if w.layout == "decode" else 2)) * args.steps,

@@ -127,6 +127,18 @@ const char* tq_status_string(tq_status status) {
   return "unknown tq_status";
 }
 
+tq_status tq_device_faults(unsigned int* bits) {
+  if (bits == nullptr) return TQ_ERR_INVALID_VALUE;
+  unsigned int v = 0;
+  cudaError_t e = tq::take_faults_simt(&v);
+  if (e == cudaSuccess) e = tq::take_faults_mma(&v);
+  if (e == cudaSuccess) e = tq::take_faults_decode(&v);
+  if (e == cudaSuccess) e = tq::take_faults_compress(&v);
+  if (e != cudaSuccess) return TQ_ERR_LAUNCH;
+  *bits |= v;
+  return TQ_OK;
+}
+
 tq_path tq_auto_path(int B, int D) {
   return (B >= 16 && D == 128 && tq::mma_path_available()) ? TQ_PATH_BF16_MMA : TQ_PATH_FP32;
 }
@@ -282,6 +294,28 @@ tq_status tq_decode_mse(const float* A, const uint8_t* k_plane, const uint16_t* 
   return from_cuda(tq::launch_decode_mse(A, k_plane, k_norm, k_codebook, k_bits, v_plane, v_norm,
                                          v_codebook, v_bits, Pi_v, out, static_cast<float*>(workspace),
                                          P, H, B, S, scale, stream));
+}
+
+tq_status tq_decode_prod(const float* A, const float* T, const uint8_t* k_plane,
+                         const uint8_t* k_sign_plane, const uint16_t* k_gamma,
+                         const float* k_codebook, int k_bits, const uint8_t* v_plane,
+                         const uint16_t* v_norm, const float* v_codebook, int v_bits,
+                         const float* Pi_v, float* out, int P, int H, int B, int S, int D,
+                         float scale, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  tq_status st = check_ptrs(A, T, k_plane, k_sign_plane, k_gamma, k_codebook, v_plane, v_norm, v_codebook,
+                            Pi_v, out);
+  if (st != TQ_OK) return st;
+  if (P < 1 || H < 1 || H > P || B < 1 || S < 1 || D < 1) return TQ_ERR_INVALID_VALUE;
+  if (P > kMaxGridYZ || B > kMaxGridYZ || S > INT_MAX - 4096) return TQ_ERR_INVALID_VALUE;
+  if (k_bits < 1 || k_bits > 3 || v_bits < 1 || v_bits > 3 || !std::isfinite(scale))
+    return TQ_ERR_INVALID_VALUE;
+  if (D != 128) return TQ_ERR_UNSUPPORTED;
+  if (workspace == nullptr) return TQ_ERR_WORKSPACE;
+  if (misaligned(workspace)) return TQ_ERR_MISALIGNED;
+  if (workspace_bytes < tq_decode_workspace_bytes(P, B, S, D)) return TQ_ERR_WORKSPACE;
+  return from_cuda(tq::launch_decode_prod(A, T, k_plane, k_sign_plane, k_gamma, k_codebook, k_bits, v_plane,
+                                          v_norm, v_codebook, v_bits, Pi_v, out,
+                                          static_cast<float*>(workspace), P, H, B, S, scale, stream));
 }
 
 tq_status tq_pack_indices(const uint8_t* K_idx, uint8_t* idx_plane, int64_t n_keys, int D,

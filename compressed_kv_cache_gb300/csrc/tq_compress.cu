@@ -216,3 +216,7 @@ tq_status tq_haar_rotation(const double* G, int D, float* Pi) {
 }
 
 }  // extern "C"
+
+namespace tq {
+cudaError_t take_faults_compress(unsigned int* bits) { return take_unit_faults(bits); }
+}  // namespace tq

@@ -1,23 +1,28 @@
-// Fused decode over an MSE-quantized key and value cache, in the rotated domain
-// ("TurboQuant: Rotate-then-Quantize KV Caches at 3 Bits", kanthi.in, §8 "Kernel
-// view: never un-rotate a key", the kernel form of tq_rotated_domain):
+// Fused decode in the rotated domain ("TurboQuant: Rotate-then-Quantize KV Caches at
+// 3 Bits", kanthi.in, §8 "Kernel view: never un-rotate a key", the kernel form of
+// tq_rotated_domain), over an MSE-quantized or a TurboQuant_prod key cache and an
+// MSE-quantized value cache:
 //
-//   s[b,i]  = scale * nk_i * <A_b, ck[kidx_i]>          A_b = Pi_k q_b (rotated query)
+//   s[b,i]  = scale * nk_i * <A_b, ck[kidx_i]>                      MSE keys
+//   s[b,i]  = scale * (<A_b, ck[kidx_i]> + kappa g_i <T_b, sigma_i>)  product keys
+//             (A_b = Pi_k q_b, T_b = S_mat q_b; "Implementing TurboQuant on NVIDIA's
+//             AGX Thor", zededa.com, v2 kernel 3 and v6 fused hybrid kernel: TQ score,
+//             value dequant, accumulate)
 //   p[b,:]  = softmax(s[b,:])
 //   acc[b]  = sum_i p[b,i] nv_i cv[vidx_i]              accumulated in the rotated basis
 //   out[b]  = Pi_v^T acc[b]                             one inverse rotation per query
 //
 // Split-KV (flash decoding): decode_split_kernel takes one chunk of keys and one tile
-// of QB queries of a problem.  Each of its 8 warps owns a contiguous run of the chunk's
-// keys and starts the asynchronous copies of their key and value rows into shared
-// memory, 32 keys to a copy group.  The CTA builds the key lookup tables of the MSE
-// scorer from the rotated queries meanwhile.  Then every warp runs an online softmax
-// over its groups as they land: logits (lane per key), the group maximum, the rescale
-// of the running sum and accumulator by exp(old max - new max), and the weighted value
-// centroids (warp per key, lane l owning coordinates 4l .. 4l+3).  The 8 warps merge
-// in shared memory and write (max, sum, acc[128]) per (query, chunk) to the workspace.
-// decode_combine_kernel merges the chunks of a query with the same rescaling and
-// applies Pi_v^T.  D = 128, 1-3 bit codes.
+// of QB queries of a problem.  Each of its 16 warps owns a contiguous run of the
+// chunk's keys and starts the asynchronous copies of their key rows (and sign rows)
+// and value rows into shared memory, 32 keys to a copy group.  The CTA builds the key
+// lookup tables (code tables from A, sign tables from T) meanwhile.  Then every warp
+// runs an online softmax over its groups as they land: logits (lane per key), the
+// group maximum, the rescale of the running sum and accumulator by exp(old max - new
+// max), and the weighted value centroids.  The warps merge in shared memory and write
+// (max, sum, acc[128]) per (query, chunk) to the workspace.  decode_combine_kernel
+// merges the chunks of a query with the same rescaling and applies Pi_v^T.  D = 128,
+// 1-3 bit codes.
 #include <atomic>
 
 #include "tq_internal.cuh"
@@ -55,19 +60,8 @@ __device__ __forceinline__ void expect_bytes(uint32_t bar, uint32_t bytes) {
                "r"(bytes)
                : "memory");
 }
-// Bounded wait for phase 0 of a local mbarrier (about a second at most); false if it
-// gave up.
-__device__ __forceinline__ bool wait_phase0(uint32_t bar) {
-  for (uint32_t it = 0; it < (1u << 22); ++it) {
-    uint32_t ok;
-    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-                 : "=r"(ok)
-                 : "r"(bar)
-                 : "memory");
-    if (ok) return true;
-  }
-  return false;
-}
+// Bounded wait for phase 0 of a local mbarrier (kWaitBudgetNs); false if it gave up.
+__device__ __forceinline__ bool wait_phase0(uint32_t bar) { return wait_parity_bounded(bar, 0, kFaultDecode); }
 
 // Shared memory: key rows [chunk][16 KBITS B] | value rows [chunk][16 VBITS B] |
 // copy barriers [warps][steps] | lut [QB][NPI*NV] | rotated queries [QB][128] |
@@ -76,32 +70,56 @@ constexpr int kDecWarps = kDecThreads / 32;
 constexpr int kStep = 32;                                  // keys per warp step (lane per key)
 constexpr int kMaxSteps = kMaxChunk / kDecWarps / kStep;   // warp steps, at most
 
-template <int KBITS, int VBITS, int QB>
-constexpr size_t split_smem_bytes(int chunk) {
-  return static_cast<size_t>(chunk) * 16 * (KBITS + VBITS) + 8 * kDecWarps * kMaxSteps +
-         sizeof(float) * (static_cast<size_t>(QB) * LutShape<KBITS>::NPI * LutShape<KBITS>::NV +
-                          static_cast<size_t>(QB) * kD + static_cast<size_t>(kDecWarps) * QB * (kD + 2) + 8);
+// Arguments of one split launch (PROD: product keys with sign rows and gamma).
+struct SplitArgs {
+  const float* A;                 // [P,B,128] rotated queries
+  const float* T;                 // [P,B,128] projected queries (product keys only)
+  const uint8_t* k_plane;         // [P,S,16 KBITS] key codes
+  const uint8_t* k_sign;          // [P,S,16] key sign rows (product keys only)
+  const uint16_t* k_scale;        // [P,S] fp16: key norms (MSE keys) or residual norms gamma
+  const float* k_cb;
+  const uint8_t* v_plane;
+  const uint16_t* v_norm;
+  const float* v_cb;
+  float* part;
+  int B, S, chunk, nchunks;
+  float scale, kappa;
+};
+
+template <int KBITS, bool PROD>
+__host__ __device__ constexpr int key_tab_floats() {
+  return LutShape<KBITS>::NPI * LutShape<KBITS>::NV + (PROD ? LutShape<KBITS>::NPS * 16 : 0);
 }
 
-template <int KBITS, int VBITS, int QB>
+template <int KBITS, int VBITS, int QB, bool PROD>
+constexpr size_t split_smem_bytes(int chunk) {
+  return static_cast<size_t>(chunk) * 16 * (KBITS + VBITS + (PROD ? 1 : 0)) + 8 * kDecWarps * kMaxSteps +
+         sizeof(float) * (static_cast<size_t>(QB) * key_tab_floats<KBITS, PROD>() +
+                          static_cast<size_t>(QB) * kD * (PROD ? 2 : 1) +
+                          static_cast<size_t>(kDecWarps) * QB * (kD + 2) + 8);
+}
+
+template <int KBITS, int VBITS, int QB, bool PROD>
 __global__ void __launch_bounds__(kDecThreads)
-decode_split_kernel(const float* __restrict__ A, const uint8_t* __restrict__ k_plane,
-                    const uint16_t* __restrict__ k_norm, const float* __restrict__ k_cb,
-                    const uint8_t* __restrict__ v_plane, const uint16_t* __restrict__ v_norm,
-                    const float* __restrict__ v_cb, float* __restrict__ part, int B, int S,
-                    int chunk, int nchunks, float scale) {
+decode_split_kernel(const SplitArgs args) {
   using L = LutShape<KBITS>;
   constexpr int kW = kDecWarps;
   constexpr int kKRow = 16 * KBITS, kVRow = 16 * VBITS;   // bytes of one key / value row
+  constexpr int kSRow = PROD ? 16 : 0;                    // bytes of one sign row
+  constexpr int kTab = key_tab_floats<KBITS, PROD>();     // table floats per query
+  constexpr int kQ = PROD ? 2 * kD : kD;                  // query-side floats per query (A, T)
   constexpr int kBlk = kStep;
   constexpr int kMaxBlk = kMaxSteps;
+  const int B = args.B, S = args.S, chunk = args.chunk, nchunks = args.nchunks;
+  const float scale = args.scale;
   extern __shared__ __align__(16) uint8_t smem_raw[];
   uint8_t* kst = smem_raw;
-  uint8_t* vst = kst + static_cast<size_t>(chunk) * kKRow;
+  uint8_t* sst = kst + static_cast<size_t>(chunk) * kKRow;
+  uint8_t* vst = sst + static_cast<size_t>(chunk) * kSRow;
   uint64_t* bars = reinterpret_cast<uint64_t*>(vst + static_cast<size_t>(chunk) * kVRow);
   float* lut = reinterpret_cast<float*>(bars + kW * kMaxBlk);
-  float* sA = lut + QB * L::NPI * L::NV;
-  float* racc = sA + QB * kD;
+  float* sA = lut + QB * kTab;                            // [QB][A | T]
+  float* racc = sA + QB * kQ;
   float* rmax = racc + kW * QB * kD;
   float* rsum = rmax + kW * QB;
   float* vtab = rsum + kW * QB;
@@ -115,16 +133,17 @@ decode_split_kernel(const float* __restrict__ A, const uint8_t* __restrict__ k_p
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   // rotated queries into registers first (stored once the copies are under way)
-  constexpr int kAPer = (QB * kD + kDecThreads - 1) / kDecThreads;
+  constexpr int kAPer = (QB * kQ + kDecThreads - 1) / kDecThreads;
   float av[kAPer];
 #pragma unroll
   for (int j = 0; j < kAPer; ++j) {
-    const int e = tid + j * kDecThreads, q = e / kD;
-    av[j] = e < QB * kD && b0 + q < B ? __ldg(A + (static_cast<size_t>(p) * B + b0 + q) * kD + (e % kD)) : 0.f;
+    const int e = tid + j * kDecThreads, q = e / kQ, x = e % kQ;
+    const size_t row = (static_cast<size_t>(p) * B + b0 + q) * kD;
+    av[j] = e < QB * kQ && b0 + q < B ? (x < kD ? __ldg(args.A + row + x) : __ldg(args.T + row + x - kD)) : 0.f;
   }
-  const float vt = tid < (1 << VBITS) ? __ldg(v_cb + tid) : 0.f;
+  const float vt = tid < (1 << VBITS) ? __ldg(args.v_cb + tid) : 0.f;
   float cv[L::G];
-  table_centroids<KBITS>(k_cb, cv);
+  table_centroids<KBITS>(args.k_cb, cv);
 
   // this warp's keys [w0, w1) of the chunk, in steps of 32: per step one bulk copy of
   // the key rows and one of the value rows, both completing on the step's barrier
@@ -139,41 +158,58 @@ decode_split_kernel(const float* __restrict__ A, const uint8_t* __restrict__ k_p
     for (int t = 0; t < nsteps; ++t) {
       const int r0 = w0 + t * kBlk, rows = min(kBlk, w1 - r0);
       const uint32_t bar = bar0 + 8 * t;
-      expect_bytes(bar, static_cast<uint32_t>(rows * (kKRow + kVRow)));
-      bulk_copy(kst + static_cast<size_t>(r0) * kKRow, k_plane + (kbase + r0) * kKRow,
+      expect_bytes(bar, static_cast<uint32_t>(rows * (kKRow + kSRow + kVRow)));
+      bulk_copy(kst + static_cast<size_t>(r0) * kKRow, args.k_plane + (kbase + r0) * kKRow,
                 static_cast<uint32_t>(rows * kKRow), bar);
-      bulk_copy(vst + static_cast<size_t>(r0) * kVRow, v_plane + (kbase + r0) * kVRow,
+      if constexpr (PROD)
+        bulk_copy(sst + static_cast<size_t>(r0) * kSRow, args.k_sign + (kbase + r0) * kSRow,
+                  static_cast<uint32_t>(rows * kSRow), bar);
+      bulk_copy(vst + static_cast<size_t>(r0) * kVRow, args.v_plane + (kbase + r0) * kVRow,
                 static_cast<uint32_t>(rows * kVRow), bar);
     }
   }
   __syncwarp();
-  // norms of this lane's keys w0 + 32 t + lane
+  // key norms (MSE keys) or residual norms (product keys) and value norms of this
+  // lane's keys w0 + 32 t + lane
   float nk[kMaxBlk], nv[kMaxBlk];
 #pragma unroll
   for (int t = 0; t < kMaxBlk; ++t) {
     const int i = w0 + t * kBlk + lane;
-    nk[t] = i < w1 ? __half2float(__ushort_as_half(__ldg(k_norm + kbase + i))) : 0.f;
-    nv[t] = i < w1 ? __half2float(__ushort_as_half(__ldg(v_norm + kbase + i))) : 0.f;
+    nk[t] = i < w1 ? __half2float(__ushort_as_half(__ldg(args.k_scale + kbase + i))) : 0.f;
+    nv[t] = i < w1 ? __half2float(__ushort_as_half(__ldg(args.v_norm + kbase + i))) : 0.f;
   }
 
 #pragma unroll
   for (int j = 0; j < kAPer; ++j) {
     const int e = tid + j * kDecThreads;
-    if (e < QB * kD) sA[e] = av[j];
+    if (e < QB * kQ) sA[e] = av[j];
   }
   if (tid < (1 << VBITS)) vtab[tid] = vt;
-  // key tables of the query tile (rows past B give zero tables)
+  // key tables of the query tile (rows past B give zero tables): code tables from A,
+  // then (product keys) 32 sign tables of 4 signs each from T
   __syncthreads();
   {
     const int v = tid % L::NV;
     for (int q = 0; q < QB; ++q) {
-      const float* a = sA + q * kD;
-      float* tq = lut + q * L::NPI * L::NV;
+      const float* a = sA + q * kQ;
+      float* tq = lut + q * kTab;
       for (int g = tid / L::NV; g < L::NPI; g += kDecThreads / L::NV) {
         float acc = 0.f;
 #pragma unroll
         for (int k = 0; k < L::G; ++k) acc = fmaf(a[g * L::G + k], cv[k], acc);
         tq[g * L::NV + v] = acc;
+      }
+      if constexpr (PROD) {
+        const int vs = tid & 15;
+        for (int g = tid >> 4; g < L::NPS; g += kDecThreads / 16) {
+          float acc = 0.f;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float t = a[kD + 4 * g + i];
+            acc += ((vs >> i) & 1) ? t : -t;
+          }
+          tq[L::NPI * L::NV + g * 16 + vs] = acc;
+        }
       }
     }
   }
@@ -229,10 +265,26 @@ decode_split_kernel(const float* __restrict__ A, const uint8_t* __restrict__ k_p
           const uint32_t val = (sh + L::KB <= 32) ? (wd[wi] >> sh) & (L::NV - 1)
                                                   : __funnelshift_r(wd[wi], wd[wi + 1], sh) & (L::NV - 1);
 #pragma unroll
-          for (int q = 0; q < QB; ++q) m[gi & 1][q] += lut[(q * L::NPI + gi) * L::NV + val];
+          for (int q = 0; q < QB; ++q) m[gi & 1][q] += lut[q * kTab + gi * L::NV + val];
         }
+        if constexpr (PROD) {
+          // the sign row: 32 lookups of 4 signs each, then score = mse + kappa g res
+          const uint4 sr = *reinterpret_cast<const uint4*>(sst + static_cast<size_t>(i) * kSRow);
+          unsigned long long r2[QB][2];
 #pragma unroll
-        for (int q = 0; q < QB; ++q) sc[q] = scale * nk[t] * (m[0][q] + m[1][q]);
+          for (int q = 0; q < QB; ++q) r2[q][0] = r2[q][1] = 0ull;
+          lut_nibbles<QB, kTab>(lut + L::NPI * L::NV, sr.x, 0, r2);
+          lut_nibbles<QB, kTab>(lut + L::NPI * L::NV, sr.y, 8, r2);
+          lut_nibbles<QB, kTab>(lut + L::NPI * L::NV, sr.z, 16, r2);
+          lut_nibbles<QB, kTab>(lut + L::NPI * L::NV, sr.w, 24, r2);
+          const float kg = args.kappa * nk[t];
+#pragma unroll
+          for (int q = 0; q < QB; ++q)
+            sc[q] = scale * fmaf(kg, sum2(r2[q][0]) + sum2(r2[q][1]), m[0][q] + m[1][q]);
+        } else {
+#pragma unroll
+          for (int q = 0; q < QB; ++q) sc[q] = scale * nk[t] * (m[0][q] + m[1][q]);
+        }
       }
       float w[QB];
 #pragma unroll
@@ -311,7 +363,7 @@ decode_split_kernel(const float* __restrict__ A, const uint8_t* __restrict__ k_p
       s = fmaf(racc[(w * QB + q) * kD + d], f, s);
       ls = fmaf(rsum[w * QB + q], f, ls);
     }
-    float* pp = part + ((static_cast<size_t>(p) * B + b0 + q) * nchunks + c) * kPart;
+    float* pp = args.part + ((static_cast<size_t>(p) * B + b0 + q) * nchunks + c) * kPart;
     pp[kAcc + d] = s;
     if (d == 0) {
       pp[0] = mx;
@@ -415,12 +467,9 @@ decode_combine_kernel(const float* __restrict__ part, const float* __restrict__ 
   }
 }
 
-template <int KBITS, int VBITS, int QB>
-cudaError_t launch_decode_qb(const float* A, const uint8_t* k_plane, const uint16_t* k_norm,
-                             const float* k_cb, const uint8_t* v_plane, const uint16_t* v_norm,
-                             const float* v_cb, const float* Pi_v, float* out, float* part, int P,
-                             int H, int B, int S, float scale, cudaStream_t st) {
-  auto kernel = decode_split_kernel<KBITS, VBITS, QB>;
+template <int KBITS, int VBITS, int QB, bool PROD>
+cudaError_t launch_decode_qb(SplitArgs a, const float* Pi_v, float* out, int P, int H, cudaStream_t st) {
+  auto kernel = decode_split_kernel<KBITS, VBITS, QB, PROD>;
   static std::atomic<int> sms_cache[64];
   static std::atomic<uint64_t> configured{0};
   int dev = 0;
@@ -435,7 +484,7 @@ cudaError_t launch_decode_qb(const float* A, const uint8_t* k_plane, const uint1
   const uint64_t bit = 1ull << (dev & 63);
   if (!(configured.load(std::memory_order_acquire) & bit)) {
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(split_smem_bytes<KBITS, VBITS, QB>(kMaxChunk)));
+                             static_cast<int>(split_smem_bytes<KBITS, VBITS, QB, PROD>(kMaxChunk)));
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return e;
@@ -446,16 +495,17 @@ cudaError_t launch_decode_qb(const float* A, const uint8_t* k_plane, const uint1
   if (e != cudaSuccess) return e;
   // chunks of 256..1024 keys, as many as give every SM one CTA (equal chunks, so that
   // no SM gets more keys than another)
+  const int B = a.B, S = a.S;
   const int qtiles = ceil_div(B, QB);
   const int64_t units = static_cast<int64_t>(P) * qtiles;
   const int64_t per_unit = (static_cast<int64_t>(sms) + units - 1) / units;
   int chunk = ceil_div(S, per_unit < 1 ? 1 : per_unit);
   chunk = chunk < 256 ? 256 : (chunk > kMaxChunk ? kMaxChunk : chunk);
-  const int nchunks = ceil_div(S, chunk);
-  const size_t smem = split_smem_bytes<KBITS, VBITS, QB>(chunk);
-  dim3 grid(nchunks, qtiles, P);
-  kernel<<<grid, kDecThreads, smem, st>>>(A, k_plane, k_norm, k_cb, v_plane, v_norm, v_cb, part, B, S,
-                                          chunk, nchunks, scale);
+  a.chunk = chunk;
+  a.nchunks = ceil_div(S, chunk);
+  const size_t smem = split_smem_bytes<KBITS, VBITS, QB, PROD>(chunk);
+  dim3 grid(a.nchunks, qtiles, P);
+  kernel<<<grid, kDecThreads, smem, st>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -467,32 +517,37 @@ cudaError_t launch_decode_qb(const float* A, const uint8_t* k_plane, const uint1
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, decode_combine_kernel, static_cast<const float*>(part), Pi_v, out, H, B,
-                         nchunks);
+  e = cudaLaunchKernelEx(&cfg, decode_combine_kernel, static_cast<const float*>(a.part), Pi_v, out, H, B,
+                         a.nchunks);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
-template <int KBITS, int VBITS>
-cudaError_t launch_decode_kv(const float* A, const uint8_t* k_plane, const uint16_t* k_norm,
-                             const float* k_cb, const uint8_t* v_plane, const uint16_t* v_norm,
-                             const float* v_cb, const float* Pi_v, float* out, float* part, int P,
-                             int H, int B, int S, float scale, cudaStream_t st) {
-  if (B <= 1) return launch_decode_qb<KBITS, VBITS, 1>(A, k_plane, k_norm, k_cb, v_plane, v_norm, v_cb, Pi_v, out, part, P, H, B, S, scale, st);
-  if (B <= 2) return launch_decode_qb<KBITS, VBITS, 2>(A, k_plane, k_norm, k_cb, v_plane, v_norm, v_cb, Pi_v, out, part, P, H, B, S, scale, st);
-  if (B <= 4 || KBITS == 3) return launch_decode_qb<KBITS, VBITS, 4>(A, k_plane, k_norm, k_cb, v_plane, v_norm, v_cb, Pi_v, out, part, P, H, B, S, scale, st);
-  return launch_decode_qb<KBITS, VBITS, 8>(A, k_plane, k_norm, k_cb, v_plane, v_norm, v_cb, Pi_v, out, part, P, H, B, S, scale, st);
+template <int KBITS, int VBITS, bool PROD>
+cudaError_t launch_decode_kv(const SplitArgs& a, const float* Pi_v, float* out, int P, int H, cudaStream_t st) {
+  if (a.B <= 1) return launch_decode_qb<KBITS, VBITS, 1, PROD>(a, Pi_v, out, P, H, st);
+  if (a.B <= 2) return launch_decode_qb<KBITS, VBITS, 2, PROD>(a, Pi_v, out, P, H, st);
+  if (a.B <= 4 || KBITS == 3) return launch_decode_qb<KBITS, VBITS, 4, PROD>(a, Pi_v, out, P, H, st);
+  return launch_decode_qb<KBITS, VBITS, 8, PROD>(a, Pi_v, out, P, H, st);
 }
 
-template <int KBITS>
-cudaError_t launch_decode_k(const float* A, const uint8_t* k_plane, const uint16_t* k_norm,
-                            const float* k_cb, const uint8_t* v_plane, const uint16_t* v_norm,
-                            const float* v_cb, int v_bits, const float* Pi_v, float* out, float* part,
-                            int P, int H, int B, int S, float scale, cudaStream_t st) {
+template <int KBITS, bool PROD>
+cudaError_t launch_decode_k(const SplitArgs& a, int v_bits, const float* Pi_v, float* out, int P, int H,
+                            cudaStream_t st) {
   switch (v_bits) {
-    case 1: return launch_decode_kv<KBITS, 1>(A, k_plane, k_norm, k_cb, v_plane, v_norm, v_cb, Pi_v, out, part, P, H, B, S, scale, st);
-    case 2: return launch_decode_kv<KBITS, 2>(A, k_plane, k_norm, k_cb, v_plane, v_norm, v_cb, Pi_v, out, part, P, H, B, S, scale, st);
-    default: return launch_decode_kv<KBITS, 3>(A, k_plane, k_norm, k_cb, v_plane, v_norm, v_cb, Pi_v, out, part, P, H, B, S, scale, st);
+    case 1: return launch_decode_kv<KBITS, 1, PROD>(a, Pi_v, out, P, H, st);
+    case 2: return launch_decode_kv<KBITS, 2, PROD>(a, Pi_v, out, P, H, st);
+    default: return launch_decode_kv<KBITS, 3, PROD>(a, Pi_v, out, P, H, st);
+  }
+}
+
+template <bool PROD>
+cudaError_t launch_decode(const SplitArgs& a, int k_bits, int v_bits, const float* Pi_v, float* out, int P,
+                          int H, cudaStream_t st) {
+  switch (k_bits) {
+    case 1: return launch_decode_k<1, PROD>(a, v_bits, Pi_v, out, P, H, st);
+    case 2: return launch_decode_k<2, PROD>(a, v_bits, Pi_v, out, P, H, st);
+    default: return launch_decode_k<3, PROD>(a, v_bits, Pi_v, out, P, H, st);
   }
 }
 
@@ -508,11 +563,22 @@ cudaError_t launch_decode_mse(const float* A, const uint8_t* k_plane, const uint
                               const uint16_t* v_norm, const float* v_cb, int v_bits,
                               const float* Pi_v, float* out, float* part, int P, int H, int B, int S,
                               float scale, cudaStream_t st) {
-  switch (k_bits) {
-    case 1: return launch_decode_k<1>(A, k_plane, k_norm, k_cb, v_plane, v_norm, v_cb, v_bits, Pi_v, out, part, P, H, B, S, scale, st);
-    case 2: return launch_decode_k<2>(A, k_plane, k_norm, k_cb, v_plane, v_norm, v_cb, v_bits, Pi_v, out, part, P, H, B, S, scale, st);
-    default: return launch_decode_k<3>(A, k_plane, k_norm, k_cb, v_plane, v_norm, v_cb, v_bits, Pi_v, out, part, P, H, B, S, scale, st);
-  }
+  SplitArgs a = {A, nullptr, k_plane, nullptr, k_norm, k_cb, v_plane, v_norm, v_cb, part, B, S, 0, 0, scale, 0.f};
+  return launch_decode<false>(a, k_bits, v_bits, Pi_v, out, P, H, st);
 }
 
+cudaError_t launch_decode_prod(const float* A, const float* T, const uint8_t* k_plane,
+                               const uint8_t* k_sign, const uint16_t* k_gamma, const float* k_cb,
+                               int k_bits, const uint8_t* v_plane, const uint16_t* v_norm,
+                               const float* v_cb, int v_bits, const float* Pi_v, float* out,
+                               float* part, int P, int H, int B, int S, float scale, cudaStream_t st) {
+  SplitArgs a = {A, T, k_plane, k_sign, k_gamma, k_cb, v_plane, v_norm, v_cb, part, B, S, 0, 0, scale,
+                 qjl_scale(128)};
+  return launch_decode<true>(a, k_bits, v_bits, Pi_v, out, P, H, st);
+}
+
+}  // namespace tq
+
+namespace tq {
+cudaError_t take_faults_decode(unsigned int* bits) { return take_unit_faults(bits); }
 }  // namespace tq

@@ -106,6 +106,12 @@ cudaError_t launch_decode_mse(const float* A, const uint8_t* k_plane, const uint
                               const uint16_t* v_norm, const float* v_cb, int v_bits,
                               const float* Pi_v, float* out, float* part, int P, int H, int B, int S,
                               float scale, cudaStream_t st);
+// The same over a TurboQuant_prod key cache: code plane, sign plane and fp16 gamma.
+cudaError_t launch_decode_prod(const float* A, const float* T, const uint8_t* k_plane,
+                               const uint8_t* k_sign, const uint16_t* k_gamma, const float* k_cb,
+                               int k_bits, const uint8_t* v_plane, const uint16_t* v_norm,
+                               const float* v_cb, int v_bits, const float* Pi_v, float* out,
+                               float* part, int P, int H, int B, int S, float scale, cudaStream_t st);
 
 cudaError_t launch_pack_indices(const uint8_t* K_idx, uint8_t* plane, int64_t n, int D, int bits,
                                 cudaStream_t st);
@@ -117,5 +123,69 @@ cudaError_t launch_unpack_signs(const uint8_t* plane, int8_t* signs, int64_t n, 
                                 cudaStream_t st);
 
 inline int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
+
+// ---- bounded waits ----------------------------------------------------------
+// Every spin on an mbarrier in this library gives up after kWaitBudgetNs of the GPU's
+// global timer, records the failure in its translation unit's fault word and lets the
+// kernel finish (its outputs are then NaN); tq_device_faults reads and clears the words.
+constexpr uint64_t kWaitBudgetNs = 1000000000ull;   // 1 s
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Fault bits, one per kernel family.
+enum : unsigned int { kFaultLut = 1u, kFaultMma = 2u, kFaultDecode = 4u, kFaultCompress = 8u };
+
+// Reads and clears the fault word of each translation unit that has bounded waits
+// (synchronous: a cudaMemcpyFromSymbol per unit); ORs the bits into *bits.
+cudaError_t take_faults_simt(unsigned int* bits);
+cudaError_t take_faults_mma(unsigned int* bits);
+cudaError_t take_faults_decode(unsigned int* bits);
+cudaError_t take_faults_compress(unsigned int* bits);
+
+namespace {
+// This translation unit's fault word (internal linkage: one per unit).
+__device__ unsigned int g_wait_fault = 0;
+
+__device__ __forceinline__ bool mbar_poll(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+               : "=r"(ok)
+               : "r"(bar), "r"(parity)
+               : "memory");
+  return ok != 0;
+}
+
+// Wait for the given phase parity of a local mbarrier for at most kWaitBudgetNs; on
+// running out, set `fault` in this unit's fault word and return false.
+__device__ __forceinline__ bool wait_parity_bounded(uint32_t bar, uint32_t parity, unsigned int fault) {
+  if (mbar_poll(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (;;) {
+    for (int i = 0; i < 64; ++i)
+      if (mbar_poll(bar, parity)) return true;
+    if (global_ns() - t0 > kWaitBudgetNs) {
+      atomicOr(&g_wait_fault, fault);
+      return false;
+    }
+  }
+}
+
+// Host side of this unit's fault word.
+inline cudaError_t take_unit_faults(unsigned int* bits) {
+  unsigned int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_wait_fault, sizeof v);
+  if (e != cudaSuccess) return e;
+  if (v != 0) {
+    const unsigned int z = 0;
+    e = cudaMemcpyToSymbol(g_wait_fault, &z, sizeof z);
+  }
+  *bits |= v;
+  return e;
+}
+}  // namespace
 
 }  // namespace tq

@@ -31,4 +31,33 @@ __device__ __forceinline__ void table_centroids(const float* __restrict__ codebo
   for (int k = 0; k < L::G; ++k) cv[k] = __ldg(codebook + ((v >> (BITS * k)) & ((1 << BITS) - 1)));
 }
 
+// Two fp32 additions in one instruction (sm_100 packed f32x2): acc.lo += a, acc.hi += b.
+__device__ __forceinline__ void add2(unsigned long long& acc, float a, float b) {
+  asm("{\n\t.reg .b64 t;\n\tmov.b64 t, {%1, %2};\n\tadd.rn.f32x2 %0, %0, t;\n\t}" : "+l"(acc) : "f"(a), "f"(b));
+}
+__device__ __forceinline__ float sum2(unsigned long long acc) {
+  return __uint_as_float(static_cast<uint32_t>(acc)) + __uint_as_float(static_cast<uint32_t>(acc >> 32));
+}
+
+// Eight lookups, one per 4-bit field of w, in the 16-entry tables g0 .. g0+7 (table g
+// at tab + 16 g; field f of w is bits 4f .. 4f+3, field 2j the low and 2j+1 the high
+// nibble of byte j).  The byte offsets 4 * field come from two masked shifts of w and
+// one byte permute per field; each pair of lookups is one packed add per query.
+template <int QB, int PER_Q>
+__device__ __forceinline__ void lut_nibbles(const float* tab, uint32_t w, int g0,
+                                            unsigned long long (&acc)[QB][2]) {
+  const uint32_t lo = (w << 2) & 0x3C3C3C3Cu;
+  const uint32_t hi = (w >> 2) & 0x3C3C3C3Cu;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t ol = __byte_perm(lo, 0u, 0x4440u + j);
+    const uint32_t oh = __byte_perm(hi, 0u, 0x4440u + j);
+#pragma unroll
+    for (int q = 0; q < QB; ++q) {
+      const char* t = reinterpret_cast<const char*>(tab + q * PER_Q + (g0 + 2 * j) * 16);
+      add2(acc[q][j & 1], *reinterpret_cast<const float*>(t + ol), *reinterpret_cast<const float*>(t + 64 + oh));
+    }
+  }
+}
+
 }  // namespace tq

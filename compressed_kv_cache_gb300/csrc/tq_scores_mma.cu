@@ -57,7 +57,6 @@ template <int EPIW> struct Cfg {
 constexpr int kRawStages = 3;           // packed key-row stages in flight (full configuration)
 constexpr int kMaxN = 128;              // queries per tile
 constexpr int kXBytes = kM * kK * 2;    // 64 KB per key-tile buffer
-constexpr uint32_t kWaitPolls = 1u << 22;
 
 enum Layout { kUnpackedSmallC = 0, kUnpackedLargeC = 1, kPacked1 = 2, kPacked2 = 3, kPacked3 = 4 };
 
@@ -336,13 +335,20 @@ __device__ __forceinline__ void store_row(const Params& prm, const RawRow<LAYOUT
   }
 }
 
-// Bounded wait that also gives up once another role has raised the abort flag.
+// Bounded wait (kWaitBudgetNs of the global timer) that also gives up once another
+// role has raised the abort flag; the first role to run out records the fault.
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-  for (uint32_t i = 0; i < kWaitPolls; ++i) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 255u && *abort_flag) return false;
+    if ((i & 255u) == 0u) {
+      if (*abort_flag) return false;
+      if (global_ns() - t0 > kWaitBudgetNs) break;
+    }
   }
   *abort_flag = 1;
+  atomicOr(&g_wait_fault, kFaultMma);
   return false;
 }
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
@@ -921,4 +927,8 @@ cudaError_t launch_scores_mma(const float* A, const float* T, const uint8_t* idx
   }
 }
 
+}  // namespace tq
+
+namespace tq {
+cudaError_t take_faults_mma(unsigned int* bits) { return take_unit_faults(bits); }
 }  // namespace tq

@@ -254,43 +254,61 @@ __device__ __forceinline__ void load_packed_key(PackedKey<BITS>& k,
   k.g = __ldg(gamma_f16 + key);
 }
 
-// Code and sign sums of one key for QB queries, read from the tables [QB][PER_Q].
-// Two partial sums per part give two independent add chains.
+// Code and sign sums of one key for QB queries, read from the tables [QB][PER_Q]
+// (code tables first, then the 32 sign tables).
 template <int BITS, int QB>
 __device__ __forceinline__ void lut_key_sums(const float* lut, const PackedKey<BITS>& k,
                                              float (&mm)[QB], float (&rr)[QB]) {
   using L = LutShape<BITS>;
-  uint32_t w[4 * BITS + 1];
-#pragma unroll
-  for (int i = 0; i < BITS; ++i) {
-    w[4 * i] = k.idx[i].x; w[4 * i + 1] = k.idx[i].y; w[4 * i + 2] = k.idx[i].z; w[4 * i + 3] = k.idx[i].w;
-  }
-  w[4 * BITS] = 0u;
   const uint32_t ws[4] = {k.sg.x, k.sg.y, k.sg.z, k.sg.w};
-  float m[2][QB], r[2][QB];
+  unsigned long long r2[QB][2];
 #pragma unroll
-  for (int q = 0; q < QB; ++q) { m[0][q] = m[1][q] = 0.f; r[0][q] = r[1][q] = 0.f; }
+  for (int q = 0; q < QB; ++q) r2[q][0] = r2[q][1] = 0ull;
 #pragma unroll
-  for (int gi = 0; gi < L::NPI; ++gi) {
-    const int off = L::KB * gi;
-    const int wd = off >> 5, sh = off & 31;
-    uint32_t v;
-    if (sh + L::KB <= 32) {
-      v = (w[wd] >> sh) & (L::NV - 1);
-    } else {
-      v = __funnelshift_r(w[wd], w[wd + 1], sh) & (L::NV - 1);
+  for (int i = 0; i < 4; ++i) lut_nibbles<QB, L::PER_Q>(lut + L::NPI * L::NV, ws[i], 8 * i, r2);
+  if constexpr (L::KB == 4) {
+    // 1- and 2-bit codes: 4-bit fields, as the signs
+    unsigned long long m2[QB][2];
+#pragma unroll
+    for (int q = 0; q < QB; ++q) m2[q][0] = m2[q][1] = 0ull;
+#pragma unroll
+    for (int i = 0; i < BITS; ++i) {
+      lut_nibbles<QB, L::PER_Q>(lut, k.idx[i].x, 32 * i, m2);
+      lut_nibbles<QB, L::PER_Q>(lut, k.idx[i].y, 32 * i + 8, m2);
+      lut_nibbles<QB, L::PER_Q>(lut, k.idx[i].z, 32 * i + 16, m2);
+      lut_nibbles<QB, L::PER_Q>(lut, k.idx[i].w, 32 * i + 24, m2);
     }
 #pragma unroll
-    for (int q = 0; q < QB; ++q) m[gi & 1][q] += lut[q * L::PER_Q + gi * L::NV + v];
+    for (int q = 0; q < QB; ++q) mm[q] = sum2(m2[q][0]) + sum2(m2[q][1]);
+  } else {
+    // 3-bit codes: 6-bit fields (pairs of codes), some straddling two words
+    uint32_t w[4 * BITS + 1];
+#pragma unroll
+    for (int i = 0; i < BITS; ++i) {
+      w[4 * i] = k.idx[i].x; w[4 * i + 1] = k.idx[i].y; w[4 * i + 2] = k.idx[i].z; w[4 * i + 3] = k.idx[i].w;
+    }
+    w[4 * BITS] = 0u;
+    float m[2][QB];
+#pragma unroll
+    for (int q = 0; q < QB; ++q) m[0][q] = m[1][q] = 0.f;
+#pragma unroll
+    for (int gi = 0; gi < L::NPI; ++gi) {
+      const int off = L::KB * gi;
+      const int wd = off >> 5, sh = off & 31;
+      uint32_t v;
+      if (sh + L::KB <= 32) {
+        v = (w[wd] >> sh) & (L::NV - 1);
+      } else {
+        v = __funnelshift_r(w[wd], w[wd + 1], sh) & (L::NV - 1);
+      }
+#pragma unroll
+      for (int q = 0; q < QB; ++q) m[gi & 1][q] += lut[q * L::PER_Q + gi * L::NV + v];
+    }
+#pragma unroll
+    for (int q = 0; q < QB; ++q) mm[q] = m[0][q] + m[1][q];
   }
 #pragma unroll
-  for (int gi = 0; gi < L::NPS; ++gi) {
-    const uint32_t v = (ws[gi >> 3] >> (4 * (gi & 7))) & 15u;
-#pragma unroll
-    for (int q = 0; q < QB; ++q) r[gi & 1][q] += lut[q * L::PER_Q + L::NPI * L::NV + gi * 16 + v];
-  }
-#pragma unroll
-  for (int q = 0; q < QB; ++q) { mm[q] = m[0][q] + m[1][q]; rr[q] = r[0][q] + r[1][q]; }
+  for (int q = 0; q < QB; ++q) rr[q] = sum2(r2[q][0]) + sum2(r2[q][1]);
 }
 
 // Tables of QB queries from A (a[0..127]) and T (a[128..255]) of each query,
@@ -476,54 +494,57 @@ cudaError_t launch_lut_bits(const float* A, const float* T, const uint8_t* idx_p
 // per call with nothing written to a workspace ("TurboQuant Attention in CUDA",
 // "Two kernels, two jobs": the first kernel, here inside the second).
 //
-// A cluster of CS CTAs (8 for few problems, 2 for many) serves one (problem,
-// query tile); each CTA scores one contiguous range of the keys.  The stacked
-// matrix [Pi; S_mat] of the problem's head has 256 rows; CTA rank r brings rows
-// r*R .. r*R+R-1 (R = 256/CS) into its shared memory with one bulk copy, forms
-// those rows of A = Pi q and T = S_mat q for its QB queries (a warp per 8 rows,
-// the query in registers), and sends each group of 8 rows to every CTA of the
-// cluster by a shared-to-shared bulk copy that completes bytes on the receiver's
-// mbarrier.  Once that mbarrier has seen all 256 rows a CTA holds all of A and
-// T, builds the same lookup tables as scores_packed_lut_kernel and scores its
-// keys.  Order of requests: the rows and, for short ranges, an L2 prefetch of the
-// key rows (copy engine), then the query and the codebook, then - after the rows
-// have landed - every thread's first two keys, which stay in flight through the
-// exchange and the table build.  The kernel is launched as a programmatic
-// dependent: everything it reads from global memory is read after
-// griddepcontrol.wait.
+// A cluster of CS CTAs serves one (problem, query tile); each CTA scores one
+// contiguous range of the keys.  The stacked matrix [Pi; S_mat] of the problem's
+// head has 256 rows; CTA rank r brings rows r*R .. r*R+R-1 (R = 256/CS) into its
+// shared memory with one bulk copy, forms those rows of A = Pi q and T = S_mat q for
+// its QB queries (a warp per 8 rows, the query in registers), and sends each group
+// of 8 rows to every CTA of the cluster by a shared-to-shared bulk copy that
+// completes bytes on the receiver's mbarrier.  Once that mbarrier has seen all 256
+// rows a CTA holds all of A and T, builds the lookup tables and scores its keys.
+//
+// Keys stream through a ring of kFusedStages shared-memory tiles of kFusedThreads
+// keys (one key per thread per tile), each filled by two bulk copies (code rows, sign
+// rows) that complete on the tile's mbarrier.  Registers hold the kernel to two CTAs
+// a SM, so the clusters spread evenly.  The kernel is launched as a programmatic
+// dependent and triggers its own dependents at entry: the next call's CTAs take each
+// SM as this call's leave it.  Before griddepcontrol.wait a CTA only asks L2 to
+// prefetch what it will read (its key range, its rows of [Pi; S_mat], the query
+// tile), a hint that changes no result whatever the kernel before it writes.  Every
+// read of global memory into registers or shared memory follows the wait; the rows
+// of [Pi; S_mat] are requested before the key tiles, which queue behind them.
 // ---------------------------------------------------------------------------
-template <int QB>
-__host__ __device__ constexpr int fused_threads() { return QB <= 2 ? 512 : 256; }
-// CTAs per SM the register budget is cut for (64 registers a thread for 512
-// threads, 128 for 256)
-template <int QB>
-__host__ __device__ constexpr int fused_min_blocks() { return 2; }
-
-// Shared memory of the fused kernel: the CTA's rows of [Pi; S_mat], three mbarriers,
-// its slice of A/T, all of A/T and the tables; then, when its key range is staged, the
-// range's code rows and sign rows.
+constexpr int kFusedThreads = 512;
+constexpr int kFusedStages = 3;
+// Dynamic shared memory of one CTA: the tables, the CTA's rows of [Pi; S_mat] and the
+// key-tile ring (A/T and the barriers are static).
 template <int BITS, int QB, int CS>
-constexpr size_t fused_smem_bytes() {
-  return (256 / CS) * 128 * sizeof(float) + 32 +
-         ((256 / CS) * QB + QB * 256 + QB * LutShape<BITS>::PER_Q) * sizeof(float);
+constexpr size_t fused_dyn_smem_bytes() {
+  return static_cast<size_t>(QB) * LutShape<BITS>::PER_Q * sizeof(float) + (256 / CS) * 128 * sizeof(float) +
+         static_cast<size_t>(kFusedStages) * kFusedThreads * (16 * BITS + 16);
 }
-constexpr int kFusedStageMax = 48 * 1024;   // the largest key range staged in shared memory (bytes)
-
-// Bounded wait for the given phase parity of a local mbarrier (about a second at most).
-__device__ __forceinline__ bool wait_parity(uint32_t bar, uint32_t parity) {
-  for (uint32_t it = 0; it < (1u << 22); ++it) {
-    uint32_t ok;
-    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-                 : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
-    if (ok) return true;
-  }
-  return false;
-}
+// Keys of a range asked of L2 before the dependency wait, at most.
+constexpr int kFusedPrefetchKeys = 2048;
 
 __device__ __forceinline__ void expect_bytes(uint32_t bar, uint32_t bytes) {
   asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(bar),
                "r"(bytes)
                : "memory");
+}
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+// L2 prefetch of [p, p + bytes), trimmed to whole 16-byte blocks inside the range.
+__device__ __forceinline__ void prefetch_l2(const void* p, size_t bytes) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  const uintptr_t lo = (a + 15) & ~static_cast<uintptr_t>(15);
+  const uintptr_t hi = (a + bytes) & ~static_cast<uintptr_t>(15);
+  if (hi > lo)
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(lo), "r"(static_cast<uint32_t>(hi - lo))
+                 : "memory");
 }
 
 // Coordinates 4*lane .. 4*lane+3 of one query row of 128.
@@ -579,54 +600,66 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t local_addr, uint32_t ra
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
   return remote;
 }
+
 template <int BITS, int QB, int CS, typename QT>
-__global__ void __launch_bounds__(fused_threads<QB>(), fused_min_blocks<QB>())
+__global__ void __launch_bounds__(kFusedThreads, QB <= 2 ? 2 : 1)
 solve_packed_lut_kernel(const QT* __restrict__ Q, const float* __restrict__ Pi,
                         const float* __restrict__ Sm, int H, const uint8_t* __restrict__ idx_plane,
                         const uint8_t* __restrict__ sign_plane,
                         const uint16_t* __restrict__ gamma_f16,
                         const float* __restrict__ codebook, float* __restrict__ scores, int B,
-                        int S, float kappa, int staged) {
+                        int S, float kappa) {
+  using L = LutShape<BITS>;
   constexpr int D = 128;
-  constexpr int kT = fused_threads<QB>();
+  constexpr int kT = kFusedThreads;
   constexpr int R = 256 / CS;                             // rows of [Pi; S_mat] per CTA
-  static_assert(R % 8 == 0 && CS <= 32, "transform split");
-  extern __shared__ __align__(16) float smem[];
-  float* sRows = smem;                                    // [R][128]
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sRows + R * D);   // [0]: rows, [1]: A/T, [2]: keys
-  float* sMine = reinterpret_cast<float*>(bar + 4);       // [R][QB]: this CTA's rows of A/T
-  float* sAT = sMine + R * QB;                            // [256][QB]: rows of A, then of T
-  float* lut = sAT + QB * 256;                            // [QB][PER_Q]
-  uint8_t* sKidx = reinterpret_cast<uint8_t*>(lut + QB * LutShape<BITS>::PER_Q);   // [range][16 BITS]
+  constexpr int kRowBytes = 16 * BITS;                    // code bytes of one key
+  constexpr int kTile = kT * (kRowBytes + 16);            // bytes of one key tile
+  static_assert(R % 8 == 0 && CS <= 32 && R / 8 <= kT / 32, "transform split");
+  __shared__ __align__(16) float sAT[256 * QB];           // [256][QB]: rows of A, then of T
+  __shared__ __align__(16) float sMine[R * QB];           // [R][QB]: this CTA's rows of A/T
+  __shared__ __align__(8) uint64_t bars[2 + kFusedStages];   // rows, A/T, key tiles
+  extern __shared__ __align__(128) float dsm[];
+  float* lut = dsm;                                       // [QB][PER_Q]
+  float* sRows = lut + QB * L::PER_Q;                     // [R][128]
+  uint8_t* sTiles = reinterpret_cast<uint8_t*>(sRows + R * D);   // [stage][kT code rows | kT sign rows]
   const int p = blockIdx.z;
   const int h = p % H;
   const int b0 = blockIdx.y * QB;
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
-  // this CTA's keys: one contiguous range, walked by the threads in steps of kT
-  const int chunk = static_cast<int>((static_cast<int64_t>(S) + gridDim.x - 1) / gridDim.x);
-  const int k_begin = static_cast<int>(min(static_cast<int64_t>(blockIdx.x) * chunk, static_cast<int64_t>(S)));
-  const int k_end = k_begin + chunk < S ? k_begin + chunk : S;
-  const int first = k_begin + tid;
-  // staged: the whole key range comes into shared memory by two bulk copies
-  const int nkeys = k_end - k_begin;
-  const bool stage = staged != 0 && nkeys > 0;
-  uint8_t* sKsg = sKidx + static_cast<size_t>(chunk) * (16 * BITS);                  // [range][16]
+  // this CTA's keys: one contiguous range of whole tiles of 8 keys
+  const int64_t per = ((static_cast<int64_t>(S) + gridDim.x - 1) / gridDim.x + 7) / 8 * 8;
+  const int k_begin = static_cast<int>(min(static_cast<int64_t>(blockIdx.x) * per, static_cast<int64_t>(S)));
+  const int k_end = static_cast<int>(min(static_cast<int64_t>(k_begin) + per, static_cast<int64_t>(S)));
+  const int ntiles = (k_end - k_begin + kT - 1) / kT;
+  const size_t key0 = static_cast<size_t>(p) * S + k_begin;
   const uint32_t rank = cluster_ctarank();
   const int row0 = static_cast<int>(rank) * R;
+  const float* rows_src = (row0 < D ? Pi : Sm) + (static_cast<size_t>(h) * D + (row0 & (D - 1))) * D;
+  const uint32_t bar_rows = static_cast<uint32_t>(__cvta_generic_to_shared(bars));
+  const uint32_t bar_at = bar_rows + 8;
+  const uint32_t bar_tile = bar_rows + 16;
 
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const uint32_t bar_rows = static_cast<uint32_t>(__cvta_generic_to_shared(bar));
-  const uint32_t bar_at = bar_rows + 8;
-  const uint32_t bar_keys = bar_rows + 16;
   if (tid == 0) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar_rows) : "memory");
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar_at) : "memory");
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar_keys) : "memory");
+#pragma unroll
+    for (int i = 0; i < 2 + kFusedStages; ++i)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar_rows + 8 * i) : "memory");
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     expect_bytes(bar_at, 256 * QB * 4);
+    // hints only: whatever lands in L2 now is still read after the wait below
+    prefetch_l2(rows_src, R * D * sizeof(float));
+    const int npre = min(k_end - k_begin, kFusedPrefetchKeys);
+    if (npre > 0) {
+      prefetch_l2(idx_plane + key0 * kRowBytes, static_cast<size_t>(npre) * kRowBytes);
+      prefetch_l2(sign_plane + key0 * 16, static_cast<size_t>(npre) * 16);
+      prefetch_l2(gamma_f16 + key0, static_cast<size_t>(npre) * 2);
+    }
+    const int nq = min(QB, B - b0);
+    if (nq > 0) prefetch_l2(Q + (static_cast<size_t>(p) * B + b0) * D, static_cast<size_t>(nq) * D * sizeof(QT));
   }
-  // both barriers are initialised before any thread of the cluster uses them, and
+  // the barriers are initialised before any thread of the cluster uses them, and
   // every CTA of the cluster runs before anyone copies into a peer
   __syncthreads();
   cluster_arrive_relaxed();
@@ -634,109 +667,78 @@ solve_packed_lut_kernel(const QT* __restrict__ Q, const float* __restrict__ Pi,
   asm volatile("griddepcontrol.wait;" ::: "memory");
   if (tid == 0) {
     expect_bytes(bar_rows, R * D * 4);
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     static_cast<uint32_t>(__cvta_generic_to_shared(sRows))),
-                 "l"((row0 < D ? Pi : Sm) + (static_cast<size_t>(h) * D + (row0 & (D - 1))) * D),
-                 "r"(static_cast<uint32_t>(R * D * 4)), "r"(bar_rows)
-                 : "memory");
-    // a short range of key rows (up to 64 KB) starts streaming from HBM into L2
-    // now, through the copy engine rather than the load pipe, so the prologue's own
-    // reads are not held up
-    if (!stage && k_end > k_begin && (k_end - k_begin) * (16 * BITS + 16) <= 65536) {
-      const size_t key0 = static_cast<size_t>(p) * S + k_begin;
-      const uint32_t n = static_cast<uint32_t>(k_end - k_begin);
-      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(idx_plane + key0 * (16 * BITS)),
-                   "r"(n * (16u * BITS))
-                   : "memory");
-      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(sign_plane + key0 * 16), "r"(n * 16u)
-                   : "memory");
+    bulk_g2s(sRows, rows_src, R * D * 4, bar_rows);
+    for (int t = 0; t < kFusedStages && t < ntiles; ++t) {
+      const int nk = min(kT, k_end - k_begin - t * kT);
+      uint8_t* st = sTiles + t * kTile;
+      expect_bytes(bar_tile + 8 * t, static_cast<uint32_t>(nk * (kRowBytes + 16)));
+      bulk_g2s(st, idx_plane + (key0 + t * kT) * kRowBytes, nk * kRowBytes, bar_tile + 8 * t);
+      bulk_g2s(st + kT * kRowBytes, sign_plane + (key0 + t * kT) * 16, nk * 16, bar_tile + 8 * t);
     }
   }
-  float cv[LutShape<BITS>::G];
+  float cv[L::G];
   table_centroids<BITS>(codebook, cv);
-  // gamma of this thread's first key (staged ranges)
-  const float g_first =
-      stage && first < k_end ? __half2float(__ushort_as_half(__ldg(gamma_f16 + static_cast<size_t>(p) * S + first))) : 0.f;
+  // gamma of this thread's key in the first tile (later tiles: one tile ahead)
+  float g_next = k_begin + tid < k_end ? __half2float(__ushort_as_half(__ldg(gamma_f16 + key0 + tid))) : 0.f;
   // rows of A/T: warp w takes groups of 8 rows; lane l reads coordinates 4l .. 4l+3
   // of each row (one conflict-free 512-byte row a warp) and the warp sums them.  Each
   // group goes to every CTA of the cluster by its own bulk copies, completing bytes
   // on the receiver's mbarrier, so no warp waits for another here.
-  // Every warp waits for the rows before its keys are requested, so that their
-  // flood does not delay the query and the rows.
-  float4 qx[QB];                                          // the query tile; rows past B are zero
   if (warp < R / 8) {
+    float4 qx[QB];                                        // the query tile; rows past B are zero
 #pragma unroll
     for (int q = 0; q < QB; ++q) {
       qx[q] = b0 + q < B ? load_query4(Q + (static_cast<size_t>(p) * B + b0 + q) * D, lane)
                          : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-  }
-  const bool landed = wait_parity(bar_rows, 0);
-  // the query and the rows are in: the key range may stream in now, during the
-  // transform, the exchange and the tables
-  if (stage && tid == 0) {
-    const size_t key0 = static_cast<size_t>(p) * S + k_begin;
-    expect_bytes(bar_keys, static_cast<uint32_t>(nkeys * (16 * BITS + 16)));
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     static_cast<uint32_t>(__cvta_generic_to_shared(sKidx))),
-                 "l"(idx_plane + key0 * (16 * BITS)), "r"(static_cast<uint32_t>(nkeys * (16 * BITS))), "r"(bar_keys)
-                 : "memory");
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     static_cast<uint32_t>(__cvta_generic_to_shared(sKsg))),
-                 "l"(sign_plane + key0 * 16), "r"(static_cast<uint32_t>(nkeys * 16)), "r"(bar_keys)
-                 : "memory");
-  }
-  if (warp < R / 8) {
-    for (int g = warp; g < R / 8; g += kT / 32) {
-      float part[QB][8];
+    const bool landed = wait_parity_bounded(bar_rows, 0, kFaultLut);
+    const int g = warp;
+    float part[QB][8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float4 m = *reinterpret_cast<const float4*>(sRows + (g * 8 + i) * D + 4 * lane);
+    for (int i = 0; i < 8; ++i) {
+      const float4 m = *reinterpret_cast<const float4*>(sRows + (g * 8 + i) * D + 4 * lane);
 #pragma unroll
-        for (int q = 0; q < QB; ++q)
-          part[q][i] = fmaf(m.w, qx[q].w, fmaf(m.z, qx[q].z, fmaf(m.y, qx[q].y, m.x * qx[q].x)));
-      }
-      const int r = g * 8 + ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
+      for (int q = 0; q < QB; ++q)
+        part[q][i] = fmaf(m.w, qx[q].w, fmaf(m.z, qx[q].z, fmaf(m.y, qx[q].y, m.x * qx[q].x)));
+    }
+    const int r = g * 8 + ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
 #pragma unroll
-      for (int q = 0; q < QB; ++q) {
-        const float v = warp_sum8(part[q], lane);
-        if ((lane & 3) == 0) sMine[r * QB + q] = landed ? v : __int_as_float(0x7fc00000);
-      }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      __syncwarp();
-      if (lane < CS) {
-        const uint32_t src = static_cast<uint32_t>(__cvta_generic_to_shared(sMine + g * 8 * QB));
-        const uint32_t dst = map_to_rank(
-            static_cast<uint32_t>(__cvta_generic_to_shared(sAT + (row0 + g * 8) * QB)), static_cast<uint32_t>(lane));
-        asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-                     "r"(src), "r"(static_cast<uint32_t>(8 * QB * 4)),
-                     "r"(map_to_rank(bar_at, static_cast<uint32_t>(lane)))
-                     : "memory");
-      }
+    for (int q = 0; q < QB; ++q) {
+      const float v = warp_sum8(part[q], lane);
+      if ((lane & 3) == 0) sMine[r * QB + q] = landed ? v : __int_as_float(0x7fc00000);
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    if (lane < CS) {
+      const uint32_t src = static_cast<uint32_t>(__cvta_generic_to_shared(sMine + g * 8 * QB));
+      const uint32_t dst = map_to_rank(
+          static_cast<uint32_t>(__cvta_generic_to_shared(sAT + (row0 + g * 8) * QB)), static_cast<uint32_t>(lane));
+      asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                   "r"(src), "r"(static_cast<uint32_t>(8 * QB * 4)),
+                   "r"(map_to_rank(bar_at, static_cast<uint32_t>(lane)))
+                   : "memory");
     }
   }
-  // the first two keys of every thread, in flight during the exchange and the tables
-  PackedKey<BITS> k0, k1;
-  if (!stage) prefetch_two_keys<BITS>(k0, k1, idx_plane, sign_plane, gamma_f16, p, first, kT, k_end, S);
   // every copy into this CTA has completed (so every peer is done reading the slices
-  // it sent here); the cluster barrier below keeps each CTA alive until all have
-  const bool have_at = wait_parity(bar_at, 0);
+  // it sent here); the cluster barrier at the end keeps each CTA alive until all have
+  const bool have_at = wait_parity_bounded(bar_at, 0, kFaultLut);
   cluster_arrive_relaxed();
   build_luts<BITS, QB, kT>(
       [&](int q, int e) { return have_at ? sAT[e * QB + q] : __int_as_float(0x7fc00000); }, lut, cv);
   __syncthreads();
-  if (stage) {
-    // keys from the staged range; a range that never landed scores NaN
-    const bool have_keys = wait_parity(bar_keys, 0);
-    for (int s = first; s < k_end; s += kT) {
-      const int i = s - k_begin;
+  for (int t = 0; t < ntiles; ++t) {
+    const int stage = t % kFusedStages;
+    const uint8_t* st = sTiles + stage * kTile;
+    const bool have_keys = wait_parity_bounded(bar_tile + 8 * stage, (t / kFusedStages) & 1, kFaultLut);
+    const int s = k_begin + t * kT + tid;
+    const float g = g_next;
+    if (t + 1 < ntiles)
+      g_next = s + kT < k_end ? __half2float(__ushort_as_half(__ldg(gamma_f16 + key0 + (t + 1) * kT + tid))) : 0.f;
+    if (s < k_end) {
       PackedKey<BITS> k;
 #pragma unroll
-      for (int r = 0; r < BITS; ++r)
-        k.idx[r] = *reinterpret_cast<const uint4*>(sKidx + static_cast<size_t>(i) * (16 * BITS) + 16 * r);
-      k.sg = *reinterpret_cast<const uint4*>(sKsg + static_cast<size_t>(i) * 16);
-      const float g = s == first ? g_first
-                                 : __half2float(__ushort_as_half(__ldg(gamma_f16 + static_cast<size_t>(p) * S + s)));
+      for (int r = 0; r < BITS; ++r) k.idx[r] = *reinterpret_cast<const uint4*>(st + tid * kRowBytes + 16 * r);
+      k.sg = *reinterpret_cast<const uint4*>(st + kT * kRowBytes + tid * 16);
       float mm[QB], rr[QB];
       lut_key_sums<BITS, QB>(lut, k, mm, rr);
       if (!have_keys) {
@@ -745,24 +747,36 @@ solve_packed_lut_kernel(const QT* __restrict__ Q, const float* __restrict__ Pi,
       }
       store_scores<QB>(scores, mm, rr, kappa * g, p, b0, B, S, s);
     }
-  } else {
-    lut_score_keys<BITS, QB>(lut, idx_plane, sign_plane, gamma_f16, scores, k0, k1, first, kT, k_end,
-                             p, b0, B, S, kappa);
+    if (t + kFusedStages < ntiles) {
+      __syncthreads();                    // every thread is done with this stage
+      if (tid == 0) {
+        const int tn = t + kFusedStages;
+        const int nk = min(kT, k_end - k_begin - tn * kT);
+        uint8_t* sd = sTiles + stage * kTile;
+        expect_bytes(bar_tile + 8 * stage, static_cast<uint32_t>(nk * (kRowBytes + 16)));
+        bulk_g2s(sd, idx_plane + (key0 + static_cast<size_t>(tn) * kT) * kRowBytes, nk * kRowBytes, bar_tile + 8 * stage);
+        bulk_g2s(sd + kT * kRowBytes, sign_plane + (key0 + static_cast<size_t>(tn) * kT) * 16, nk * 16,
+                 bar_tile + 8 * stage);
+      }
+    }
   }
   cluster_wait();
 }
 
 // One launch of the fused kernel with clusters of CS CTAs.  The grid gets as many
-// clusters per (problem, query tile) unit as the co-resident capacity holds for
-// every unit at once (at least one), and no more than leave a CTA 64 keys.
+// clusters per (problem, query tile) unit as are co-resident for every unit at once
+// (at least one), and no more than leave a CTA 64 keys.  For short calls (at most two
+// key tiles a CTA) it keeps 1/9 of the co-resident clusters free: back-to-back calls
+// overlap (programmatic dependent launch), and with every slot planned some clusters
+// of the next call find no whole group of free SMs and start a wave late.  Measured on
+// GB300 at B = 1: 131072 keys took 5.35 us a call at 36 clusters, 4.66 us at 32; from
+// 524288 keys on the full grid is faster (3-9 %).
 template <int BITS, int QB, int CS, typename QT>
 cudaError_t launch_fused_cs(const QT* Q, const float* Pi, const float* S_mat, int H,
                             const uint8_t* idx_plane, const uint8_t* sign_plane,
                             const uint16_t* gamma_f16, const float* codebook, float* scores,
                             int P, int B, int S, cudaStream_t st) {
-  constexpr int kT = fused_threads<QB>();
-  constexpr size_t smem_base = fused_smem_bytes<BITS, QB, CS>();
-  constexpr size_t smem_max = smem_base + kFusedStageMax;
+  constexpr size_t smem = fused_dyn_smem_bytes<BITS, QB, CS>();
   auto kernel = solve_packed_lut_kernel<BITS, QB, CS, QT>;
   static std::atomic<uint64_t> configured{0};
   static std::atomic<int> capacity[64];                   // co-resident clusters per device
@@ -778,16 +792,16 @@ cudaError_t launch_fused_cs(const QT* Q, const float* Pi, const float* S_mat, in
   attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.blockDim = dim3(kT);
-  cfg.dynamicSmemBytes = smem_max;          // the capacity below holds for any staged range
+  cfg.blockDim = dim3(kFusedThreads);
   cfg.stream = st;
   cfg.attrs = attr;
   if (!(configured.load(std::memory_order_acquire) & bit)) {
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_max));
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     int n = 0;
     cfg.gridDim = dim3(CS);
     cfg.numAttrs = 1;
+    cfg.dynamicSmemBytes = smem;
     e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
     if (e != cudaSuccess) return e;
     capacity[dev & 63].store(n > 0 ? n : 1, std::memory_order_relaxed);
@@ -795,19 +809,17 @@ cudaError_t launch_fused_cs(const QT* Q, const float* Pi, const float* S_mat, in
   }
   const int qtiles = ceil_div(B, QB);
   const int64_t units = static_cast<int64_t>(P) * qtiles;
-  const int fill = static_cast<int>(capacity[dev & 63].load(std::memory_order_relaxed) / units);
+  int cap = capacity[dev & 63].load(std::memory_order_relaxed);
+  if (static_cast<int64_t>(S) * units <= static_cast<int64_t>(cap) * CS * 2 * kFusedThreads) cap = cap * 8 / 9;
+  const int fill = static_cast<int>(cap / units);
   const int most = ceil_div(S, 64 * CS);                  // at least 64 keys a CTA on average
   const int clusters = fill < most ? fill : most;
   const int gx = (clusters < 1 ? 1 : clusters) * CS;
   cfg.gridDim = dim3(gx, qtiles, P);
   cfg.numAttrs = 2;
-  // the key range of a CTA (as the kernel cuts it) is staged when it fits
-  const int64_t chunk = (static_cast<int64_t>(S) + gx - 1) / gx;
-  const int64_t stage_bytes = chunk * (16 * BITS + 16);
-  const int staged = stage_bytes <= kFusedStageMax ? 1 : 0;
-  cfg.dynamicSmemBytes = smem_base + (staged ? static_cast<size_t>(stage_bytes) : 0);
+  cfg.dynamicSmemBytes = smem;
   e = cudaLaunchKernelEx(&cfg, kernel, Q, Pi, S_mat, H, idx_plane, sign_plane, gamma_f16, codebook,
-                         scores, B, S, qjl_scale(128), staged);
+                         scores, B, S, qjl_scale(128));
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -949,4 +961,8 @@ cudaError_t launch_solve_packed_fused(const void* Q, tq_qtype qtype, const float
                             gamma_f16, codebook, scores, P, B, S, idx_bits, st);
 }
 
+}  // namespace tq
+
+namespace tq {
+cudaError_t take_faults_simt(unsigned int* bits) { return take_unit_faults(bits); }
 }  // namespace tq

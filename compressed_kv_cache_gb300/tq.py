@@ -38,6 +38,7 @@ _P, _I, _L, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
 _SIGNATURES = {
     "tq_status_string": ([_I], ctypes.c_char_p),
     "tq_auto_path": ([_I, _I], _I),
+    "tq_device_faults": ([ctypes.POINTER(ctypes.c_uint)], _I),
     "tq_prepare_queries": ([_P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _P], _I),
     "tq_scores": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P], _I),
     "tq_scores_packed": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P], _I),
@@ -47,6 +48,8 @@ _SIGNATURES = {
     "tq_decode_workspace_bytes": ([_I, _I, _I, _I], ctypes.c_size_t),
     "tq_decode_mse": ([_P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, ctypes.c_float,
                        _P, ctypes.c_size_t, _P], _I),
+    "tq_decode_prod": ([_P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, ctypes.c_float,
+                        _P, ctypes.c_size_t, _P], _I),
     "tq_workspace_bytes": ([_I, _I, _I], _Z),
     "tq_solve": ([_P, _I, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _Z, _I, _P], _I),
     "tq_solve_packed": ([_P, _I, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _Z, _I, _P], _I),
@@ -91,6 +94,15 @@ def status_string(status: int) -> str:
 
 def auto_path(B: int, D: int) -> str:
     return PATH_NAMES[lib().tq_auto_path(B, D)]
+
+
+def device_faults() -> int:
+    """Fault bits the bounded waits of libtq's kernels set on the current device since the
+    last call (0 = none; 1 lookup-table scorers, 2 tensor-core scorer, 4 decode, 8
+    compressor); reading clears them.  Synchronises with the device."""
+    v = ctypes.c_uint(0)
+    _check("tq_device_faults", lib().tq_device_faults(ctypes.byref(v)))
+    return int(v.value)
 
 
 def _check(fn: str, status: int) -> None:
@@ -251,6 +263,39 @@ def decode_mse(A, k_plane, k_norm, k_codebook, k_bits, v_plane, v_norm, v_codebo
     _check("tq_decode_mse", lib().tq_decode_mse(
         _dev(A, "A", (torch.float32,)), _dev(k_plane, "k_plane", (torch.uint8,)),
         _dev(k_norm, "k_norm", (torch.float16,)), _dev(k_codebook, "k_codebook", (torch.float32,)), k_bits,
+        _dev(v_plane, "v_plane", (torch.uint8,)), _dev(v_norm, "v_norm", (torch.float16,)),
+        _dev(v_codebook, "v_codebook", (torch.float32,)), v_bits, _dev(Pi_v, "Pi_v", (torch.float32,)),
+        _dev(o, "out", (torch.float32,)), P, H, B, S, D, float(scale),
+        _dev(workspace, "workspace", (torch.uint8,)), workspace.numel(), _stream()))
+    return o if (out is not None or A.dim() == 3) else o.view(B, D)
+
+
+def decode_prod(A, T, k_plane, k_sign_plane, k_gamma, k_codebook, k_bits, v_plane, v_norm, v_codebook,
+                v_bits, Pi_v, scale=None, workspace=None, out=None):
+    """Attention output over a TurboQuant_prod key cache and MSE-quantized values.
+    A, T [P,B,128] from prepare_queries; k_plane uint8 [P,S,128*k_bits/8], k_sign_plane
+    uint8 [P,S,16], k_gamma float16 [P,S]; values as for decode_mse.  Returns [P,B,128]
+    (or [B,128])."""
+    P, B, D = _as3(A)
+    if _as3(T) != (P, B, D):
+        raise ValueError("A and T must have the same shape")
+    S, krow = _keys3(k_plane, P)
+    S2, srow = _keys3(k_sign_plane, P)
+    _, vrow = _keys3(v_plane, P)
+    H = 1 if Pi_v.dim() == 2 else Pi_v.shape[0]
+    if (krow * 8 != D * k_bits or srow * 8 != D or S2 != S or vrow * 8 != D * v_bits
+            or k_gamma.numel() != P * S or v_norm.numel() != P * S):
+        raise ValueError("inconsistent key/value shapes")
+    need = int(lib().tq_decode_workspace_bytes(P, B, S, D))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), device=A.device, dtype=torch.uint8)
+    o = out if out is not None else torch.empty((P, B, D), device=A.device, dtype=torch.float32)
+    if scale is None:
+        scale = 1.0 / float(D) ** 0.5
+    _check("tq_decode_prod", lib().tq_decode_prod(
+        _dev(A, "A", (torch.float32,)), _dev(T, "T", (torch.float32,)), _dev(k_plane, "k_plane", (torch.uint8,)),
+        _dev(k_sign_plane, "k_sign_plane", (torch.uint8,)), _dev(k_gamma, "k_gamma", (torch.float16,)),
+        _dev(k_codebook, "k_codebook", (torch.float32,)), k_bits,
         _dev(v_plane, "v_plane", (torch.uint8,)), _dev(v_norm, "v_norm", (torch.float16,)),
         _dev(v_codebook, "v_codebook", (torch.float32,)), v_bits, _dev(Pi_v, "Pi_v", (torch.float32,)),
         _dev(o, "out", (torch.float32,)), P, H, B, S, D, float(scale),

@@ -18,9 +18,11 @@
  * Conventions shared by every entry point
  * ---------------------------------------
  * - Memory: unless stated otherwise every pointer is a DEVICE pointer owned by
- *   the caller.  The library allocates no memory and keeps no mutable global
- *   state; concurrent calls on different streams are safe as long as their
- *   output and workspace buffers do not overlap.
+ *   the caller.  The library allocates no memory.  Its only mutable device state
+ *   is the fault bits of the bounded waits (tq_device_faults) and the fixed
+ *   scratch array of tq_solve_packed_noalloc; every other call is safe to run
+ *   concurrently on different streams as long as their output and workspace
+ *   buffers do not overlap.
  * - Streams: every call is asynchronous on `stream` (0 = legacy default
  *   stream).  Outputs are valid once the stream reaches the call.
  * - Errors: argument errors are reported synchronously, before anything is
@@ -74,6 +76,17 @@ const char* tq_status_string(tq_status status);
 
 /* The path TQ_PATH_AUTO resolves to for B queries of length D per problem. */
 tq_path tq_auto_path(int B, int D);
+
+/* Faults of the bounded waits.  Every wait of a kernel on an mbarrier (a bulk copy
+ * landing, a peer CTA's rows arriving, a tensor-core stage) gives up after one second
+ * of the GPU's global timer; the kernel then finishes with NaN in the outputs it could
+ * not compute and sets a fault bit on the device instead of hanging it.
+ * tq_device_faults ORs into *bits the fault bits set on the CURRENT device since the
+ * last call and clears them: 1 = fp32 lookup-table scorers, 2 = tensor-core scorer,
+ * 4 = fused decode, 8 = compressor.  It synchronises with the device (it reads device
+ * memory) and is not for use inside stream capture.  bits: host pointer, not NULL.
+ * Errors: TQ_ERR_INVALID_VALUE (bits NULL), TQ_ERR_LAUNCH (the device read failed). */
+tq_status tq_device_faults(unsigned int* bits);
 
 /* ------------------------------------------------------------------------
  * Query transform (riteshyadav.xyz, "Two kernels, two jobs", first kernel;
@@ -192,6 +205,30 @@ tq_status tq_decode_mse(const float* A, const uint8_t* k_plane, const uint16_t* 
                         float scale, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Fused decode over a TurboQuant_prod KEY cache and an MSE-quantized VALUE cache
+ * ("Implementing TurboQuant on NVIDIA's AGX Thor", zededa.com, "The Optimization
+ * Journey", v2 kernel 3 and v6 "Fused hybrid Triton kernel": per compressed block
+ * the TQ score, the value dequantization and the accumulation, with online softmax):
+ *
+ *   s[b,i] = scale * (<A_b, kcb[kidx_i]> + (sqrt(pi/2)/D) gamma_i <T_b, sigma_i>)
+ *            (the raw score of tq_scores_packed, times scale)
+ *   p[b,:] = softmax(s[b,:])
+ *   out[b] = Pi_v^T sum_i p[b,i] nv_i vcb[vidx_i]
+ *
+ * A, T: [P,B,D] fp32 from tq_prepare_queries.  Keys in the tq_scores_packed format:
+ * k_plane [P,S,D*k_bits/8], k_sign_plane [P,S,D/8], k_gamma [P,S] fp16, codebook
+ * k_codebook of 2^k_bits fp32 centroids.  Values, Pi_v, out, scale, workspace and
+ * errors as for tq_decode_mse (the same workspace size).  D == 128, k_bits and v_bits
+ * in {1,2,3}.  fp32 arithmetic.
+ * ---------------------------------------------------------------------- */
+tq_status tq_decode_prod(const float* A, const float* T, const uint8_t* k_plane,
+                         const uint8_t* k_sign_plane, const uint16_t* k_gamma,
+                         const float* k_codebook, int k_bits, const uint8_t* v_plane,
+                         const uint16_t* v_norm, const float* v_codebook, int v_bits,
+                         const float* Pi_v, float* out, int P, int H, int B, int S, int D,
+                         float scale, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
  * Fused query transform + scoring: the challenge's `solve` without its
  * per-call cudaMalloc/cudaFree (riteshyadav.xyz, "What the rearrangement
  * saves": its solve "allocates temporary arrays on every call").  The caller
@@ -287,7 +324,9 @@ tq_status tq_haar_rotation(const double* G, int D, float* Pi);
  * TQ_ERR_WORKSPACE and launch nothing.
  * The first call on each device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream
- * capture.  Nothing in the array needs to start at zero (the transform writes
+ * capture.  The looked-up address is kept for the life of the process, so do not
+ * call this entry point on a device after cudaDeviceReset on it (the reset unloads
+ * the array and the kept address would be stale).  Nothing in the array needs to start at zero (the transform writes
  * all of A and T before scoring reads them).  All calls on one device share the
  * array: calls that may overlap on the GPU (other streams, other host threads)
  * race on it and must be serialised by the caller.

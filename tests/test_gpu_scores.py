@@ -229,8 +229,9 @@ def test_c4_prefill_fp32_path_sampled(tq):
 
 
 def test_fused_solve_many_keys_per_thread(tq):
-    """One problem with far more keys than the fused kernel's threads: every thread walks
-    several keys of its CTA's range (two in flight), S is ragged, queries are bf16."""
+    """One problem with far more keys than the fused kernel's threads: each CTA's range
+    spans several key tiles, so its two-stage ring of tiles is refilled; S is ragged and
+    the queries are bf16."""
     c = Case(1, 1, 2, 400_001, 128, 3, seed=91, gamma_dtype="f16", q_dtype="bf16")
     ip, sp = c.packed()
     out = tq.solve_packed(q_tensor(c), dev(ip), dev(sp), f16(c.gamma), dev(c.Pi), dev(c.S_mat), dev(c.cb),
@@ -241,9 +242,8 @@ def test_fused_solve_many_keys_per_thread(tq):
 
 @pytest.mark.parametrize("bits,S", [(2, 172_801), (3, 161_281)])
 def test_fused_solve_staged_range_two_keys_per_thread(tq, bits, S):
-    """Key ranges that the fused kernel stages in shared memory (up to 48 KB a CTA) yet
-    that hold more keys than its 512 threads: some threads score two staged keys.  The
-    last range is ragged."""
+    """Key ranges of one to three tiles of the fused kernel's ring (a tile holds one key
+    per thread), so some threads score keys of two tiles; the last range is ragged."""
     c = Case(1, 1, 2, S, 128, bits, seed=93 + bits, gamma_dtype="f16")
     ip, sp = c.packed()
     out = tq.solve_packed(q_tensor(c), dev(ip), dev(sp), f16(c.gamma), dev(c.Pi), dev(c.S_mat), dev(c.cb),
@@ -348,3 +348,12 @@ def test_device_errors_raise(tq):
     with pytest.raises(tq.TQError, match="WORKSPACE"):
         tq.solve(dev(c.Q[0]), dev(c.idx[0]), dev(c.signs[0]), dev(c.gamma[0]), dev(c.Pi[0]),
                  dev(c.S_mat[0]), dev(c.cb), workspace=ws)
+
+
+@pytest.mark.gpu
+def test_no_bounded_wait_ran_out(tq):
+    """Every bounded wait of the kernels above completed: no fault bit is set (reading clears them)."""
+    tq.device_faults()
+    test_c2_single_query_decode(tq)
+    torch.cuda.synchronize()
+    assert tq.device_faults() == 0

@@ -5,8 +5,10 @@ library instead of a caller workspace.
 
 Checked through the C ABI against tq_solve_packed (the workspace entry point) on two
 calls in a row with different shapes, so the second call runs on scratch that still
-holds the first call's data; plus the size limit.  This file is collected last so that
-a run stopping at its first failure has already run every other test."""
+holds the first call's data; under AUTO against the CPU oracle, including the
+tensor-core path whose bf16 query operand also sits in the scratch; plus the size
+limit.  This file is collected last so that a run stopping at its first failure has
+already run every other test."""
 import ctypes
 
 import numpy as np
@@ -33,7 +35,7 @@ def _dev(x):
     return torch.from_numpy(np.ascontiguousarray(x)).cuda()
 
 
-def _run_both(tq, c):
+def _run_both(tq, c, path=1):
     ip, sp = c.packed()
     Q, idx, sg = _dev(c.Q), _dev(ip), _dev(sp)
     gamma = _dev(c.gamma.astype(np.float16))
@@ -43,14 +45,14 @@ def _run_both(tq, c):
     L = tq.lib()
     st = L.tq_solve_packed_noalloc(Q.data_ptr(), 0, idx.data_ptr(), sg.data_ptr(), gamma.data_ptr(),
                                    Pi.data_ptr(), Sm.data_ptr(), cb.data_ptr(), out_new.data_ptr(),
-                                   c.P, c.H, c.B, c.S, c.D, c.bits, 1, stream)
+                                   c.P, c.H, c.B, c.S, c.D, c.bits, path, stream)
     assert st == 0, tq.status_string(st)
     out_ref = torch.empty_like(out_new)
     ws = torch.empty(tq.workspace_bytes(c.P, c.B, c.D), dtype=torch.uint8, device="cuda")
     st = L.tq_solve_packed(Q.data_ptr(), 0, idx.data_ptr(), sg.data_ptr(), gamma.data_ptr(),
                            Pi.data_ptr(), Sm.data_ptr(), cb.data_ptr(), out_ref.data_ptr(),
                            c.P, c.H, c.B, c.S, c.D, c.bits, ctypes.c_void_p(ws.data_ptr()), ws.numel(),
-                           1, stream)
+                           path, stream)
     assert st == 0, tq.status_string(st)
     torch.cuda.synchronize()
     return out_new.cpu().numpy().astype(np.float64), out_ref.cpu().numpy().astype(np.float64)
@@ -66,6 +68,29 @@ def test_noalloc_matches_workspace_entry_on_two_calls(tq):
         assert np.isfinite(new).all()
         err = np.abs(new - ref)
         assert (err <= 1e-5 * (1.0 + np.abs(ref))).all(), err.max()
+
+
+def test_noalloc_auto_path_against_the_oracle(tq):
+    """Under AUTO: 16 and 40 queries take the tensor cores, whose bf16 query operand also
+    lives in the fixed scratch after A and T; 3 queries take the single fused fp32 kernel,
+    which leaves the scratch untouched.  Each call is checked against the CPU oracle at its
+    path's bound and against the workspace entry point, two calls in a row per shape."""
+    # gamma is stored as fp16 (the packed layout), so the oracle takes the same fp16 values
+    for case, bf16 in ((Case(2, 2, 16, 2000, 128, 2, seed=63, gamma_dtype="f16"), True),
+                       (Case(3, 1, 40, 700, 128, 3, seed=64, random_codebook=True, gamma_dtype="f16"), True),
+                       (Case(1, 1, 3, 5000, 128, 2, seed=65, gamma_dtype="f16"), False)):
+        want = case.expected()
+        for _ in range(2):
+            new, ref = _run_both(tq, case, path=0)
+            assert np.isfinite(new).all()
+            err = np.abs(new - want)
+            if bf16:
+                bound = 2e-3 * case.qnorm()[:, :, None]
+                assert (err <= bound).all(), err.max()
+                assert np.array_equal(new, ref)       # same kernels, same operand layout
+            else:
+                assert (err <= 1e-5 * (1.0 + np.abs(want))).all(), err.max()
+                assert np.array_equal(new, ref)
 
 
 def test_noalloc_rejects_work_beyond_the_fixed_scratch(tq):

@@ -91,6 +91,8 @@ def key_bytes(w) -> int:
         return w.D * w.mse_bits // 8 + (4 if w.gamma_dtype == "f32" else 2)
     if w.layout == "decode":              # the key's and the value's code plane + norm
         return 2 * (w.D * w.mse_bits // 8 + 2)
+    if w.layout == "decode_prod":         # product key (codes, signs, gamma) + value (codes, norm)
+        return w.D * w.mse_bits // 8 + w.D // 8 + 2 + w.D * w.v_bits // 8 + 2
     return w.D * w.mse_bits // 8 + w.D // 8 + (4 if w.gamma_dtype == "f32" else 2)
 
 
@@ -100,6 +102,10 @@ def score_kernel_bytes(w) -> int:
     if w.layout == "decode":
         # cache once, A and the outputs once, Pi_v once, both codebooks
         return (w.P * w.S * key_bytes(w) + 2 * 4 * w.P * w.B * w.D + 4 * w.H * w.D * w.D + 8 * w.C)
+    if w.layout == "decode_prod":
+        # cache once, A, T and the outputs once, Pi_v once, both codebooks
+        return (w.P * w.S * key_bytes(w) + 3 * 4 * w.P * w.B * w.D + 4 * w.H * w.D * w.D
+                + 4 * w.C + 4 * (1 << w.v_bits))
     n_at = 1 if w.layout == "mse" else 2
     return (w.P * w.S * key_bytes(w) + 4 * w.P * w.B * w.S + n_at * 4 * w.P * w.B * w.D + 4 * w.C)
 
@@ -154,6 +160,8 @@ KERNEL_SOURCES = {
 def kernel_family(w, path) -> str:
     if w.layout in ("mse", "decode"):
         return w.layout
+    if w.layout == "decode_prod":
+        return "decode"
     return "mma" if path == "bf16_mma" else "simt"
 
 
@@ -294,11 +302,29 @@ def build_device_workload(w, tq, torch, dev):
     else:
         cache["idx"] = tq.pack_indices(idx, w.mse_bits)
         cache["signs"] = tq.pack_signs(sg)
+        if w.layout == "decode_prod":
+            # unit values of their own, with their own rotation per head and codebook
+            vcb = torch.from_numpy(tq.lloyd_max_codebook(w.D, w.v_bits)).to(dev)
+            Pi_v = torch.from_numpy(np.stack([tq.haar_rotation(synth.rotation_seed_matrix(w.seed + 1, h, w.D))
+                                              for h in range(w.H)])).to(dev)
+            vidx = torch.empty((w.P, w.S, w.D), dtype=torch.uint8, device=dev)
+            for p in range(w.P):
+                vals = torch.from_numpy(synth.unit_keys(w.seed + 1, p, 0, w.S, w.D).astype(np.float32)).to(dev)
+                vidx[p].copy_(tq.compress_keys(vals, Pi_v[p % w.H], S_mat[p % w.H], vcb, gdt)[0])
+            cache.update({"vidx": tq.pack_indices(vidx, w.v_bits), "Pi_v": Pi_v, "vcb": vcb,
+                          "vnorm": torch.ones((w.P, w.S), dtype=torch.float16, device=dev),
+                          "dout": torch.empty((w.P, w.B, w.D), device=dev),
+                          "dws": torch.empty(max(16, int(tq.lib().tq_decode_workspace_bytes(w.P, w.B, w.S, w.D))),
+                                             dtype=torch.uint8, device=dev)})
     torch.cuda.synchronize(dev)
     return Q, Pi, S_mat, cb, cache
 
 
 def score_call(tq, w, path, A, T, cache, cb, out):
+    if w.layout == "decode_prod":
+        return tq.decode_prod(A, T, cache["idx"], cache["signs"], cache["gamma"], cb, w.mse_bits, cache["vidx"],
+                              cache["vnorm"], cache["vcb"], w.v_bits, cache["Pi_v"], workspace=cache["dws"],
+                              out=cache["dout"])
     if w.layout == "decode":
         return tq.decode_mse(A, cache["idx"], cache["norm"], cb, w.mse_bits, cache["vidx"], cache["vnorm"], cb,
                              w.mse_bits, cache["Pi_v"], workspace=cache["dws"], out=cache["dout"])
@@ -338,6 +364,15 @@ def oracle_sample(w, n_keys):
             return oracle.scores_mse(A, idx, nrm, cb, norm_correction=True)
         return run
     idx, sg, gamma = oracle.compress_prod(keys, Pi, S_mat, cb, w.gamma_dtype)
+    if w.layout == "decode_prod":
+        vcb = oracle.lloyd_max_sphere(w.D, w.v_bits)[0].astype(np.float32)
+        Pi_v = oracle.haar_rotation(synth.rotation_seed_matrix(w.seed + 1, 0, w.D)).astype(np.float32)
+        vi, vn = oracle.compress_mse(synth.unit_keys(w.seed + 1, 0, 0, n_keys, w.D), Pi_v, vcb)
+
+        def run_decode_prod():
+            A, T = oracle.prepare_queries(Q, Pi, S_mat)
+            return oracle.decode_prod(A, T, idx, sg, gamma, cb, vi, vn, vcb, Pi_v, 1.0 / np.sqrt(w.D))
+        return run_decode_prod
     return lambda: oracle.scores_from_queries(Q, Pi, S_mat, idx, sg, gamma, cb)
 
 
@@ -551,6 +586,9 @@ def main():
         if w.layout in ("mse", "decode"):
             tq.prepare_queries(cp["Q"], Pi, Pi, out=(cp["A"], cp["T"]))
             score_call(tq, w, path, cp["A"], cp["T"], cp["cache"], cb, cp["out"])
+        elif w.layout == "decode_prod":
+            tq.prepare_queries(cp["Q"], Pi, S_mat, out=(cp["A"], cp["T"]))
+            score_call(tq, w, path, cp["A"], cp["T"], cp["cache"], cb, cp["out"])
         elif w.layout == "unpacked":
             tq.solve(cp["Q"], cp["cache"]["idx"], cp["cache"]["signs"], cp["cache"]["gamma"], Pi, S_mat, cb,
                      path=path, workspace=cp["ws"], out=cp["out"])
@@ -687,7 +725,7 @@ def main():
         hcache = {k: v.cpu().pin_memory() for k, v in cache0.items() if k not in scratch}
         hPi, hS, hcb = Pi.cpu().pin_memory(), S_mat.cpu().pin_memory(), cb.cpu().pin_memory()
         mse = w.layout in ("mse", "decode")   # no S_mat: the MSE-only paths need Pi alone
-        out_shape = (w.P, w.B, w.D) if w.layout == "decode" else (w.P, w.B, w.S)
+        out_shape = (w.P, w.B, w.D) if w.layout in ("decode", "decode_prod") else (w.P, w.B, w.S)
         h2d = (hostQ.numel() * hostQ.element_size() + sum(v.numel() * v.element_size() for v in hcache.values())
                + (hPi.numel() + (0 if mse else hS.numel()) + hcb.numel()) * 4)
         d2h = int(np.prod(out_shape)) * 4
@@ -713,8 +751,8 @@ def main():
                     eb["S"].copy_(hS, non_blocking=True)
                 eb["cb"].copy_(hcb, non_blocking=True)
                 dc, dA, dT, dout = eb["cache"], eb["A"], eb["T"], eb["out"]
-                if w.layout == "decode":
-                    tq.prepare_queries(eb["Q"], eb["Pi"], eb["Pi"], out=(dA, dT))
+                if w.layout in ("decode", "decode_prod"):
+                    tq.prepare_queries(eb["Q"], eb["Pi"], eb["Pi"] if mse else eb["S"], out=(dA, dT))
                     score_call(tq, w, path, dA, dT, dc, eb["cb"], None)
                     eb["hout"].copy_(dc["dout"], non_blocking=True)
                     return
@@ -778,7 +816,8 @@ def main():
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": ("fused transform+scoring kernel" if fused_single else
-                                "decode split + combine kernels" if w.layout == "decode" else "scoring kernel"),
+                                "decode split + combine kernels" if w.layout in ("decode", "decode_prod")
+                                else "scoring kernel"),
                      "kernel_ms": kernel_ms, "bytes_per_launch": kbytes,
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback 6.8 TB/s",
                      "timing": ktiming, "kernel_fingerprint": fp},
@@ -787,7 +826,7 @@ def main():
                          "min_ms": min(regions), "max_ms": max(regions)},
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": (1 if fused_single else (3 if w.layout == "decode" else 2)) * args.steps,
+        "gpu_launches": (1 if fused_single else (3 if w.layout in ("decode", "decode_prod") else 2)) * args.steps,
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)

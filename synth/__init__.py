@@ -64,9 +64,12 @@ class Workload:
     mse_bits: int
     layout: str          # "unpacked" (uint8 idx + int8 signs), "packed" (bit planes) or
                          # "mse" (code plane + fp16 norm, the MSE-only variant, no signs) or
-                         # "decode" (MSE keys and MSE values, for the fused decode)
+                         # "decode" (MSE keys and MSE values, for the fused decode) or
+                         # "decode_prod" (TurboQuant_prod keys and MSE values)
     gamma_dtype: str     # "f32" or "f16" (for "mse": the dtype of the stored norm)
     q_dtype: str         # "f32" or "bf16"
+    v_bits: int = 0      # "decode_prod": bits of the MSE value codes (the keys are a
+                         # TurboQuant_prod cache: mse_bits-bit codes + sign plane + fp16 gamma)
 
     @property
     def C(self) -> int:
@@ -99,6 +102,10 @@ WORKLOADS = {
     # Fused decode (softmax and values) over MSE keys and values, 3-bit codes each.
     "d1": Workload("d1_fused_decode_B1_S131072_k3v3", 1006, 1, 1, 1, 131072, 128, 3,
                    "decode", "f16", "f32"),
+    # Fused decode over the product key cache of c2 (2-bit codes + sign + fp16 gamma: the
+    # 3-bit keys of the decode page) and 3-bit MSE values.
+    "d2": Workload("d2_prod_decode_B1_S131072_k3v3", 1007, 1, 1, 1, 131072, 128, 2,
+                   "decode_prod", "f16", "f32", v_bits=3),
 }
 
 

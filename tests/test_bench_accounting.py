@@ -18,7 +18,7 @@ W = synth.WORKLOADS
 
 
 @pytest.mark.parametrize("key,per_key", [("c0", 260), ("c1", 260), ("c2", 50), ("c3", 50), ("c4", 66),
-                                         ("m1", 50), ("d1", 100)])
+                                         ("m1", 50), ("d1", 100), ("d2", 100)])
 def test_bytes_per_key(key, per_key):
     assert bench.key_bytes(W[key]) == per_key
 
@@ -45,6 +45,10 @@ def test_mse_and_decode_launch_bytes():
     d1 = 131072 * 100 + 2 * 4 * 128 + 4 * 128 * 128 + 8 * 8  # A and the output, Pi_v, two codebooks
     assert bench.score_kernel_bytes(W["m1"]) == m1
     assert bench.score_kernel_bytes(W["d1"]) == d1
+    # the product-key decode: 2-bit codes + signs + gamma (50 B) and 3-bit values + norm
+    # (50 B) a key; A, T and the output; Pi_v; a 4- and an 8-entry codebook
+    d2 = 131072 * 100 + 3 * 4 * 128 + 4 * 128 * 128 + 4 * 4 + 4 * 8
+    assert bench.score_kernel_bytes(W["d2"]) == d2
 
 
 def test_fused_kernel_also_reads_queries_and_rotations():

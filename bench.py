@@ -419,6 +419,10 @@ def run_reference(args, w):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
+    if w.layout == "compress":
+        print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the scoring path; "
+                          "the compressor's CPU baseline is in the cpu_baseline of its own line"}), flush=True)
+        return
     n_keys = min(w.S, 4096)
     run = oracle_sample(w, n_keys)
     for _ in range(args.warmup):
@@ -514,6 +518,141 @@ def run_s_sweep(args, w, tq, torch, dev, path):
     print(json.dumps({"sweep": w.name, "path": path, "peak_gbs": peak, "rows": rows, "fit": fit}), flush=True)
 
 
+def fma_peak_tflops():
+    """fp32 FMA-pipe peak: 152 SMs x 128 FMA lanes x 2 FLOP x the maximum SM clock
+    (MEASURED_PEAKS.json sm_max_mhz, else 2070 MHz)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            mhz = float(json.load(f)["sm_max_mhz"])
+    except (OSError, KeyError, ValueError):
+        mhz = 2070.0
+    return 152 * 128 * 2 * mhz * 1e6 / 1e12
+
+
+def run_compress(args, w, tq, torch, dev):
+    """The write side: tq_compress_keys_packed over P x S fp32 keys (rotating copies larger
+    than twice the L2), timed like the scoring steps; one JSON line."""
+    cb = torch.from_numpy(tq.lloyd_max_codebook(w.D, w.mse_bits)).to(dev)
+    Pi = torch.from_numpy(np.stack([tq.haar_rotation(synth.rotation_seed_matrix(w.seed, h, w.D))
+                                    for h in range(w.H)])).to(dev)
+    S_mat = torch.from_numpy(np.stack([synth.s_matrix(w.seed, h, w.D) for h in range(w.H)])).to(dev)
+    keys0 = torch.from_numpy(np.stack([synth.unit_keys(w.seed, p, 0, w.S, w.D) for p in range(w.P)])
+                             .astype(np.float32)).to(dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    key_b = 4 * w.D
+    out_b = w.D * w.mse_bits // 8 + w.D // 8 + 2
+    per_copy = w.P * w.S * (key_b + out_b)
+    R = max(2, min(64, math.ceil(2.2 * l2 / per_copy)))
+    copies = [{"k": keys0.clone(), "out": (torch.empty((w.P, w.S, w.D * w.mse_bits // 8), dtype=torch.uint8, device=dev),
+                                           torch.empty((w.P, w.S, w.D // 8), dtype=torch.uint8, device=dev),
+                                           torch.empty((w.P, w.S), dtype=torch.float16, device=dev))}
+              for _ in range(R)]
+    stream = torch.cuda.Stream(dev)
+
+    def call(cp):
+        tq.compress_keys_packed(cp["k"], Pi, S_mat, cb, w.mse_bits, out=cp["out"])
+    with torch.cuda.stream(stream):
+        for cp in copies:
+            call(cp)
+    torch.cuda.synchronize(dev)
+    G = 8
+    graphs = []
+    for b in range(R):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for j in range(G):
+                call(copies[(b + j) % R])
+        graphs.append(g)
+    clocks = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
+    with torch.cuda.stream(stream):
+        for k in range(args.warmup):
+            graphs[k % R].replay()
+    torch.cuda.synchronize(dev)
+    steps = -(-args.steps // G) * G
+
+    def region():
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record()
+            for k in range(steps // G):
+                graphs[k % R].replay()
+            e1.record()
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1)
+    t0 = time.time()
+    regions = [region()]
+    n_rep = int(min(200, max(5, math.ceil(500.0 / max(regions[0], 1e-3)))))
+    while len(regions) < n_rep:
+        regions.append(region())
+    t1 = time.time()
+    clk = clocks.stop((t0, t1))
+    ms = statistics.median(regions) / steps
+    nkeys = w.P * w.S
+    flops = 3 * 2 * w.D * w.D * nkeys                  # three D x D products per key
+    achieved = flops / (ms / 1e3) / 1e12
+    peak = fma_peak_tflops()
+    # end to end: keys in from pinned host memory, the packed cache out, two streams
+    hk = keys0.cpu().pin_memory()
+    e_streams = [stream, torch.cuda.Stream(dev)]
+    e_bufs = [{"k": torch.empty_like(keys0), "out": copies[i]["out"],
+               "h": tuple(torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in copies[i]["out"])}
+              for i in range(2)]
+
+    def e2e_run(n):
+        es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        es.record(e_streams[0])
+        e_streams[1].wait_event(es)
+        for k in range(n):
+            eb = e_bufs[k % 2]
+            with torch.cuda.stream(e_streams[k % 2]):
+                eb["k"].copy_(hk, non_blocking=True)
+                tq.compress_keys_packed(eb["k"], Pi, S_mat, cb, w.mse_bits, out=eb["out"])
+                for h_, d_ in zip(eb["h"], eb["out"]):
+                    h_.copy_(d_, non_blocking=True)
+        e_streams[0].wait_stream(e_streams[1])
+        ee.record(e_streams[0])
+        return es, ee
+    e2e_run(args.warmup)
+    torch.cuda.synchronize(dev)
+    n_e = max(3, min(args.steps, 50))
+    es, ee = e2e_run(n_e)
+    torch.cuda.synchronize(dev)
+    e_ms = es.elapsed_time(ee)
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+        n = min(w.S, 2048)
+        k_np = synth.unit_keys(w.seed, 0, 0, n, w.D)
+        cb_np, Pi_np, S_np = cb.cpu().numpy(), Pi[0].cpu().numpy(), S_mat[0].cpu().numpy()
+        t_0, reps = time.perf_counter(), 0
+        while time.perf_counter() - t_0 < args.cpu_seconds:
+            oracle.compress_prod(k_np, Pi_np, S_np, cb_np, "f16")
+            reps += 1
+        el = time.perf_counter() - t_0
+        cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+        cpu = {"value": reps * n / el, "unit": "keys/s", "cores": cores, "kind": "oracle",
+               "hardware_concurrency": os.cpu_count(),
+               "sample": f"{reps} x compress_prod of {n} keys, {el:.1f} s, float64 NumPy"}
+    line = {"metric": "compressed keys/s (fp32 keys in, packed TurboQuant_prod cache out) at 1 GB300",
+            "value": nkeys / (ms / 1e3), "unit": "keys/s", "n_gpus": 1, "steps": steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "P": w.P, "H": w.H, "S": w.S, "D": w.D, "idx_bits": w.mse_bits,
+                       "l2": f"{R} rotating key/output copies, {R * per_copy / 1e6:.0f} MB > 2x L2"},
+            "key_gbs": nkeys * key_b / (ms / 1e3) / 1e9,
+            "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "traffic": None, "kernel": "compress_tile_kernel",
+                         "kernel_ms": ms, "flops_per_launch": flops,
+                         "peak_source": "152 SMs x 128 fp32 FMA lanes x 2 FLOP x max SM clock"},
+            "timed_region": {"repeats": len(regions), "median_ms": statistics.median(regions)},
+            "cpu_baseline": cpu,
+            "e2e": {"value": nkeys * n_e / (e_ms / 1e3), "unit": "keys/s",
+                    "h2d_bytes_per_step": nkeys * key_b, "d2h_bytes_per_step": nkeys * out_b,
+                    "steps": n_e, "streams": 2},
+            "gpu_launches": steps, "clocks": clk}
+    print(json.dumps(line), flush=True)
+
+
 def dataclasses_replace(w, **kw):
     import dataclasses
     return dataclasses.replace(w, **kw)
@@ -553,6 +692,9 @@ def main():
     path = args.path if args.path != "auto" else tq.auto_path(w.B, w.D)
     if args.s_sweep:
         run_s_sweep(args, w, tq, torch, dev, path)
+        return
+    if w.layout == "compress":
+        run_compress(args, w, tq, torch, dev)
         return
     Q0, Pi, S_mat, cb, cache0 = build_device_workload(w, tq, torch, dev)
 

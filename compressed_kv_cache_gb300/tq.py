@@ -58,6 +58,7 @@ _SIGNATURES = {
     "tq_pack_signs": ([_P, _P, _L, _I, _P], _I),
     "tq_unpack_signs": ([_P, _P, _L, _I, _P], _I),
     "tq_compress_keys": ([_P, _P, _P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _P], _I),
+    "tq_compress_keys_packed": ([_P, _P, _P, _P, _I, _P, _P, _P, _I, _I, _I, _I, _P], _I),
     "tq_lloyd_max_codebook": ([_I, _I, _I, _I, _P], _I),
     "tq_haar_rotation": ([_P, _I, _P], _I),
     "tq_solve_packed_noalloc": ([_P, _I, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P], _I),
@@ -421,3 +422,23 @@ def compress_keys(keys, Pi, S_mat, codebook, gamma_dtype=torch.float32):
         codebook.numel(), _dev(K_idx, "K_idx", (torch.uint8,)), _dev(signs, "signs", (torch.int8,)),
         g32, g16, P, H, S, D, _stream()))
     return K_idx, signs, gamma
+
+
+def compress_keys_packed(keys, Pi, S_mat, codebook, idx_bits, out=None):
+    """TurboQuant_prod compression on the GPU straight into the packed cache.  keys fp32
+    [P,S,D] (or [S,D]); Pi, S_mat [H,D,D] (or [D,D]); codebook 2^idx_bits fp32.  Returns
+    (idx_plane uint8 [..,S,D*idx_bits/8], sign_plane uint8 [..,S,D/8], gamma fp16 [..,S])."""
+    P, S, D = _as3(keys)
+    H = 1 if Pi.dim() == 2 else Pi.shape[0]
+    lead = keys.shape[:-1]
+    if out is None:
+        out = (torch.empty(lead + (D * idx_bits // 8,), device=keys.device, dtype=torch.uint8),
+               torch.empty(lead + (D // 8,), device=keys.device, dtype=torch.uint8),
+               torch.empty(lead, device=keys.device, dtype=torch.float16))
+    ip, sp, g = out
+    _check("tq_compress_keys_packed", lib().tq_compress_keys_packed(
+        _dev(keys, "keys", (torch.float32,)), _dev(Pi, "Pi", (torch.float32,)),
+        _dev(S_mat, "S_mat", (torch.float32,)), _dev(codebook, "codebook", (torch.float32,)), idx_bits,
+        _dev(ip, "idx_plane", (torch.uint8,)), _dev(sp, "sign_plane", (torch.uint8,)),
+        _dev(g, "gamma", (torch.float16,)), P, H, S, D, _stream()))
+    return ip, sp, g

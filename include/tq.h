@@ -283,9 +283,16 @@ tq_status tq_unpack_signs(const uint8_t* sign_plane, int8_t* signs, int64_t n_ke
  * S_mat: [H,D,D]; codebook: [C] fp32 sorted ascending; outputs K_idx [P,S,D]
  * uint8, signs [P,S,D] int8 and exactly one of gamma_f32 / gamma_f16 [P,S]
  * (the other NULL).  Computed in fp32: a coordinate within ~1e-6 of a cell
- * edge may fall on either side.  D % 32 == 0, D <= 128, C <= 256.  Keys are
- * taken as unit length (the score has no key-norm term).  Pack the outputs
- * with tq_pack_indices / tq_pack_signs for the packed layout.
+ * edge may fall on either side.  D % 32 == 0, 32 <= D <= 256, C <= 256.  Keys
+ * are taken as unit length (the score has no key-norm term).
+ *
+ * tq_compress_keys_packed (device): the same compression in one pass that
+ * writes the packed cache of tq_scores_packed directly (kanthi.in §8 "Kernel
+ * checklist": rotate, search the midpoints, pack the bits and write the norm in
+ * the store kernel): idx_plane [P,S,D*idx_bits/8], sign_plane [P,S,D/8],
+ * gamma_f16 [P,S], codebook of 2^idx_bits centroids sorted ascending.
+ * D % 32 == 0, 32 <= D <= 256, idx_bits in {1,2,3}.  Errors: TQ_ERR_INVALID_VALUE,
+ * TQ_ERR_MISALIGNED, TQ_ERR_UNSUPPORTED (D % 32 != 0), TQ_ERR_LAUNCH.
  *
  * tq_lloyd_max_codebook (HOST pointer out): the 2^mse_bits Lloyd-Max centroids
  * of one coordinate of a uniform unit vector in R^D, density proportional to
@@ -301,6 +308,10 @@ tq_status tq_compress_keys(const float* keys, const float* Pi, const float* S_ma
                            const float* codebook, int C, uint8_t* K_idx, int8_t* signs,
                            float* gamma_f32, uint16_t* gamma_f16, int P, int H, int S, int D,
                            cudaStream_t stream);
+tq_status tq_compress_keys_packed(const float* keys, const float* Pi, const float* S_mat,
+                                  const float* codebook, int idx_bits, uint8_t* idx_plane,
+                                  uint8_t* sign_plane, uint16_t* gamma_f16, int P, int H, int S, int D,
+                                  cudaStream_t stream);
 tq_status tq_lloyd_max_codebook(int D, int mse_bits, int grid_points, int iterations,
                                 float* centroids);
 tq_status tq_haar_rotation(const double* G, int D, float* Pi);

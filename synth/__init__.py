@@ -65,7 +65,8 @@ class Workload:
     layout: str          # "unpacked" (uint8 idx + int8 signs), "packed" (bit planes) or
                          # "mse" (code plane + fp16 norm, the MSE-only variant, no signs) or
                          # "decode" (MSE keys and MSE values, for the fused decode) or
-                         # "decode_prod" (TurboQuant_prod keys and MSE values)
+                         # "decode_prod" (TurboQuant_prod keys and MSE values) or
+                         # "compress" (the write side: fp32 keys in, the packed cache out)
     gamma_dtype: str     # "f32" or "f16" (for "mse": the dtype of the stored norm)
     q_dtype: str         # "f32" or "bf16"
     v_bits: int = 0      # "decode_prod": bits of the MSE value codes (the keys are a
@@ -106,6 +107,9 @@ WORKLOADS = {
     # 3-bit keys of the decode page) and 3-bit MSE values.
     "d2": Workload("d2_prod_decode_B1_S131072_k3v3", 1007, 1, 1, 1, 131072, 128, 2,
                    "decode_prod", "f16", "f32", v_bits=3),
+    # The GPU compressor: 32768 unit fp32 keys of D = 128 into the packed 3-bit cache of c2.
+    "k1": Workload("k1_compress_S32768_D128_packed3bit", 1008, 1, 1, 1, 32768, 128, 2,
+                   "compress", "f16", "f32"),
 }
 
 

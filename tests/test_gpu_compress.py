@@ -24,18 +24,45 @@ def tq():
     return mod
 
 
-@pytest.mark.parametrize("P,H,S,D,bits,gdt", [(1, 1, 4096, 128, 2, "f32"), (4, 2, 777, 128, 3, "f16"),
-                                              (2, 2, 300, 64, 1, "f32"), (1, 1, 129, 32, 2, "f16")])
-def test_compress_matches_oracle(tq, P, H, S, D, bits, gdt):
+CASES = [(1, 1, 4096, 128, 2, "f32"), (4, 2, 777, 128, 3, "f16"), (2, 2, 300, 64, 1, "f32"),
+         (1, 1, 129, 32, 2, "f16"), (2, 1, 333, 256, 2, "f16"), (1, 1, 100, 160, 3, "f32"),
+         (3, 3, 65, 96, 2, "f16")]
+
+
+def _inputs(P, H, S, D, bits):
     seed = 900 + D + bits
     cb = codebook_for(D, bits)
     Pi = np.stack([rotation(seed, h, D) for h in range(H)])
     Sm = np.stack([synth.s_matrix(seed, h, D) for h in range(H)])
     keys = np.stack([synth.unit_keys(seed, p, 0, S, D) for p in range(P)]).astype(np.float32)
+    return cb, Pi, Sm, keys
+
+
+@pytest.mark.parametrize("P,H,S,D,bits,gdt", CASES)
+def test_compress_matches_oracle(tq, P, H, S, D, bits, gdt):
+    cb, Pi, Sm, keys = _inputs(P, H, S, D, bits)
     gd = torch.float32 if gdt == "f32" else torch.float16
     gi, gs, gg = tq.compress_keys(torch.from_numpy(keys).cuda(), torch.from_numpy(Pi).cuda(),
                                   torch.from_numpy(Sm).cuda(), torch.from_numpy(cb).cuda(), gd)
     gi, gs, gg = gi.cpu().numpy(), gs.cpu().numpy(), gg.cpu().numpy().astype(np.float64)
+    _check_against_oracle(P, H, S, D, gdt, cb, Pi, Sm, keys, gi, gs, gg)
+
+
+@pytest.mark.parametrize("P,H,S,D,bits,gdt", [c for c in CASES if c[5] == "f16"] + [(1, 1, 4096, 128, 2, "f16"),
+                                                                                     (2, 1, 999, 128, 1, "f16")])
+def test_compress_packed_matches_oracle(tq, P, H, S, D, bits, gdt):
+    """The one-pass compressor writes the packed cache: unpacked with the oracle's
+    unpackers, its codes, signs and fp16 gamma pass the same tie-aware comparison."""
+    cb, Pi, Sm, keys = _inputs(P, H, S, D, bits)
+    ip, sp, g = tq.compress_keys_packed(torch.from_numpy(keys).cuda(), torch.from_numpy(Pi).cuda(),
+                                        torch.from_numpy(Sm).cuda(), torch.from_numpy(cb).cuda(), bits)
+    ip, sp = ip.cpu().numpy(), sp.cpu().numpy()
+    gi = np.stack([oracle.unpack_indices(ip[p], bits, D) for p in range(P)])
+    gs = np.stack([oracle.unpack_signs(sp[p], D) for p in range(P)])
+    _check_against_oracle(P, H, S, D, "f16", cb, Pi, Sm, keys, gi, gs, g.cpu().numpy().astype(np.float64))
+
+
+def _check_against_oracle(P, H, S, D, gdt, cb, Pi, Sm, keys, gi, gs, gg):
     edges = 0.5 * (cb[1:].astype(np.float64) + cb[:-1])
     n_tie_idx = n_tie_sign = 0
     for p in range(P):

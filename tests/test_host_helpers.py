@@ -54,7 +54,11 @@ def test_host_helper_argument_errors():
     assert L.tq_haar_rotation(None, 4, out.ctypes.data) == 1
     f = 0x100000
     assert L.tq_compress_keys(f, f, f, f, 4, f, f, f, f, 1, 1, 8, 128, None) == 1   # both gammas
-    assert L.tq_compress_keys(f, f, f, f, 4, f, f, f, None, 1, 1, 8, 160, None) == 2  # D > 128
+    assert L.tq_compress_keys(f, f, f, f, 4, f, f, f, None, 1, 1, 8, 100, None) == 2  # D % 32 != 0
+    assert L.tq_compress_keys(f, f, f, f, 4, f, f, f, None, 1, 1, 8, 288, None) == 1  # D > 256
+    assert L.tq_compress_keys_packed(f, f, f, f, 2, f, f, f, 1, 1, 8, 100, None) == 2
+    assert L.tq_compress_keys_packed(f, f, f, f, 4, f, f, f, 1, 1, 8, 128, None) == 1  # 4-bit codes
+    assert L.tq_compress_keys_packed(f, f, f, f, 2, f, f, None, 1, 1, 8, 128, None) == 1
 
 
 def test_hadamard_rotation_matches_oracle():

@@ -42,6 +42,10 @@ __all__ = [
     "scores_mse",
     "decode_mse",
     "decode_prod",
+    "outlier_channels",
+    "compress_split",
+    "prepare_queries_split",
+    "scores_split",
     "pack_indices",
     "unpack_indices",
     "pack_signs",
@@ -379,6 +383,64 @@ def decode_prod(A: np.ndarray, T: np.ndarray, k_idx: np.ndarray, k_signs: np.nda
     vc = np.asarray(v_codebook, dtype=np.float64)[np.asarray(v_idx, dtype=np.int64)]
     acc = (p * np.asarray(v_norm, dtype=np.float64)[np.newaxis, :]) @ vc
     return acc @ np.asarray(Pi_v, dtype=np.float64)
+
+
+# ---------------------------------------------------------------------------
+# Outlier split: two TurboQuant-MSE instances per head over disjoint channel sets
+# ---------------------------------------------------------------------------
+
+def outlier_channels(keys: np.ndarray, n_out: int) -> np.ndarray:
+    """The n_out channels with the largest mean |k| over ``keys`` ([KB] §7 "Fractional
+    bits and the outlier split": channels hot across the whole sequence are known ahead
+    of time; §11 picks the 32 channels with the largest mean |k|).  Returned in
+    increasing order; among equal means the lower channel index is taken first."""
+    k = np.asarray(keys, dtype=np.float64)
+    D = k.shape[1]
+    if not 0 < n_out < D:
+        raise ValueError("both channel sets must be non-empty")
+    mean_abs = np.mean(np.abs(k), axis=0)
+    ranked = sorted(range(D), key=lambda c: (-mean_abs[c], c))
+    return np.array(sorted(ranked[:n_out]), dtype=np.int64)
+
+
+def _regular_channels(channels: np.ndarray, D: int) -> np.ndarray:
+    mask = np.ones(D, dtype=bool)
+    mask[np.asarray(channels, dtype=np.int64)] = False
+    return np.nonzero(mask)[0]
+
+
+def compress_split(keys: np.ndarray, channels: np.ndarray, Pi_out: np.ndarray, Pi_reg: np.ndarray,
+                   cb_out: np.ndarray, cb_reg: np.ndarray):
+    """Fractional-bit compression ([KB] §7): the outlier channels of each key and the
+    remaining channels are two vectors, each compressed by its own TurboQuant-MSE
+    instance (:func:`compress_mse`) with its own rotation, codebook and norm; for 2.5
+    bits, 32 outlier channels at 3 bits and 96 at 2.  Returns
+    ``(idx_out, norm_out, idx_reg, norm_reg)``."""
+    k = np.asarray(keys, dtype=np.float64)
+    ch = np.asarray(channels, dtype=np.int64)
+    reg = _regular_channels(ch, k.shape[1])
+    io, no = compress_mse(k[:, ch], Pi_out, cb_out)
+    ir, nr = compress_mse(k[:, reg], Pi_reg, cb_reg)
+    return io, no, ir, nr
+
+
+def prepare_queries_split(Q: np.ndarray, channels: np.ndarray, Pi_out: np.ndarray, Pi_reg: np.ndarray):
+    """Each instance's rotated query: A_out = Pi_out q[outlier channels] and
+    A_reg = Pi_reg q[other channels] ([KB] §8: rotate the query once per instance)."""
+    q = np.asarray(Q, dtype=np.float64)
+    ch = np.asarray(channels, dtype=np.int64)
+    reg = _regular_channels(ch, q.shape[1])
+    return (q[:, ch] @ np.asarray(Pi_out, dtype=np.float64).T,
+            q[:, reg] @ np.asarray(Pi_reg, dtype=np.float64).T)
+
+
+def scores_split(A_out: np.ndarray, A_reg: np.ndarray, idx_out: np.ndarray, norm_out: np.ndarray,
+                 cb_out: np.ndarray, idx_reg: np.ndarray, norm_reg: np.ndarray,
+                 cb_reg: np.ndarray) -> np.ndarray:
+    """<q, k_hat> for the split cache: the sum of the two instances' MSE scores
+    (:func:`scores_mse` without norm correction), since the channel sets partition q
+    and k.  float64."""
+    return scores_mse(A_out, idx_out, norm_out, cb_out) + scores_mse(A_reg, idx_reg, norm_reg, cb_reg)
 
 
 # ---------------------------------------------------------------------------

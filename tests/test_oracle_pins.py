@@ -612,3 +612,84 @@ def test_prod_decode_special_cases():
     z = np.zeros_like(A)
     o0 = oracle.decode_prod(z, z, ki, ks, kg, kcb, vi, vn, vcb, Pv, 0.25)
     assert np.allclose(o0, np.broadcast_to(Vh.mean(axis=0), o0.shape), rtol=1e-12, atol=1e-12)
+
+
+def _split_case(S, D, n_out, seed, bo=3, br=2):
+    rng = np.random.default_rng(seed)
+    K = synth.unit_keys(seed, 0, 0, S, D) * rng.uniform(0.5, 3.0, (S, 1))
+    q = rng.standard_normal((3, D))
+    ch = oracle.outlier_channels(K, n_out)
+    Po = oracle.haar_rotation(rng.standard_normal((n_out, n_out))).astype(np.float32)
+    Pr = oracle.haar_rotation(rng.standard_normal((D - n_out, D - n_out))).astype(np.float32)
+    co = codebook(n_out, bo)[0].astype(np.float32)
+    cr = codebook(D - n_out, br)[0].astype(np.float32)
+    return K, q, ch, Po, Pr, co, cr
+
+
+def test_split_scores_equal_reconstruction():
+    """The split score equals <q, k_hat> with k_hat rebuilt in the original basis: the
+    outlier channels from norm_out Pi_out^T c_out(idx_out), the others from
+    norm_reg Pi_reg^T c_reg(idx_reg), one pair at a time."""
+    for S, D, n_out in ((40, 128, 32), (25, 64, 16)):
+        K, q, ch, Po, Pr, co, cr = _split_case(S, D, n_out, 301 + D)
+        io, no, ir, nr = oracle.compress_split(K, ch, Po, Pr, co, cr)
+        Ao, Ar = oracle.prepare_queries_split(q, ch, Po, Pr)
+        got = oracle.scores_split(Ao, Ar, io, no, co, ir, nr, cr)
+        reg = np.array([c for c in range(D) if c not in set(ch.tolist())])
+        for s in range(S):
+            kh = np.zeros(D)
+            kh[ch] = float(no[s]) * (co.astype(np.float64)[io[s].astype(np.int64)] @ Po.astype(np.float64))
+            kh[reg] = float(nr[s]) * (cr.astype(np.float64)[ir[s].astype(np.int64)] @ Pr.astype(np.float64))
+            for b in range(q.shape[0]):
+                assert got[b, s] == pytest.approx(float(np.dot(q[b], kh)), rel=1e-12, abs=1e-12)
+
+
+def test_split_storage_of_the_printed_split():
+    """The split kanthi.in §7 prints: 32 channels at 3 bits and 96 at 2.  Its codes take
+    (32*3 + 96*2)/128 = 2.25 bits a coordinate (the page writes 2.5 for that expression);
+    with the two fp16 norms a key of D = 128 takes 12 + 24 + 4 = 40 bytes, 2.5 bits a
+    coordinate in all."""
+    assert (32 * 3 + 96 * 2) / 128 == 2.25
+    K, q, ch, Po, Pr, co, cr = _split_case(8, 128, 32, 311)
+    io, no, ir, nr = oracle.compress_split(K, ch, Po, Pr, co, cr)
+    code_bytes = oracle.pack_indices(io, 3).shape[1] + oracle.pack_indices(ir, 2).shape[1]
+    assert code_bytes == 36
+    assert code_bytes + no.itemsize + nr.itemsize == 40 == 2.5 * 128 / 8
+
+
+def test_outlier_channels_pick_the_hot_channels():
+    """Keys with channels {3, 17, 64, 101} scaled x15 before normalisation: those four are
+    among the 32 picked.  With channel magnitudes strictly ordered by construction, the
+    pick is exactly the top of that order; equal means take the lower index."""
+    K = synth.unit_keys(1234, 0, 0, 2000, 128)
+    ch = oracle.outlier_channels(K, 32)
+    assert len(ch) == 32 and np.all(np.diff(ch) > 0)
+    assert {3, 17, 64, 101} <= set(ch.tolist())
+    scale = np.arange(1, 9, dtype=np.float64)[::-1]             # channel 0 hottest
+    Ks = np.ones((5, 8)) * scale
+    assert oracle.outlier_channels(Ks, 3).tolist() == [0, 1, 2]
+    assert oracle.outlier_channels(np.ones((4, 6)), 2).tolist() == [0, 1]
+
+
+def test_split_distortion_sits_between_the_uniform_widths():
+    """On keys with outlier channels, the reconstruction error of the 2.5-bit split lies
+    between uniform 2-bit and uniform 3-bit TurboQuant-MSE (kanthi.in §7: the extra bits
+    of the outlier instance are not worthless)."""
+    rng = np.random.default_rng(321)
+    S, D = 3000, 128
+    K = synth.unit_keys(321, 0, 0, S, D)
+    def err_uniform(bits):
+        P = oracle.haar_rotation(rng.standard_normal((D, D))).astype(np.float32)
+        cb = codebook(D, bits)[0].astype(np.float32)
+        idx, n = oracle.compress_mse(K, P, cb)
+        kh = n.astype(np.float64)[:, None] * (cb.astype(np.float64)[idx.astype(np.int64)] @ P.astype(np.float64))
+        return float(np.mean(np.sum((K - kh) ** 2, axis=1)))
+    _, _, ch, Po, Pr, co, cr = _split_case(S, D, 32, 322)
+    ch = oracle.outlier_channels(K, 32)
+    io, no, ir, nr = oracle.compress_split(K, ch, Po, Pr, co, cr)
+    reg = np.array([c for c in range(D) if c not in set(ch.tolist())])
+    kh = np.zeros_like(K)
+    kh[:, ch] = no.astype(np.float64)[:, None] * (co.astype(np.float64)[io.astype(np.int64)] @ Po.astype(np.float64))
+    kh[:, reg] = nr.astype(np.float64)[:, None] * (cr.astype(np.float64)[ir.astype(np.int64)] @ Pr.astype(np.float64))
+    e_split = float(np.mean(np.sum((K - kh) ** 2, axis=1)))
+    assert err_uniform(3) < e_split < err_uniform(2)

@@ -91,6 +91,8 @@ def key_bytes(w) -> int:
         return w.D * w.mse_bits // 8 + (4 if w.gamma_dtype == "f32" else 2)
     if w.layout == "decode":              # the key's and the value's code plane + norm
         return 2 * (w.D * w.mse_bits // 8 + 2)
+    if w.layout == "split":               # both instances' code planes + two fp16 norms
+        return (w.n_out * (w.mse_bits + 1) + (w.D - w.n_out) * w.mse_bits) // 8 + 4
     if w.layout == "decode_prod":         # product key (codes, signs, gamma) + value (codes, norm)
         return w.D * w.mse_bits // 8 + w.D // 8 + 2 + w.D * w.v_bits // 8 + 2
     return w.D * w.mse_bits // 8 + w.D // 8 + (4 if w.gamma_dtype == "f32" else 2)
@@ -106,6 +108,10 @@ def score_kernel_bytes(w) -> int:
         # cache once, A, T and the outputs once, Pi_v once, both codebooks
         return (w.P * w.S * key_bytes(w) + 3 * 4 * w.P * w.B * w.D + 4 * w.H * w.D * w.D
                 + 4 * w.C + 4 * (1 << w.v_bits))
+    if w.layout == "split":
+        # cache once, scores once, A_out and A_reg once, both codebooks
+        return (w.P * w.S * key_bytes(w) + 4 * w.P * w.B * w.S + 4 * w.P * w.B * w.D
+                + 4 * ((1 << (w.mse_bits + 1)) + (1 << w.mse_bits)))
     n_at = 1 if w.layout == "mse" else 2
     return (w.P * w.S * key_bytes(w) + 4 * w.P * w.B * w.S + n_at * 4 * w.P * w.B * w.D + 4 * w.C)
 
@@ -154,6 +160,7 @@ KERNEL_SOURCES = {
     "simt": ("tq_scores_simt.cu", "tq_lut.cuh", "tq_internal.cuh"),
     "mse": ("tq_scores_mse.cu", "tq_lut.cuh", "tq_internal.cuh"),
     "decode": ("tq_decode.cu", "tq_lut.cuh", "tq_internal.cuh"),
+    "split": ("tq_split.cu", "tq_internal.cuh"),
 }
 
 
@@ -162,6 +169,8 @@ def kernel_family(w, path) -> str:
         return w.layout
     if w.layout == "decode_prod":
         return "decode"
+    if w.layout == "split":
+        return "split"
     return "mma" if path == "bf16_mma" else "simt"
 
 
@@ -255,6 +264,47 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # workload on the device (product code only)
 # ---------------------------------------------------------------------------
+
+def build_split_workload(w, tq, torch, dev):
+    """The outlier-split cache on the device: the n_out channels with the largest mean |k|
+    over problem 0's keys, then each instance's unit sub-vectors compressed by libtq's
+    compressor (its codes are the MSE codes of a unit vector) and their lengths as fp16."""
+    n_out, n_reg = w.n_out, w.D - w.n_out
+    bo, br = w.mse_bits + 1, w.mse_bits
+    keys = torch.from_numpy(np.stack([synth.unit_keys(w.seed, p, 0, w.S, w.D) for p in range(w.P)])
+                            .astype(np.float32)).to(dev)
+    ch = torch.sort(torch.topk(keys[0].abs().mean(dim=0), n_out).indices).values.to(torch.int32)
+    mask = torch.ones(w.D, dtype=torch.bool, device=dev)
+    mask[ch.long()] = False
+    reg = torch.nonzero(mask).flatten()
+    sub = {"out": (keys[:, :, ch.long()], n_out, bo), "reg": (keys[:, :, reg], n_reg, br)}
+    cache = {"channels": ch}
+    rot = {}
+    for name, (x, n, b) in sub.items():
+        cb = torch.from_numpy(tq.lloyd_max_codebook(n, b)).to(dev)
+        Pi = torch.from_numpy(np.stack([tq.haar_rotation(synth.rotation_seed_matrix(w.seed + n, h, n))
+                                        for h in range(w.H)])).to(dev)
+        Sx = torch.from_numpy(np.stack([synth.s_matrix(w.seed + n, h, n) for h in range(w.H)])).to(dev)
+        nrm = torch.linalg.vector_norm(x, dim=2)
+        unit = (x / nrm[:, :, None]).contiguous()
+        idx = torch.empty((w.P, w.S, n), dtype=torch.uint8, device=dev)
+        for p in range(w.P):
+            idx[p].copy_(tq.compress_keys(unit[p], Pi[p % w.H], Sx[p % w.H], cb, torch.float16)[0])
+        cache[name + "_plane"] = tq.pack_indices(idx, b)
+        cache[name + "_norm"] = nrm.to(torch.float16)
+        cache[name + "_cb"] = cb
+        rot[name] = Pi
+    Q = torch.from_numpy(np.stack([synth.queries(w.seed, p, w.B, w.D, "f32")[0] for p in range(w.P)])).to(dev)
+    torch.cuda.synchronize(dev)
+    return Q, rot["out"], rot["reg"], cache
+
+
+def split_call(tq, w, Q, Pi_out, Pi_reg, cache, Ao, Ar, out):
+    """One step of the split path: both rotated queries, then the scores."""
+    tq.prepare_queries_split(Q, cache["channels"], Pi_out, Pi_reg, out=(Ao, Ar))
+    return tq.scores_split(Ao, Ar, cache["out_plane"], cache["out_norm"], cache["out_cb"], w.mse_bits + 1,
+                           cache["reg_plane"], cache["reg_norm"], cache["reg_cb"], w.mse_bits, out=out)
+
 
 def build_device_workload(w, tq, torch, dev):
     cb = torch.from_numpy(tq.lloyd_max_codebook(w.D, w.mse_bits)).to(dev)
@@ -419,9 +469,9 @@ def run_reference(args, w):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    if w.layout == "compress":
-        print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the scoring path; "
-                          "the compressor's CPU baseline is in the cpu_baseline of its own line"}), flush=True)
+    if w.layout in ("compress", "split"):
+        print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the scoring path of "
+                          "the page configurations; this workload's CPU baseline is in its own line"}), flush=True)
         return
     n_keys = min(w.S, 4096)
     run = oracle_sample(w, n_keys)
@@ -653,6 +703,147 @@ def run_compress(args, w, tq, torch, dev):
     print(json.dumps(line), flush=True)
 
 
+def run_split(args, w, tq, torch, dev):
+    """The outlier-split decode: one step = the split query transform and the split scorer
+    over P x S keys (rotating copies larger than twice the L2); one JSON line."""
+    Q0, Pi_out, Pi_reg, cache0 = build_split_workload(w, tq, torch, dev)
+    n_reg = w.D - w.n_out
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    per_copy = score_kernel_bytes(w)
+    R = max(2, min(64, math.ceil(2.2 * l2 / per_copy)))
+    G = 8
+    R = -(-R // G) * G
+    copies = [{"Q": Q0.clone(), "c": {k: v.clone() for k, v in cache0.items()},
+               "Ao": torch.empty((w.P, w.B, w.n_out), device=dev), "Ar": torch.empty((w.P, w.B, n_reg), device=dev),
+               "out": torch.empty((w.P, w.B, w.S), device=dev)} for _ in range(R)]
+    stream = torch.cuda.Stream(dev)
+
+    def step(cp):
+        split_call(tq, w, cp["Q"], Pi_out, Pi_reg, cp["c"], cp["Ao"], cp["Ar"], cp["out"])
+
+    def score_only(cp):
+        c = cp["c"]
+        tq.scores_split(cp["Ao"], cp["Ar"], c["out_plane"], c["out_norm"], c["out_cb"], w.mse_bits + 1,
+                        c["reg_plane"], c["reg_norm"], c["reg_cb"], w.mse_bits, out=cp["out"])
+    with torch.cuda.stream(stream):
+        for cp in copies:
+            step(cp)
+    torch.cuda.synchronize(dev)
+
+    def graphs_of(fn):
+        gs = []
+        for b in range(R // G):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for j in range(G):
+                    fn(copies[b * G + j])
+            gs.append(g)
+        return gs
+    steps_g, score_g = graphs_of(step), graphs_of(score_only)
+    clocks = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
+    with torch.cuda.stream(stream):
+        for k in range(max(1, args.warmup // G + 1)):
+            steps_g[k % len(steps_g)].replay()
+    torch.cuda.synchronize(dev)
+    steps = -(-args.steps // G) * G
+
+    def region(gs, n):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record()
+            for k in range(n // G):
+                gs[k % len(gs)].replay()
+            e1.record()
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1)
+    t0 = time.time()
+    regions = [region(steps_g, steps)]
+    n_rep = int(min(500, max(5, math.ceil(500.0 / max(regions[0], 1e-3)))))
+    while len(regions) < n_rep:
+        regions.append(region(steps_g, steps))
+    t1 = time.time()
+    clk = clocks.stop((t0, t1))
+    ms = statistics.median(regions) / steps
+    kernel_ms = statistics.median([region(score_g, 3 * R) for _ in range(5)]) / (3 * R)
+    kbytes = score_kernel_bytes(w)
+    achieved = kbytes / (kernel_ms / 1e3) / 1e9
+    peak, peak_src = hbm_peak()
+    # end to end: the query, the cache and the rotations in from pinned host memory, the
+    # scores out, two streams
+    hQ = Q0.cpu().pin_memory()
+    hc = {k: v.cpu().pin_memory() for k, v in cache0.items()}
+    hPo, hPr = Pi_out.cpu().pin_memory(), Pi_reg.cpu().pin_memory()
+    h2d = (hQ.numel() * 4 + sum(v.numel() * v.element_size() for v in hc.values()) + (hPo.numel() + hPr.numel()) * 4)
+    e_streams = [stream, torch.cuda.Stream(dev)]
+    e_bufs = [{"Q": torch.empty_like(Q0), "c": {k: torch.empty_like(v) for k, v in cache0.items()},
+               "Po": torch.empty_like(Pi_out), "Pr": torch.empty_like(Pi_reg), "Ao": copies[i]["Ao"],
+               "Ar": copies[i]["Ar"], "out": copies[i]["out"],
+               "h": torch.empty((w.P, w.B, w.S), dtype=torch.float32).pin_memory()} for i in range(2)]
+
+    def e2e_run(n):
+        es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        es.record(e_streams[0])
+        e_streams[1].wait_event(es)
+        for k in range(n):
+            eb = e_bufs[k % 2]
+            with torch.cuda.stream(e_streams[k % 2]):
+                eb["Q"].copy_(hQ, non_blocking=True)
+                for key in hc:
+                    eb["c"][key].copy_(hc[key], non_blocking=True)
+                eb["Po"].copy_(hPo, non_blocking=True)
+                eb["Pr"].copy_(hPr, non_blocking=True)
+                split_call(tq, w, eb["Q"], eb["Po"], eb["Pr"], eb["c"], eb["Ao"], eb["Ar"], eb["out"])
+                eb["h"].copy_(eb["out"], non_blocking=True)
+        e_streams[0].wait_stream(e_streams[1])
+        ee.record(e_streams[0])
+        return es, ee
+    e2e_run(args.warmup)
+    torch.cuda.synchronize(dev)
+    n_e = max(3, min(args.steps, 50))
+    es, ee = e2e_run(n_e)
+    torch.cuda.synchronize(dev)
+    e_ms = es.elapsed_time(ee)
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+        n = min(w.S, 4096)
+        keys = synth.unit_keys(w.seed, 0, 0, n, w.D)
+        ch = cache0["channels"].cpu().numpy().astype(np.int64)
+        Po, Pr = Pi_out[0].cpu().numpy(), Pi_reg[0].cpu().numpy()
+        co, cr = cache0["out_cb"].cpu().numpy(), cache0["reg_cb"].cpu().numpy()
+        io, no, ir, nr = oracle.compress_split(keys, ch, Po, Pr, co, cr)
+        Qs = Q0[0].cpu().numpy()
+        t_0, reps = time.perf_counter(), 0
+        while time.perf_counter() - t_0 < args.cpu_seconds:
+            Ao, Ar = oracle.prepare_queries_split(Qs, ch, Po, Pr)
+            oracle.scores_split(Ao, Ar, io, no, co, ir, nr, cr)
+            reps += 1
+        el = time.perf_counter() - t_0
+        cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+        cpu = {"value": reps * w.B * n / el, "unit": "scores/s", "cores": cores, "kind": "oracle",
+               "hardware_concurrency": os.cpu_count(),
+               "sample": f"{reps} x (split query transform + {w.B} queries x {n} keys), {el:.1f} s, float64 NumPy"}
+    fp = kernel_fingerprint("split")
+    line = {"metric": METRIC, "value": w.P * w.B * w.S / (ms / 1e3), "unit": "scores/s", "n_gpus": 1,
+            "steps": steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "P": w.P, "H": w.H, "B": w.B, "S": w.S, "D": w.D,
+                       "n_out": w.n_out, "out_bits": w.mse_bits + 1, "reg_bits": w.mse_bits,
+                       "l2": f"{R} rotating copies, {R * per_copy / 1e6:.0f} MB > 2x L2"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": None, "kernel": "split_scores_kernel",
+                         "kernel_ms": kernel_ms, "bytes_per_launch": kbytes,
+                         "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
+                         "kernel_fingerprint": fp},
+            "timed_region": {"repeats": len(regions), "median_ms": statistics.median(regions)},
+            "cpu_baseline": cpu,
+            "e2e": {"value": w.P * w.B * w.S * n_e / (e_ms / 1e3), "unit": "scores/s",
+                    "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": 4 * w.P * w.B * w.S,
+                    "steps": n_e, "streams": 2},
+            "gpu_launches": 2 * steps, "clocks": clk}
+    print(json.dumps(line), flush=True)
+
+
 def dataclasses_replace(w, **kw):
     import dataclasses
     return dataclasses.replace(w, **kw)
@@ -695,6 +886,9 @@ def main():
         return
     if w.layout == "compress":
         run_compress(args, w, tq, torch, dev)
+        return
+    if w.layout == "split":
+        run_split(args, w, tq, torch, dev)
         return
     Q0, Pi, S_mat, cb, cache0 = build_device_workload(w, tq, torch, dev)
 

@@ -50,6 +50,8 @@ _SIGNATURES = {
                        _P, ctypes.c_size_t, _P], _I),
     "tq_decode_prod": ([_P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, ctypes.c_float,
                         _P, ctypes.c_size_t, _P], _I),
+    "tq_prepare_queries_split": ([_P, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P], _I),
+    "tq_scores_split": ([_P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _P], _I),
     "tq_workspace_bytes": ([_I, _I, _I], _Z),
     "tq_solve": ([_P, _I, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _Z, _I, _P], _I),
     "tq_solve_packed": ([_P, _I, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _Z, _I, _P], _I),
@@ -302,6 +304,47 @@ def decode_prod(A, T, k_plane, k_sign_plane, k_gamma, k_codebook, k_bits, v_plan
         _dev(o, "out", (torch.float32,)), P, H, B, S, D, float(scale),
         _dev(workspace, "workspace", (torch.uint8,)), workspace.numel(), _stream()))
     return o if (out is not None or A.dim() == 3) else o.view(B, D)
+
+
+def prepare_queries_split(Q, channels, Pi_out, Pi_reg, out=None):
+    """A_out = Pi_out q[channels], A_reg = Pi_reg q[other channels] for Q [P,B,D] (or [B,D])
+    f32/bf16; channels int32 [n_out] increasing; Pi_out [H,n_out,n_out] (or 2-D), Pi_reg
+    [H,n_reg,n_reg].  Returns (A_out, A_reg) fp32."""
+    P, B, D = _as3(Q)
+    n_out = channels.numel()
+    H = 1 if Pi_out.dim() == 2 else Pi_out.shape[0]
+    lead = Q.shape[:-1]
+    if out is None:
+        out = (torch.empty(lead + (n_out,), device=Q.device, dtype=torch.float32),
+               torch.empty(lead + (D - n_out,), device=Q.device, dtype=torch.float32))
+    A_out, A_reg = out
+    _check("tq_prepare_queries_split", lib().tq_prepare_queries_split(
+        _dev(Q, "Q", tuple(QTYPE)), QTYPE[Q.dtype], _dev(channels, "channels", (torch.int32,)),
+        _dev(Pi_out, "Pi_out", (torch.float32,)), _dev(Pi_reg, "Pi_reg", (torch.float32,)),
+        _dev(A_out, "A_out", (torch.float32,)), _dev(A_reg, "A_reg", (torch.float32,)), P, H, B, D, n_out,
+        _stream()))
+    return A_out, A_reg
+
+
+def scores_split(A_out, A_reg, out_plane, out_norm, out_codebook, out_bits, reg_plane, reg_norm,
+                 reg_codebook, reg_bits, out=None):
+    """Scores of the outlier-split cache: [P,B,S] (or [B,S])."""
+    P, B, n_out = _as3(A_out)
+    _, _, n_reg = _as3(A_reg)
+    S, orow = _keys3(out_plane, P)
+    S2, rrow = _keys3(reg_plane, P)
+    if (S2 != S or orow * 8 != n_out * out_bits or rrow * 8 != n_reg * reg_bits
+            or out_norm.numel() != P * S or reg_norm.numel() != P * S):
+        raise ValueError("inconsistent split cache shapes")
+    o = _scores_out(out, P, B, S, A_out)
+    _check("tq_scores_split", lib().tq_scores_split(
+        _dev(A_out, "A_out", (torch.float32,)), _dev(A_reg, "A_reg", (torch.float32,)),
+        _dev(out_plane, "out_plane", (torch.uint8,)), _dev(out_norm, "out_norm", (torch.float16,)),
+        _dev(out_codebook, "out_codebook", (torch.float32,)), out_bits,
+        _dev(reg_plane, "reg_plane", (torch.uint8,)), _dev(reg_norm, "reg_norm", (torch.float16,)),
+        _dev(reg_codebook, "reg_codebook", (torch.float32,)), reg_bits, _dev(o, "scores", (torch.float32,)),
+        P, B, S, n_out, n_reg, _stream()))
+    return o if (out is not None or A_out.dim() == 3) else o.view(B, S)
 
 
 def workspace_bytes(P: int, B: int, D: int) -> int:

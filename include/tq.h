@@ -178,6 +178,38 @@ tq_status tq_scores_mse(const float* A, const uint8_t* idx_plane, const uint16_t
                         int idx_bits, int norm_correction, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Outlier-split cache: fractional bits from two TurboQuant-MSE instances per head
+ * over disjoint channel sets (kanthi.in §7 "Fractional bits and the outlier split":
+ * the channels hot across the sequence are known ahead of time and get their own,
+ * wider instance; each instance has its own rotation, codebook and norm):
+ *
+ *   A_out = Pi_out q[channels],  A_reg = Pi_reg q[other channels, increasing]
+ *   score = n_out * <A_out, c_out(idx_out)> + n_reg * <A_reg, c_reg(idx_reg)>
+ *
+ * tq_prepare_queries_split: Q [P,B,D] (f32 or bf16); channels: n_out int32 device
+ * values, strictly increasing, each in [0, D) (the caller's contract: a list that
+ * breaks it gives wrong results, never an out-of-bounds access); Pi_out [H,n_out,n_out],
+ * Pi_reg [H,D-n_out,D-n_out] fp32; A_out [P,B,n_out], A_reg [P,B,D-n_out] fp32
+ * outputs.  2 <= D <= 256, 1 <= n_out < D.
+ *
+ * tq_scores_split: each instance's cache in the tq_scores_mse format of its own
+ * width: out_plane [P,S,n_out*out_bits/8] + out_norm [P,S] fp16 + out_codebook
+ * [2^out_bits], reg_plane [P,S,n_reg*reg_bits/8] + reg_norm + reg_codebook;
+ * scores [P,B,S] fp32.  n_out and n_reg multiples of 32, bits in {1,...,4}.  The
+ * printed split is n_out = 32 at 3 bits and n_reg = 96 at 2: 36 bytes of codes and
+ * two fp16 norms, 40 bytes (2.5 bits a coordinate) a key.  fp32 arithmetic.
+ * Errors: TQ_ERR_INVALID_VALUE, TQ_ERR_MISALIGNED, TQ_ERR_UNSUPPORTED, TQ_ERR_LAUNCH.
+ * ---------------------------------------------------------------------- */
+tq_status tq_prepare_queries_split(const void* Q, tq_qtype qtype, const int* channels, const float* Pi_out,
+                                   const float* Pi_reg, float* A_out, float* A_reg, int P, int H, int B,
+                                   int D, int n_out, cudaStream_t stream);
+tq_status tq_scores_split(const float* A_out, const float* A_reg, const uint8_t* out_plane,
+                          const uint16_t* out_norm, const float* out_codebook, int out_bits,
+                          const uint8_t* reg_plane, const uint16_t* reg_norm, const float* reg_codebook,
+                          int reg_bits, float* scores, int P, int B, int S, int n_out, int n_reg,
+                          cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
  * Fused decode over an MSE-quantized key AND value cache, in the rotated
  * domain (kanthi.in §8 "Kernel view: never un-rotate a key", the kernel form
  * of tq_rotated_domain; §7 on values):

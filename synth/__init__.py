@@ -66,11 +66,14 @@ class Workload:
                          # "mse" (code plane + fp16 norm, the MSE-only variant, no signs) or
                          # "decode" (MSE keys and MSE values, for the fused decode) or
                          # "decode_prod" (TurboQuant_prod keys and MSE values) or
-                         # "compress" (the write side: fp32 keys in, the packed cache out)
+                         # "compress" (the write side: fp32 keys in, the packed cache out) or
+                         # "split" (outlier split: n_out channels at mse_bits + 1 bits, the
+                         # rest at mse_bits, two MSE instances with norms)
     gamma_dtype: str     # "f32" or "f16" (for "mse": the dtype of the stored norm)
     q_dtype: str         # "f32" or "bf16"
     v_bits: int = 0      # "decode_prod": bits of the MSE value codes (the keys are a
                          # TurboQuant_prod cache: mse_bits-bit codes + sign plane + fp16 gamma)
+    n_out: int = 0       # "split": outlier channels
 
     @property
     def C(self) -> int:
@@ -110,6 +113,9 @@ WORKLOADS = {
     # The GPU compressor: 32768 unit fp32 keys of D = 128 into the packed 3-bit cache of c2.
     "k1": Workload("k1_compress_S32768_D128_packed3bit", 1008, 1, 1, 1, 32768, 128, 2,
                    "compress", "f16", "f32"),
+    # Outlier-split decode: 32 outlier channels at 3 bits, 96 at 2, two fp16 norms (40 B a key).
+    "s1": Workload("s1_split_decode_B1_S131072_32x3_96x2", 1009, 1, 1, 1, 131072, 128, 2,
+                   "split", "f16", "f32", n_out=32),
 }
 
 

@@ -18,7 +18,7 @@ W = synth.WORKLOADS
 
 
 @pytest.mark.parametrize("key,per_key", [("c0", 260), ("c1", 260), ("c2", 50), ("c3", 50), ("c4", 66),
-                                         ("m1", 50), ("d1", 100), ("d2", 100)])
+                                         ("m1", 50), ("d1", 100), ("d2", 100), ("s1", 40)])
 def test_bytes_per_key(key, per_key):
     assert bench.key_bytes(W[key]) == per_key
 

@@ -21,14 +21,17 @@ struct LutShape {
 };
 
 // Centroids of the table value this thread keeps fixed while it builds tables
-// (value v = thread % NV; code i of v is bits BITS*i .. BITS*i+BITS-1).
+// (value v = thread % NV; code i of v is bits BITS*i .. BITS*i+BITS-1).  Read through
+// L2 (ld.global.cg): kernels launched as programmatic dependents run beside the grid
+// before them, so nothing they read after griddepcontrol.wait may go through the
+// read-only path, which assumes the data stays unchanged for the kernel's lifetime.
 template <int BITS>
 __device__ __forceinline__ void table_centroids(const float* __restrict__ codebook,
                                                 float (&cv)[LutShape<BITS>::G]) {
   using L = LutShape<BITS>;
   const int v = threadIdx.x % L::NV;
 #pragma unroll
-  for (int k = 0; k < L::G; ++k) cv[k] = __ldg(codebook + ((v >> (BITS * k)) & ((1 << BITS) - 1)));
+  for (int k = 0; k < L::G; ++k) cv[k] = __ldcg(codebook + ((v >> (BITS * k)) & ((1 << BITS) - 1)));
 }
 
 // Two fp32 additions in one instruction (sm_100 packed f32x2): acc.lo += a, acc.hi += b.

@@ -516,8 +516,8 @@ scores_mma_kernel(const __grid_constant__ Params prm) {
         lo[u] = hi[u] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (e < NT * 32 && q0 + n < prm.B) {
           const float* src = (kc < 16 ? prm.A : prm.T) + (static_cast<size_t>(p) * prm.B + q0 + n) * 128 + (kc & 15) * 8;
-          lo[u] = __ldg(reinterpret_cast<const float4*>(src));
-          hi[u] = __ldg(reinterpret_cast<const float4*>(src + 4));
+          lo[u] = __ldcg(reinterpret_cast<const float4*>(src));
+          hi[u] = __ldcg(reinterpret_cast<const float4*>(src + 4));
         }
       }
 #pragma unroll

@@ -38,8 +38,8 @@ __device__ __forceinline__ void load_mse_key(MseKey<BITS>& k, const uint8_t* __r
                                              const uint16_t* __restrict__ norm_f16, size_t key) {
   const uint4* ip = reinterpret_cast<const uint4*>(idx_plane + key * (16 * BITS));
 #pragma unroll
-  for (int i = 0; i < BITS; ++i) k.idx[i] = __ldg(ip + i);
-  k.n = __ldg(norm_f16 + key);
+  for (int i = 0; i < BITS; ++i) k.idx[i] = __ldcg(ip + i);
+  k.n = __ldcg(norm_f16 + key);
 }
 
 template <int QB>
@@ -95,7 +95,7 @@ scores_mse_lut_kernel(const float* __restrict__ A, const uint8_t* __restrict__ i
 #pragma unroll
     for (int j = 0; j < kAP; ++j) {
       const int e = tid + 256 * j, q = e >> 7;
-      av[j] = e < QB * 128 && b0 + q < B ? __ldg(A + (static_cast<size_t>(p) * B + b0 + q) * 128 + (e & 127)) : 0.f;
+      av[j] = e < QB * 128 && b0 + q < B ? __ldcg(A + (static_cast<size_t>(p) * B + b0 + q) * 128 + (e & 127)) : 0.f;
     }
     MseKey<BITS> k0, k1;
     const int first = sb + tid;

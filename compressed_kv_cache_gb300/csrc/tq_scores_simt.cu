@@ -418,7 +418,7 @@ scores_packed_lut_kernel(const float* __restrict__ A, const float* __restrict__ 
     for (int j = 0; j < QB; ++j) {
       const int e = static_cast<int>(threadIdx.x) + 256 * j, q = e >> 8, x = e & 255;
       const size_t row = (static_cast<size_t>(p) * B + b0 + q) * 128;
-      at[j] = b0 + q < B ? (x < 128 ? __ldg(A + row + x) : __ldg(T + row + x - 128)) : 0.f;
+      at[j] = b0 + q < B ? (x < 128 ? __ldcg(A + row + x) : __ldcg(T + row + x - 128)) : 0.f;
     }
     __syncthreads();                      // the previous segment's tables are no longer read
 #pragma unroll
@@ -477,12 +477,265 @@ cudaError_t launch_lut_qb(const float* A, const float* T, const uint8_t* idx_pla
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// Bit-packed cache, D = 128, 2-bit codes, 2-4 queries: byte tables, skewed by lane.
+//
+// Per query tile, tables of partial sums indexed by a whole byte: a code byte (4 codes)
+// at each of its 32 positions, and a sign byte (8 signs) at each of its 16 positions.
+// An entry holds the QB queries' values side by side (QB floats), entry (e, p) of a
+// table set sitting at ((e * NP + p) * QB) floats.  A key then costs 32 + 16 lookups
+// of QB floats instead of 64 + 32.  Lane l walks a key's positions starting at l (its
+// code row rotated left by l bytes, its sign row by l mod 16, in registers), so the
+// lanes of one shared-memory phase (8 for 16-byte entries, 16 for 8-byte entries) read
+// distinct positions, that is distinct bank groups, whatever their byte values.
+// Tables are built from 16-entry tables of two codes / four signs:
+//   byte entry (e, p) = pair/nibble entry (e & 15, 2p) + pair/nibble entry (e >> 4, 2p+1)
+// ---------------------------------------------------------------------------
+template <int QB>
+struct Lut8 {
+  static constexpr int kCode = 256 * 32 * QB;            // floats of the code byte tables
+  static constexpr int kSign = 256 * 16 * QB;            // floats of the sign byte tables
+  static constexpr int kPair = 64 * 16 * QB;             // 2-code tables, [e4][pos 0..63][q]
+  static constexpr int kNib = 32 * 16 * QB;              // 4-sign tables, [e4][pos 0..31][q]
+  static constexpr int kFloats = kCode + kSign + kPair + kNib + 256 * QB;   // + A/T staging
+  static constexpr int kThreads = 512;
+};
+
+// rotate the 8 words left by r words (r in 0..7) and then by b bytes (b in 0..3)
+__device__ __forceinline__ void rotate8(uint32_t (&w)[8], int r, int b) {
+  uint32_t t[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) t[j] = (r & 1) ? w[(j + 1) & 7] : w[j];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) w[j] = (r & 2) ? t[(j + 2) & 7] : t[j];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) t[j] = (r & 4) ? w[(j + 4) & 7] : w[j];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) w[j] = __funnelshift_r(t[j], t[(j + 1) & 7], 8 * b);
+}
+__device__ __forceinline__ void rotate4(uint32_t (&w)[4], int r, int b) {
+  uint32_t t[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) t[j] = (r & 1) ? w[(j + 1) & 3] : w[j];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) w[j] = (r & 2) ? t[(j + 2) & 3] : t[j];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) t[j] = __funnelshift_r(w[j], w[(j + 1) & 3], 8 * b);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) w[j] = t[j];
+}
+
+// one lookup of QB floats at byte offset off from tab, added to the pair accumulators
+template <int QB>
+__device__ __forceinline__ void lut8_add(const char* tab, uint32_t off, unsigned long long (&acc)[2]) {
+  if constexpr (QB == 4) {
+    const float4 v = *reinterpret_cast<const float4*>(tab + off);
+    add2(acc[0], v.x, v.y);
+    add2(acc[1], v.z, v.w);
+  } else {
+    const float2 v = *reinterpret_cast<const float2*>(tab + off);
+    add2(acc[0], v.x, v.y);
+  }
+}
+
+// The 8 partial sums (code and sign parts, QB queries) of one key from the byte tables.
+template <int QB>
+__device__ __forceinline__ void lut8_key_sums(const float* code8, const float* sign8, const PackedKey<2>& k,
+                                              int lane, float (&mm)[QB], float (&rr)[QB]) {
+  constexpr uint32_t kC = 4 * QB;                         // bytes of one entry
+  constexpr int kEC = 32 * kC;                            // bytes per code byte value (32 positions)
+  constexpr int kES = 16 * kC;                            // bytes per sign byte value (16 positions)
+  uint32_t w[8] = {k.idx[0].x, k.idx[0].y, k.idx[0].z, k.idx[0].w, k.idx[1].x, k.idx[1].y, k.idx[1].z, k.idx[1].w};
+  uint32_t ws[4] = {k.sg.x, k.sg.y, k.sg.z, k.sg.w};
+  rotate8(w, lane >> 2, lane & 3);
+  rotate4(ws, (lane >> 2) & 3, lane & 3);
+  unsigned long long m2[2][2] = {{0ull, 0ull}, {0ull, 0ull}}, r2[2][2] = {{0ull, 0ull}, {0ull, 0ull}};
+  const char* ct = reinterpret_cast<const char*>(code8);
+  const char* st = reinterpret_cast<const char*>(sign8);
+  // column of step i: ((i + lane) mod 32) entries for codes, ((i + lane) mod 16) for signs
+  uint32_t col = static_cast<uint32_t>(lane) * kC;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const uint32_t byte = (w[i >> 2] >> (8 * (i & 3))) & 0xffu;
+    lut8_add<QB>(ct, byte * kEC + col, m2[i & 1]);
+    if (i < 16) {
+      const uint32_t sb = (ws[i >> 2] >> (8 * (i & 3))) & 0xffu;
+      lut8_add<QB>(st, sb * kES + (col & (15u * kC)), r2[i & 1]);
+    }
+    col = (col + kC) & (31u * kC);
+  }
+#pragma unroll
+  for (int q = 0; q < QB; ++q) {
+    const int a = q >> 1;
+    const bool hi = q & 1;
+    const float m0 = hi ? __uint_as_float(static_cast<uint32_t>(m2[0][a] >> 32)) : __uint_as_float(static_cast<uint32_t>(m2[0][a]));
+    const float m1 = hi ? __uint_as_float(static_cast<uint32_t>(m2[1][a] >> 32)) : __uint_as_float(static_cast<uint32_t>(m2[1][a]));
+    const float r0 = hi ? __uint_as_float(static_cast<uint32_t>(r2[0][a] >> 32)) : __uint_as_float(static_cast<uint32_t>(r2[0][a]));
+    const float r1 = hi ? __uint_as_float(static_cast<uint32_t>(r2[1][a] >> 32)) : __uint_as_float(static_cast<uint32_t>(r2[1][a]));
+    mm[q] = m0 + m1;
+    rr[q] = r0 + r1;
+  }
+}
+
+// Tables of one unit from its A and T rows staged as sAT [256][QB]: first the 2-code and
+// 4-sign tables, then the byte tables as sums of two of them.
+template <int QB>
+__device__ __forceinline__ void build_lut8(const float* sAT, float* code8, float* sign8, float* pair, float* nib,
+                                           const float* cb4) {
+  constexpr int NT = Lut8<QB>::kThreads;
+  const int tid = threadIdx.x;
+  // 2-code tables: pair[(e4 * 64 + g) * QB + q] = A[2g] c[e4 & 3] + A[2g+1] c[e4 >> 2]
+  for (int e = tid; e < 64 * 16 * QB; e += NT) {
+    const int q = e % QB, g = (e / QB) % 64, e4 = e / (QB * 64);
+    pair[e] = fmaf(sAT[(2 * g) * QB + q], cb4[e4 & 3], sAT[(2 * g + 1) * QB + q] * cb4[e4 >> 2]);
+  }
+  // 4-sign tables: nib[(e4 * 32 + g) * QB + q] = sum_i T[4g+i] (bit i of e4 ? +1 : -1)
+  for (int e = tid; e < 32 * 16 * QB; e += NT) {
+    const int q = e % QB, g = (e / QB) % 32, e4 = e / (QB * 32);
+    float acc = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float t = sAT[(128 + 4 * g + i) * QB + q];
+      acc += ((e4 >> i) & 1) ? t : -t;
+    }
+    nib[e] = acc;
+  }
+  __syncthreads();
+  // code byte tables: code8[(e * 32 + p) * QB + q] = pair(e & 15, 2p) + pair(e >> 4, 2p + 1)
+  for (int e = tid; e < 256 * 32 * QB; e += NT) {
+    const int q = e % QB, p = (e / QB) % 32, v = e / (QB * 32);
+    code8[e] = pair[((v & 15) * 64 + 2 * p) * QB + q] + pair[((v >> 4) * 64 + 2 * p + 1) * QB + q];
+  }
+  // sign byte tables: sign8[(e * 16 + p) * QB + q] = nib(e & 15, 2p) + nib(e >> 4, 2p + 1)
+  for (int e = tid; e < 256 * 16 * QB; e += NT) {
+    const int q = e % QB, p = (e / QB) % 16, v = e / (QB * 16);
+    sign8[e] = nib[((v & 15) * 32 + 2 * p) * QB + q] + nib[((v >> 4) * 32 + 2 * p + 1) * QB + q];
+  }
+}
+
+// Stream-K scorer with byte tables (2-bit codes, QB = 2 or 4); the unit boundaries,
+// staging and programmatic-dependent-launch protocol of scores_packed_lut_kernel.
+template <int QB>
+__global__ void __launch_bounds__(Lut8<QB>::kThreads, 1)
+scores_packed_lut8_kernel(const float* __restrict__ A, const float* __restrict__ T,
+                          const uint8_t* __restrict__ idx_plane, const uint8_t* __restrict__ sign_plane,
+                          const uint16_t* __restrict__ gamma_f16, const float* __restrict__ codebook,
+                          float* __restrict__ scores, int B, int S, int qtiles, int64_t total, float kappa) {
+  using L = Lut8<QB>;
+  constexpr int NT = L::kThreads;
+  extern __shared__ __align__(16) float smem[];
+  float* code8 = smem;
+  float* sign8 = code8 + L::kCode;
+  float* pair = sign8 + L::kSign;
+  float* nib = pair + L::kPair;
+  float* sAT = nib + L::kNib;                             // [256][QB]: the unit's A, then T
+  __shared__ float cb4[4];
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int64_t per = (total + gridDim.x - 1) / gridDim.x;
+  int64_t w = min(static_cast<int64_t>(blockIdx.x) * per, total);
+  const int64_t wend = min(w + per, total);
+  bool waited = false;
+  while (w < wend) {
+    const int u = static_cast<int>(w / S);
+    const int sb = static_cast<int>(w - static_cast<int64_t>(u) * S);
+    const int se = static_cast<int>(min(static_cast<int64_t>(S), sb + (wend - w)));
+    const int p = u / qtiles;
+    const int b0 = (u - p * qtiles) * QB;
+    const int first = sb + tid;
+    // the segment's first two keys are requested before its tables are built
+    PackedKey<2> k0, k1;
+    prefetch_two_keys<2>(k0, k1, idx_plane, sign_plane, gamma_f16, p, first, NT, se, S);
+    if (!waited) {
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      waited = true;
+    }
+    // the unit's A and T rows: one load round trip (QB values a thread before the
+    // barrier), queries past B read as zero
+    float at[(256 * QB + NT - 1) / NT];
+#pragma unroll
+    for (int j = 0; j < (256 * QB + NT - 1) / NT; ++j) {
+      const int e = tid + NT * j, x = e / QB, q = e % QB;
+      const size_t row = (static_cast<size_t>(p) * B + b0 + q) * 128;
+      at[j] = e < 256 * QB && b0 + q < B ? (x < 128 ? __ldcg(A + row + x) : __ldcg(T + row + x - 128)) : 0.f;
+    }
+    const float cbv = tid < 4 ? __ldcg(codebook + tid) : 0.f;
+    __syncthreads();                      // the previous segment's tables are no longer read
+#pragma unroll
+    for (int j = 0; j < (256 * QB + NT - 1) / NT; ++j) {
+      const int e = tid + NT * j;
+      if (e < 256 * QB) sAT[e] = at[j];
+    }
+    if (tid < 4) cb4[tid] = cbv;
+    __syncthreads();
+    build_lut8<QB>(sAT, code8, sign8, pair, nib, cb4);
+    __syncthreads();
+    const size_t base = static_cast<size_t>(p) * S;
+    for (int64_t s = first; s < se; s += NT) {
+      const PackedKey<2> cur = k0;
+      k0 = k1;
+      if (s + 2 * NT < se) load_packed_key<2>(k1, idx_plane, sign_plane, gamma_f16, base + s + 2 * NT);
+      float mm[QB], rr[QB];
+      lut8_key_sums<QB>(code8, sign8, cur, lane, mm, rr);
+      store_scores<QB>(scores, mm, rr, kappa * __half2float(__ushort_as_half(cur.g)), p, b0, B, S,
+                       static_cast<int>(s));
+    }
+    w += se - sb;
+  }
+}
+
+template <int QB>
+cudaError_t launch_lut8_qb(const float* A, const float* T, const uint8_t* idx_plane,
+                           const uint8_t* sign_plane, const uint16_t* gamma_f16, const float* codebook,
+                           float* scores, int P, int B, int S, bool after_prepare, cudaStream_t st) {
+  using L = Lut8<QB>;
+  const size_t smem = static_cast<size_t>(L::kFloats) * sizeof(float);
+  auto kernel = scores_packed_lut8_kernel<QB>;
+  static std::atomic<int> slots[64];      // co-resident CTAs per device
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  int n = slots[dev & 63].load(std::memory_order_acquire);
+  if (n == 0) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    int sms = 0, per_sm = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, L::kThreads, smem);
+    if (e != cudaSuccess) return e;
+    n = sms * (per_sm > 0 ? per_sm : 1);
+    slots[dev & 63].store(n, std::memory_order_release);
+  }
+  const int qtiles = ceil_div(B, QB);
+  const int64_t total = static_cast<int64_t>(P) * qtiles * S;
+  const int64_t want = (total + L::kThreads - 1) / L::kThreads;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(want < n ? want : n));
+  cfg.blockDim = dim3(L::kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = after_prepare ? 1 : 0;
+  e = cudaLaunchKernelEx(&cfg, kernel, A, T, idx_plane, sign_plane, gamma_f16, codebook, scores, B, S, qtiles,
+                         total, qjl_scale(128));
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 template <int BITS>
 cudaError_t launch_lut_bits(const float* A, const float* T, const uint8_t* idx_plane,
                             const uint8_t* sign_plane, const uint16_t* gamma_f16,
                             const float* codebook, float* scores, int P, int B, int S,
                             bool after_prepare, cudaStream_t st) {
   if (B <= 1) return launch_lut_qb<BITS, 1>(A, T, idx_plane, sign_plane, gamma_f16, codebook, scores, P, B, S, after_prepare, st);
+  if constexpr (BITS == 2) {
+    // 2-bit codes with 2-4 queries: byte tables (half the lookups)
+    if (B <= 2) return launch_lut8_qb<2>(A, T, idx_plane, sign_plane, gamma_f16, codebook, scores, P, B, S, after_prepare, st);
+    if (B <= 4) return launch_lut8_qb<4>(A, T, idx_plane, sign_plane, gamma_f16, codebook, scores, P, B, S, after_prepare, st);
+  }
   if (B <= 2) return launch_lut_qb<BITS, 2>(A, T, idx_plane, sign_plane, gamma_f16, codebook, scores, P, B, S, after_prepare, st);
   if (B <= 4 || BITS == 3) return launch_lut_qb<BITS, 4>(A, T, idx_plane, sign_plane, gamma_f16, codebook, scores, P, B, S, after_prepare, st);
   return launch_lut_qb<BITS, 8>(A, T, idx_plane, sign_plane, gamma_f16, codebook, scores, P, B, S, after_prepare, st);
@@ -547,12 +800,13 @@ __device__ __forceinline__ void prefetch_l2(const void* p, size_t bytes) {
                  : "memory");
 }
 
-// Coordinates 4*lane .. 4*lane+3 of one query row of 128.
+// Coordinates 4*lane .. 4*lane+3 of one query row of 128 (through L2: the kernel before
+// this one on the stream may have written the query).
 __device__ __forceinline__ float4 load_query4(const float* q, int lane) {
-  return __ldg(reinterpret_cast<const float4*>(q) + lane);
+  return __ldcg(reinterpret_cast<const float4*>(q) + lane);
 }
 __device__ __forceinline__ float4 load_query4(const __nv_bfloat16* q, int lane) {
-  const uint2 v = __ldg(reinterpret_cast<const uint2*>(q) + lane);
+  const uint2 v = __ldcg(reinterpret_cast<const uint2*>(q) + lane);
   return make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u),
                      __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
 }
@@ -679,7 +933,7 @@ solve_packed_lut_kernel(const QT* __restrict__ Q, const float* __restrict__ Pi,
   float cv[L::G];
   table_centroids<BITS>(codebook, cv);
   // gamma of this thread's key in the first tile (later tiles: one tile ahead)
-  float g_next = k_begin + tid < k_end ? __half2float(__ushort_as_half(__ldg(gamma_f16 + key0 + tid))) : 0.f;
+  float g_next = k_begin + tid < k_end ? __half2float(__ushort_as_half(__ldcg(gamma_f16 + key0 + tid))) : 0.f;
   // rows of A/T: warp w takes groups of 8 rows; lane l reads coordinates 4l .. 4l+3
   // of each row (one conflict-free 512-byte row a warp) and the warp sums them.  Each
   // group goes to every CTA of the cluster by its own bulk copies, completing bytes
@@ -733,7 +987,7 @@ solve_packed_lut_kernel(const QT* __restrict__ Q, const float* __restrict__ Pi,
     const int s = k_begin + t * kT + tid;
     const float g = g_next;
     if (t + 1 < ntiles)
-      g_next = s + kT < k_end ? __half2float(__ushort_as_half(__ldg(gamma_f16 + key0 + (t + 1) * kT + tid))) : 0.f;
+      g_next = s + kT < k_end ? __half2float(__ushort_as_half(__ldcg(gamma_f16 + key0 + (t + 1) * kT + tid))) : 0.f;
     if (s < k_end) {
       PackedKey<BITS> k;
 #pragma unroll

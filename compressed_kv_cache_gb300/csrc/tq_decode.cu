@@ -142,8 +142,8 @@ decode_split_kernel(const SplitArgs args) {
     av[j] = e < QB * kQ && b0 + q < B ? (x < kD ? __ldg(args.A + row + x) : __ldg(args.T + row + x - kD)) : 0.f;
   }
   const float vt = tid < (1 << VBITS) ? __ldg(args.v_cb + tid) : 0.f;
-  float cv[L::G];
-  table_centroids<KBITS>(args.k_cb, cv);
+  __shared__ float sKcb[1 << KBITS];
+  stage_codebook<KBITS>(args.k_cb, sKcb, 0);   // read after the barrier before the table build
 
   // this warp's keys [w0, w1) of the chunk, in steps of 32: per step one bulk copy of
   // the key rows and one of the value rows, both completing on the step's barrier
@@ -189,6 +189,8 @@ decode_split_kernel(const SplitArgs args) {
   // then (product keys) 32 sign tables of 4 signs each from T
   __syncthreads();
   {
+    float cv[L::G];
+    table_centroids<KBITS>(sKcb, cv);
     const int v = tid % L::NV;
     for (int q = 0; q < QB; ++q) {
       const float* a = sA + q * kQ;

@@ -20,18 +20,29 @@ struct LutShape {
   static constexpr int PER_Q = NPI * NV + NPS * 16;      // floats per query (codes and signs)
 };
 
-// Centroids of the table value this thread keeps fixed while it builds tables
-// (value v = thread % NV; code i of v is bits BITS*i .. BITS*i+BITS-1).  Read through
-// L2 (ld.global.cg): kernels launched as programmatic dependents run beside the grid
-// before them, so nothing they read after griddepcontrol.wait may go through the
-// read-only path, which assumes the data stays unchanged for the kernel's lifetime.
+// The codebook (2^BITS centroids) copied into shared memory, one load per centroid
+// per CTA: the first 2^BITS threads of the calling group (from `first` on) each copy
+// one, and the caller orders the copy before any read with a barrier.  Every thread of
+// every CTA reading the codebook from global memory would send all those requests to
+// the one L2 slice that holds it.  The load goes through L2 (ld.global.cg): kernels
+// launched as programmatic dependents run beside the grid before them, so nothing they
+// read after griddepcontrol.wait may go through the read-only path, which assumes the
+// data stays unchanged for the kernel's lifetime.
 template <int BITS>
-__device__ __forceinline__ void table_centroids(const float* __restrict__ codebook,
-                                                float (&cv)[LutShape<BITS>::G]) {
+__device__ __forceinline__ void stage_codebook(const float* __restrict__ codebook, float* sCb, int first) {
+  const int i = static_cast<int>(threadIdx.x) - first;
+  if (i >= 0 && i < (1 << BITS)) sCb[i] = __ldcg(codebook + i);
+}
+
+// Centroids of the table value this thread keeps fixed while it builds tables
+// (value v = thread % NV; code i of v is bits BITS*i .. BITS*i+BITS-1), from the
+// shared copy stage_codebook made.
+template <int BITS>
+__device__ __forceinline__ void table_centroids(const float* sCb, float (&cv)[LutShape<BITS>::G]) {
   using L = LutShape<BITS>;
   const int v = threadIdx.x % L::NV;
 #pragma unroll
-  for (int k = 0; k < L::G; ++k) cv[k] = __ldcg(codebook + ((v >> (BITS * k)) & ((1 << BITS) - 1)));
+  for (int k = 0; k < L::G; ++k) cv[k] = sCb[(v >> (BITS * k)) & ((1 << BITS) - 1)];
 }
 
 // Two fp32 additions in one instruction (sm_100 packed f32x2): acc.lo += a, acc.hi += b.

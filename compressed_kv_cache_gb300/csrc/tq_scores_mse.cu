@@ -70,14 +70,8 @@ scores_mse_lut_kernel(const float* __restrict__ A, const uint8_t* __restrict__ i
   // overlaps that kernel's tail and nothing else.
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int v = tid % L::NV;
-  float cv[L::G];
-  table_centroids<BITS>(codebook, cv);
-  if (tid < L::NV) {
-    float acc = 0.f;
-#pragma unroll
-    for (int k = 0; k < L::G; ++k) acc = fmaf(cv[k], cv[k], acc);
-    sq[tid] = acc;
-  }
+  __shared__ float sCb[1 << BITS];
+  stage_codebook<BITS>(codebook, sCb, 0);   // read after the loop's first barrier
   const int64_t per = (total + gridDim.x - 1) / gridDim.x;
   int64_t w = min(static_cast<int64_t>(blockIdx.x) * per, total);
   const int64_t wend = min(w + per, total);
@@ -106,6 +100,14 @@ scores_mse_lut_kernel(const float* __restrict__ A, const uint8_t* __restrict__ i
     for (int j = 0; j < kAP; ++j) {
       const int e = tid + 256 * j;
       if (e < QB * 128) sA[e] = av[j];
+    }
+    float cv[L::G];
+    table_centroids<BITS>(sCb, cv);
+    if (tid < L::NV) {
+      float acc = 0.f;
+#pragma unroll
+      for (int k = 0; k < L::G; ++k) acc = fmaf(cv[k], cv[k], acc);
+      sq[tid] = acc;
     }
     __syncthreads();
     for (int q = 0; q < QB; ++q) {

@@ -394,8 +394,11 @@ scores_packed_lut_kernel(const float* __restrict__ A, const float* __restrict__ 
   const int64_t per = (total + gridDim.x - 1) / gridDim.x;
   int64_t w = min(static_cast<int64_t>(blockIdx.x) * per, total);
   const int64_t wend = min(w + per, total);
-  float cv[LutShape<BITS>::G];
-  table_centroids<BITS>(codebook, cv);
+  __shared__ float sCb[1 << BITS];
+  // every kernel before the query transform has completed when this grid starts, and
+  // the transform does not write the codebook, so it may be read before the wait; the
+  // barriers in the loop order the copy before the first table build
+  stage_codebook<BITS>(codebook, sCb, 0);
   bool waited = false;
   while (w < wend) {
     const int u = static_cast<int>(w / S);
@@ -424,6 +427,8 @@ scores_packed_lut_kernel(const float* __restrict__ A, const float* __restrict__ 
 #pragma unroll
     for (int j = 0; j < QB; ++j) sAT[threadIdx.x + 256 * j] = at[j];
     __syncthreads();
+    float cv[LutShape<BITS>::G];
+    table_centroids<BITS>(sCb, cv);
     build_luts<BITS, QB, 256>([&](int q, int e) { return sAT[q * 256 + e]; }, lut, cv);
     __syncthreads();
     lut_score_keys<BITS, QB>(lut, idx_plane, sign_plane, gamma_f16, scores, k0, k1, first, 256, se,
@@ -873,6 +878,7 @@ solve_packed_lut_kernel(const QT* __restrict__ Q, const float* __restrict__ Pi,
   __shared__ __align__(16) float sAT[256 * QB];           // [256][QB]: rows of A, then of T
   __shared__ __align__(16) float sMine[R * QB];           // [R][QB]: this CTA's rows of A/T
   __shared__ __align__(8) uint64_t bars[2 + kFusedStages];   // rows, A/T, key tiles
+  __shared__ float sCb[1 << BITS];
   extern __shared__ __align__(128) float dsm[];
   float* lut = dsm;                                       // [QB][PER_Q]
   float* sRows = lut + QB * L::PER_Q;                     // [R][128]
@@ -930,8 +936,9 @@ solve_packed_lut_kernel(const QT* __restrict__ Q, const float* __restrict__ Pi,
       bulk_g2s(st + kT * kRowBytes, sign_plane + (key0 + t * kT) * 16, nk * 16, bar_tile + 8 * t);
     }
   }
-  float cv[L::G];
-  table_centroids<BITS>(codebook, cv);
+  // warps R/8 and up compute no rows of A/T, so the last one copies the codebook; the
+  // barrier before the table build orders its copy before any read
+  stage_codebook<BITS>(codebook, sCb, kT - 32);
   // gamma of this thread's key in the first tile (later tiles: one tile ahead)
   float g_next = k_begin + tid < k_end ? __half2float(__ushort_as_half(__ldcg(gamma_f16 + key0 + tid))) : 0.f;
   // rows of A/T: warp w takes groups of 8 rows; lane l reads coordinates 4l .. 4l+3
@@ -977,6 +984,9 @@ solve_packed_lut_kernel(const QT* __restrict__ Q, const float* __restrict__ Pi,
   // it sent here); the cluster barrier at the end keeps each CTA alive until all have
   const bool have_at = wait_parity_bounded(bar_at, 0, kFaultLut);
   cluster_arrive_relaxed();
+  __syncthreads();
+  float cv[L::G];
+  table_centroids<BITS>(sCb, cv);
   build_luts<BITS, QB, kT>(
       [&](int q, int e) { return have_at ? sAT[e * QB + q] : __int_as_float(0x7fc00000); }, lut, cv);
   __syncthreads();

@@ -755,8 +755,8 @@ cudaError_t launch_lut_bits(const float* A, const float* T, const uint8_t* idx_p
 // A cluster of CS CTAs serves one (problem, query tile); each CTA scores one
 // contiguous range of the keys.  The stacked matrix [Pi; S_mat] of the problem's
 // head has 256 rows; CTA rank r brings rows r*R .. r*R+R-1 (R = 256/CS) into its
-// shared memory with one bulk copy, forms those rows of A = Pi q and T = S_mat q for
-// its QB queries (a warp per 8 rows, the query in registers), and sends each group
+// shared memory with one bulk copy and the query tile with another, forms those rows
+// of A = Pi q and T = S_mat q for its QB queries (a warp per 8 rows), and sends each group
 // of 8 rows to every CTA of the cluster by a shared-to-shared bulk copy that
 // completes bytes on the receiver's mbarrier.  Once that mbarrier has seen all 256
 // rows a CTA holds all of A and T, builds the lookup tables and scores its keys.
@@ -805,13 +805,12 @@ __device__ __forceinline__ void prefetch_l2(const void* p, size_t bytes) {
                  : "memory");
 }
 
-// Coordinates 4*lane .. 4*lane+3 of one query row of 128 (through L2: the kernel before
-// this one on the stream may have written the query).
-__device__ __forceinline__ float4 load_query4(const float* q, int lane) {
-  return __ldcg(reinterpret_cast<const float4*>(q) + lane);
+// Coordinates 4*lane .. 4*lane+3 of one query row of 128, from the CTA's shared copy.
+__device__ __forceinline__ float4 query4(const float* q, int lane) {
+  return reinterpret_cast<const float4*>(q)[lane];
 }
-__device__ __forceinline__ float4 load_query4(const __nv_bfloat16* q, int lane) {
-  const uint2 v = __ldcg(reinterpret_cast<const uint2*>(q) + lane);
+__device__ __forceinline__ float4 query4(const __nv_bfloat16* q, int lane) {
+  const uint2 v = reinterpret_cast<const uint2*>(q)[lane];
   return make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u),
                      __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
 }
@@ -879,6 +878,7 @@ solve_packed_lut_kernel(const QT* __restrict__ Q, const float* __restrict__ Pi,
   __shared__ __align__(16) float sMine[R * QB];           // [R][QB]: this CTA's rows of A/T
   __shared__ __align__(8) uint64_t bars[2 + kFusedStages];   // rows, A/T, key tiles
   __shared__ float sCb[1 << BITS];
+  __shared__ __align__(16) QT sQ[QB * D];                 // the query tile (rows up to B)
   extern __shared__ __align__(128) float dsm[];
   float* lut = dsm;                                       // [QB][PER_Q]
   float* sRows = lut + QB * L::PER_Q;                     // [R][128]
@@ -917,7 +917,7 @@ solve_packed_lut_kernel(const QT* __restrict__ Q, const float* __restrict__ Pi,
       prefetch_l2(gamma_f16 + key0, static_cast<size_t>(npre) * 2);
     }
     const int nq = min(QB, B - b0);
-    if (nq > 0) prefetch_l2(Q + (static_cast<size_t>(p) * B + b0) * D, static_cast<size_t>(nq) * D * sizeof(QT));
+    prefetch_l2(Q + (static_cast<size_t>(p) * B + b0) * D, static_cast<size_t>(nq) * D * sizeof(QT));
   }
   // the barriers are initialised before any thread of the cluster uses them, and
   // every CTA of the cluster runs before anyone copies into a peer
@@ -925,9 +925,14 @@ solve_packed_lut_kernel(const QT* __restrict__ Q, const float* __restrict__ Pi,
   cluster_arrive_relaxed();
   cluster_wait();
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int nq = min(QB, B - b0);                          // >= 1
   if (tid == 0) {
-    expect_bytes(bar_rows, R * D * 4);
+    // the query tile comes with the rows: one request per CTA rather than one per warp
+    // that uses it (every CTA of the unit reads the same lines)
+    const uint32_t qbytes = static_cast<uint32_t>(nq * D * sizeof(QT));
+    expect_bytes(bar_rows, R * D * 4 + qbytes);
     bulk_g2s(sRows, rows_src, R * D * 4, bar_rows);
+    bulk_g2s(sQ, Q + (static_cast<size_t>(p) * B + b0) * D, qbytes, bar_rows);
     for (int t = 0; t < kFusedStages && t < ntiles; ++t) {
       const int nk = min(kT, k_end - k_begin - t * kT);
       uint8_t* st = sTiles + t * kTile;
@@ -946,13 +951,10 @@ solve_packed_lut_kernel(const QT* __restrict__ Q, const float* __restrict__ Pi,
   // group goes to every CTA of the cluster by its own bulk copies, completing bytes
   // on the receiver's mbarrier, so no warp waits for another here.
   if (warp < R / 8) {
+    const bool landed = wait_parity_bounded(bar_rows, 0, kFaultLut);
     float4 qx[QB];                                        // the query tile; rows past B are zero
 #pragma unroll
-    for (int q = 0; q < QB; ++q) {
-      qx[q] = b0 + q < B ? load_query4(Q + (static_cast<size_t>(p) * B + b0 + q) * D, lane)
-                         : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    const bool landed = wait_parity_bounded(bar_rows, 0, kFaultLut);
+    for (int q = 0; q < QB; ++q) qx[q] = q < nq ? query4(sQ + q * D, lane) : make_float4(0.f, 0.f, 0.f, 0.f);
     const int g = warp;
     float part[QB][8];
 #pragma unroll

@@ -136,6 +136,18 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 
+// L2 prefetch of [p, p + bytes), trimmed to whole 16-byte blocks inside the range.  A
+// hint only: what it brings into L2 is read by later loads, so it may be issued before
+// griddepcontrol.wait whatever the grid before this one writes.
+__device__ __forceinline__ void prefetch_l2(const void* p, size_t bytes) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  const uintptr_t lo = (a + 15) & ~static_cast<uintptr_t>(15);
+  const uintptr_t hi = (a + bytes) & ~static_cast<uintptr_t>(15);
+  if (hi > lo)
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(lo), "r"(static_cast<uint32_t>(hi - lo))
+                 : "memory");
+}
+
 // Fault bits, one per kernel family.
 enum : unsigned int { kFaultLut = 1u, kFaultMma = 2u, kFaultDecode = 4u, kFaultCompress = 8u };
 

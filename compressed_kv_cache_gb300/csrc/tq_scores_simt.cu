@@ -795,15 +795,6 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
                "l"(src), "r"(bytes), "r"(bar)
                : "memory");
 }
-// L2 prefetch of [p, p + bytes), trimmed to whole 16-byte blocks inside the range.
-__device__ __forceinline__ void prefetch_l2(const void* p, size_t bytes) {
-  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
-  const uintptr_t lo = (a + 15) & ~static_cast<uintptr_t>(15);
-  const uintptr_t hi = (a + bytes) & ~static_cast<uintptr_t>(15);
-  if (hi > lo)
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(lo), "r"(static_cast<uint32_t>(hi - lo))
-                 : "memory");
-}
 
 // Coordinates 4*lane .. 4*lane+3 of one query row of 128, from the CTA's shared copy.
 __device__ __forceinline__ float4 query4(const float* q, int lane) {

@@ -53,12 +53,15 @@ FALLBACK_HBM_GBS = 6800.0
 # reported null.
 # Writes that were still in L2 when the kernel ended are not in the figure.
 NCU_TRAFFIC = {
-    ("c1", "bf16_mma", "21322bf8f55c"): 8582144,      # scores_mma_kernel, unpacked, lite
-    ("c2", "fp32", "2bf1566ae994"): 6713088,          # solve_packed_lut_kernel, cluster of 8, staged keys
-    ("c3", "fp32", "2bf1566ae994"): 256231424,        # scores_packed_lut_kernel, stream-K
-    ("c4", "bf16_mma", "21322bf8f55c"): 89145600,     # scores_mma_kernel, packed 3-bit, full
-    ("m1", "fp32", "62ab8eab09d4"): 6573312,          # scores_mse_lut_kernel, stream-K
-    ("d1", "fp32", "d664c21c33df"): 13317120,         # decode_split_kernel + decode_combine_kernel
+    ("c1", "bf16_mma", "3ebe3055731f"): 8580352,      # scores_mma_kernel, unpacked, lite
+    ("c2", "fp32", "cb02f6e173b7"): 6714368,          # solve_packed_lut_kernel, cluster of 8
+    ("c3", "fp32", "cb02f6e173b7"): 255750912,        # scores_packed_lut8_kernel, stream-K, 4 queries
+    ("c4", "bf16_mma", "3ebe3055731f"): 89167104,     # scores_mma_kernel, packed 3-bit, full
+    ("m1", "fp32", "294cce443cd0"): 6573312,          # scores_mse_lut_kernel, stream-K
+    ("d1", "fp32", "584008419dc3"): 13317888,         # decode_split_kernel + decode_combine_kernel
+    ("d2", "fp32", "584008419dc3"): 13324032,         # the same, product keys
+    ("k1", "compress", "3cf3e4fc3955"): 16954880,     # compress_tile_kernel, packed output
+    ("s1", "split", "65e987245ff7"): 5256192,         # split_scores_kernel
 }
 
 
@@ -161,6 +164,7 @@ KERNEL_SOURCES = {
     "mse": ("tq_scores_mse.cu", "tq_lut.cuh", "tq_internal.cuh"),
     "decode": ("tq_decode.cu", "tq_lut.cuh", "tq_internal.cuh"),
     "split": ("tq_split.cu", "tq_internal.cuh"),
+    "compress": ("tq_compress.cu", "tq_internal.cuh"),
 }
 
 
@@ -691,7 +695,9 @@ def run_compress(args, w, tq, torch, dev):
                        "l2": f"{R} rotating key/output copies, {R * per_copy / 1e6:.0f} MB > 2x L2"},
             "key_gbs": nkeys * key_b / (ms / 1e3) / 1e9,
             "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                         "frac": achieved / peak, "traffic": None, "kernel": "compress_tile_kernel",
+                         "frac": achieved / peak,
+                         "traffic": NCU_TRAFFIC.get((args.config, "compress", kernel_fingerprint("compress"))),
+                         "kernel": "compress_tile_kernel", "kernel_fingerprint": kernel_fingerprint("compress"),
                          "kernel_ms": ms, "flops_per_launch": flops,
                          "peak_source": "152 SMs x 128 fp32 FMA lanes x 2 FLOP x max SM clock"},
             "timed_region": {"repeats": len(regions), "median_ms": statistics.median(regions)},
@@ -831,7 +837,8 @@ def run_split(args, w, tq, torch, dev):
                        "n_out": w.n_out, "out_bits": w.mse_bits + 1, "reg_bits": w.mse_bits,
                        "l2": f"{R} rotating copies, {R * per_copy / 1e6:.0f} MB > 2x L2"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": None, "kernel": "split_scores_kernel",
+                         "frac": achieved / peak, "traffic": NCU_TRAFFIC.get((args.config, "split", fp)),
+                         "kernel": "split_scores_kernel",
                          "kernel_ms": kernel_ms, "bytes_per_launch": kbytes,
                          "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
                          "kernel_fingerprint": fp},

@@ -113,6 +113,12 @@ tq_status check_pack_sizes(int64_t n_keys, int D, int bits) {
 
 }  // namespace
 
+namespace tq {
+// tq_faults.cu: one warp whose only bounded wait runs out, and that unit's fault word
+cudaError_t launch_wait_expiry(cudaStream_t st);
+cudaError_t take_faults_check(unsigned int* bits);
+}  // namespace tq
+
 extern "C" {
 
 const char* tq_status_string(tq_status status) {
@@ -134,9 +140,14 @@ tq_status tq_device_faults(unsigned int* bits) {
   if (e == cudaSuccess) e = tq::take_faults_mma(&v);
   if (e == cudaSuccess) e = tq::take_faults_decode(&v);
   if (e == cudaSuccess) e = tq::take_faults_compress(&v);
+  if (e == cudaSuccess) e = tq::take_faults_check(&v);
   if (e != cudaSuccess) return TQ_ERR_LAUNCH;
   *bits |= v;
   return TQ_OK;
+}
+
+tq_status tq_check_wait_expiry(cudaStream_t stream) {
+  return tq::launch_wait_expiry(stream) == cudaSuccess ? TQ_OK : TQ_ERR_LAUNCH;
 }
 
 tq_path tq_auto_path(int B, int D) {

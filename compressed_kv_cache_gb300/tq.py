@@ -39,6 +39,7 @@ _SIGNATURES = {
     "tq_status_string": ([_I], ctypes.c_char_p),
     "tq_auto_path": ([_I, _I], _I),
     "tq_device_faults": ([ctypes.POINTER(ctypes.c_uint)], _I),
+    "tq_check_wait_expiry": ([_P], _I),
     "tq_prepare_queries": ([_P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _P], _I),
     "tq_scores": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P], _I),
     "tq_scores_packed": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P], _I),
@@ -102,10 +103,16 @@ def auto_path(B: int, D: int) -> str:
 def device_faults() -> int:
     """Fault bits the bounded waits of libtq's kernels set on the current device since the
     last call (0 = none; 1 lookup-table scorers, 2 tensor-core scorer, 4 decode, 8
-    compressor); reading clears them.  Synchronises with the device."""
+    compressor, 16 check_wait_expiry); reading clears them.  Synchronises with the device."""
     v = ctypes.c_uint(0)
     _check("tq_device_faults", lib().tq_device_faults(ctypes.byref(v)))
     return int(v.value)
+
+
+def check_wait_expiry() -> None:
+    """Runs one warp whose only bounded wait can never complete, on the current stream:
+    after about a second it sets fault bit 16 and returns (see device_faults)."""
+    _check("tq_check_wait_expiry", lib().tq_check_wait_expiry(_stream()))
 
 
 def _check(fn: str, status: int) -> None:

@@ -83,10 +83,19 @@ tq_path tq_auto_path(int B, int D);
  * not compute and sets a fault bit on the device instead of hanging it.
  * tq_device_faults ORs into *bits the fault bits set on the CURRENT device since the
  * last call and clears them: 1 = fp32 lookup-table scorers, 2 = tensor-core scorer,
- * 4 = fused decode, 8 = compressor.  It synchronises with the device (it reads device
+ * 4 = fused decode, 8 = compressor, 16 = tq_check_wait_expiry.  It synchronises with the device (it reads device
  * memory) and is not for use inside stream capture.  bits: host pointer, not NULL.
  * Errors: TQ_ERR_INVALID_VALUE (bits NULL), TQ_ERR_LAUNCH (the device read failed). */
 tq_status tq_device_faults(unsigned int* bits);
+
+/* Failure path of the bounded waits, run on purpose (no counterpart in the pages).
+ * Launches one warp on `stream` whose only mbarrier wait can never complete: nothing
+ * arrives on it.  After the one-second budget the wait gives up, sets fault bit 16 and
+ * the kernel returns; the context stays usable and nothing else is written.  Read the
+ * bit with tq_device_faults once the stream has passed the call (about one second).
+ * For tests of a caller's fault handling; it computes nothing.
+ * Errors: TQ_ERR_LAUNCH. */
+tq_status tq_check_wait_expiry(cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
  * Query transform (riteshyadav.xyz, "Two kernels, two jobs", first kernel;

@@ -3,6 +3,8 @@
 Tolerances are the parity bounds: fp32 path max |err| <= 1e-5 (1 + |score|);
 bf16 tensor-core path max |err| <= 2e-3 ||q_b||_2; packing bit-exact.
 """
+import time
+
 import numpy as np
 import pytest
 
@@ -354,6 +356,22 @@ def test_device_errors_raise(tq):
 def test_no_bounded_wait_ran_out(tq):
     """Every bounded wait of the kernels above completed: no fault bit is set (reading clears them)."""
     tq.device_faults()
+    test_c2_single_query_decode(tq)
+    torch.cuda.synchronize()
+    assert tq.device_faults() == 0
+
+
+def test_bounded_wait_runs_out_and_reports(tq):
+    """A wait that nothing completes gives up after its budget: the kernel returns, the
+    fault bit reaches the host, reading clears it, and the context still computes."""
+    tq.device_faults()
+    t0 = time.perf_counter()
+    tq.check_wait_expiry()
+    torch.cuda.synchronize()
+    waited = time.perf_counter() - t0
+    assert tq.device_faults() == 16
+    assert tq.device_faults() == 0
+    assert 0.9 <= waited < 30.0
     test_c2_single_query_decode(tq)
     torch.cuda.synchronize()
     assert tq.device_faults() == 0

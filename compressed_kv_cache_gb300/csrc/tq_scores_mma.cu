@@ -392,16 +392,19 @@ scores_mma_kernel(const __grid_constant__ Params prm) {
   constexpr int kMmaWarp = Cfg<EPIW>::kMmaWarp;
   constexpr int kThreads = Cfg<EPIW>::kThreads;
   extern __shared__ __align__(1024) uint8_t smem[];
-  // [X: XS x 64K][Y NT*512][scores NT*512, full][key rows: kRawStages x 128 x (code row +
-  // sign row), full and packed][lut 256 words][cbf 256 halves][24 mbarriers][tmem slot]
-  constexpr bool kBulkEpilogue = EPIW == 16;
-  constexpr bool kRawTma = kBulkEpilogue && LAYOUT >= kPacked1;   // key rows by the copy engine
+  // [X: XS x 64K][Y NT*512][scores NT*512][key rows: kRawStages x 128 x (code row + sign
+  // row), full and packed][lut 256 words][cbf 256 halves][24 mbarriers][tmem slot]
+  constexpr bool kRawTma = EPIW == 16 && LAYOUT >= kPacked1;     // key rows by the copy engine
+  // The score tile of the tensor-store epilogue: a region of its own in the full
+  // configuration; in the lite one, whose query operand region is sized for 64 queries,
+  // the half that a tile of at most 32 queries leaves unused.
+  const bool sbuf_on = EPIW == 16 || prm.NT <= 32;
   constexpr int kCodeRow = 16 * RawRow<LAYOUT>::kBits;             // bytes of codes per packed key
   constexpr int kRawIdx = kM * kCodeRow, kRawSgn = kM * 16;        // bytes per stage
   uint8_t* X = smem;
   uint8_t* Yp = X + XS * kXBytes;
   float* sbuf = reinterpret_cast<float*>(Yp + prm.NT * kK * 2);   // [NT columns][128 keys]
-  uint8_t* rawp = reinterpret_cast<uint8_t*>(sbuf) + (kBulkEpilogue ? prm.NT * 512 : 0);
+  uint8_t* rawp = reinterpret_cast<uint8_t*>(sbuf) + (sbuf_on ? prm.NT * 512 : 0);
   uint32_t* lut = reinterpret_cast<uint32_t*>(rawp + (kRawTma ? kRawStages * (kRawIdx + kRawSgn) : 0));
   uint16_t* cbf = reinterpret_cast<uint16_t*>(lut + 256);
   // x_full[2] x_empty[2] acc_full[4] acc_empty[4] y raw_full[3] raw_empty[3]
@@ -476,18 +479,26 @@ scores_mma_kernel(const __grid_constant__ Params prm) {
   // The codebook (independent of the transform) is requested first, ahead of the key rows.
   const int C = prm.C;
   const float cval = tid < C ? __ldg(prm.codebook + tid) : 0.f;
-  // With the query operand prepared by the transform (one bulk copy), producers request
-  // their first tile's rows before the rest of the set-up, so the loads are in flight
-  // while the transform finishes and TMEM is prepared.  Without it, the rows are
-  // requested only after A and T have been read and converted: issued together, the
-  // flood of key rows would hold up those reads and with them the whole set-up.
+  // Without the loader warp, one thread asks L2 for the first tile's key rows at entry
+  // (a hint, carried out by the copy engine), and the producers load them into registers
+  // only after the set-up.  Loaded into registers at entry, the rows of every CTA queue
+  // in the SMs' load path ahead of the set-up's own reads and of the transform running
+  // beside this grid, and hold up the query operand (measured on c1: the query operand
+  // arrived 2.2 us later that way).
   constexpr bool kTwoDeep = false;   // one tile ahead: the register budget of 800 threads
   RawRow<LAYOUT> raw0, raw1;
-  const bool rows_early = prm.Ybf != nullptr;
-  if (!kRawTma && rows_early && warp < kProducerThreads / 32) {
-    if (static_cast<int>(blockIdx.x) < prm.key_tiles) load_row<LAYOUT>(prm, p, blockIdx.x, raw0);
-    if (kTwoDeep && static_cast<int>(blockIdx.x) + gx < prm.key_tiles)
-      load_row<LAYOUT>(prm, p, blockIdx.x + gx, raw1);
+  if (!kRawTma && tid == 0 && static_cast<int>(blockIdx.x) < prm.key_tiles) {
+    const size_t k0 = static_cast<size_t>(p) * prm.S + static_cast<size_t>(blockIdx.x) * kM;
+    const size_t n = static_cast<size_t>(min(kM, prm.S - static_cast<int>(blockIdx.x) * kM));
+    if constexpr (LAYOUT >= kPacked1) {
+      prefetch_l2(prm.idx + k0 * kCodeRow, n * kCodeRow);
+      prefetch_l2(prm.signs + k0 * 16, n * 16);
+      prefetch_l2(static_cast<const uint16_t*>(prm.gamma) + k0, n * 2);
+    } else {
+      prefetch_l2(prm.idx + k0 * 128, n * 128);
+      prefetch_l2(prm.signs + k0 * 128, n * 128);
+      prefetch_l2(static_cast<const float*>(prm.gamma) + k0, n * 4);
+    }
   }
 
   // --- set-up: TMEM, barriers, tables, the query operand ---
@@ -546,7 +557,7 @@ scores_mma_kernel(const __grid_constant__ Params prm) {
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (!kRawTma && !rows_early && warp < kProducerThreads / 32) {
+  if (!kRawTma && warp < kProducerThreads / 32) {
     if (static_cast<int>(blockIdx.x) < prm.key_tiles) load_row<LAYOUT>(prm, p, blockIdx.x, raw0);
     if (kTwoDeep && static_cast<int>(blockIdx.x) + gx < prm.key_tiles)
       load_row<LAYOUT>(prm, p, blockIdx.x + gx, raw1);
@@ -626,9 +637,9 @@ scores_mma_kernel(const __grid_constant__ Params prm) {
     const int cbeg = (e >> 2) * width;
     const int r = lg * 32 + lane;
     int i = 0;
-    if (kBulkEpilogue && prm.tma_scores && width == 32) {
-      // Full configuration (128 queries: 32 columns a warp) with a tensor map of the
-      // scores.  The four warps of a column
+    if (sbuf_on && prm.tma_scores && width == 32) {
+      // 32 columns a warp (128 queries in the full configuration, 32 in the lite one) and
+      // a tensor map of the scores.  The four warps of a column
       // group (one per lane quarter) drain their 32 columns into the shared score tile and
       // free the TMEM stage at once; one thread of the group then writes the 32 x 128
       // block with one tensor store, so the scores leave through the copy engine while

@@ -367,8 +367,8 @@ def decode_prod(A: np.ndarray, T: np.ndarray, k_idx: np.ndarray, k_signs: np.nda
     """Attention output over a TurboQuant_prod key cache and an MSE-quantized value cache
     ([ZT] "The Optimization Journey", v2 kernel 3 and v6 "Fused hybrid Triton kernel":
     per compressed block the TQ score, the value dequantization and the accumulation;
-    the score is the paper's <y, x_mse> + ||r|| sqrt(pi/2)/d <S y, qjl>, [ZT] "Relevance
-    to v6"):
+    the score is TurboQuant_prod's <y, x_mse> + ||r|| sqrt(pi/2)/d <S y, qjl>, [ZT]
+    "Relevance to v6"):
 
         s[b, i]  = scale * score[b, i]        (score: :func:`scores`, from A = Pi q, T = S_mat q)
         p[b, :]  = softmax(s[b, :])           (max subtracted)

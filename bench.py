@@ -188,6 +188,58 @@ def kernel_fingerprint(family: str) -> str:
     return h.hexdigest()[:12]
 
 
+def staging_pair(torch, dev, tensors):
+    """One pinned host buffer and one device buffer holding `tensors` (name -> host
+    tensor) back to back at 256-byte aligned offsets, so that a step's inputs travel in
+    one host-to-device copy; returns (host, device, {name: device view})."""
+    offs, off = {}, 0
+    for k, t in tensors.items():
+        offs[k] = off
+        off += (t.numel() * t.element_size() + 255) // 256 * 256
+    host = torch.empty(off, dtype=torch.uint8).pin_memory()
+    devb = torch.empty(off, dtype=torch.uint8, device=dev)
+    views = {}
+    for k, t in tensors.items():
+        nb = t.numel() * t.element_size()
+        host[offs[k]:offs[k] + nb].copy_(t.contiguous().view(-1).view(torch.uint8))
+        views[k] = devb[offs[k]:offs[k] + nb].view(t.dtype).view(t.shape)
+    return host, devb, views
+
+
+def time_e2e(torch, dev, streams, step, n, warmup):
+    """Times n end-to-end steps (step(k) issues step k, copies in, call, read-back, on
+    streams[k % 2]) two ways: issued from Python call by call, and captured once as a
+    CUDA graph and replayed.  Returns (graph_ms, eager_ms) for the n steps."""
+    def body(m):
+        streams[1].wait_stream(streams[0])          # the second stream forks from the first
+        for k in range(m):
+            step(k)
+        streams[0].wait_stream(streams[1])          # and joins it at the end
+
+    def timed(fn, reps=1):
+        es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(streams[0]):
+            es.record()
+            for _ in range(reps):
+                fn()
+            ee.record()
+        torch.cuda.synchronize(dev)
+        return es.elapsed_time(ee) / reps
+
+    with torch.cuda.stream(streams[0]):
+        body(max(2, warmup))
+    torch.cuda.synchronize(dev)
+    eager_ms = timed(lambda: body(n))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=streams[0]):
+        body(n)
+    with torch.cuda.stream(streams[0]):
+        for _ in range(max(1, warmup)):
+            g.replay()
+    torch.cuda.synchronize(dev)
+    return timed(g.replay, reps=5), eager_ms
+
+
 # ---------------------------------------------------------------------------
 # clocks
 # ---------------------------------------------------------------------------
@@ -652,26 +704,15 @@ def run_compress(args, w, tq, torch, dev):
                "h": tuple(torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in copies[i]["out"])}
               for i in range(2)]
 
-    def e2e_run(n):
-        es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        es.record(e_streams[0])
-        e_streams[1].wait_event(es)
-        for k in range(n):
-            eb = e_bufs[k % 2]
-            with torch.cuda.stream(e_streams[k % 2]):
-                eb["k"].copy_(hk, non_blocking=True)
-                tq.compress_keys_packed(eb["k"], Pi, S_mat, cb, w.mse_bits, out=eb["out"])
-                for h_, d_ in zip(eb["h"], eb["out"]):
-                    h_.copy_(d_, non_blocking=True)
-        e_streams[0].wait_stream(e_streams[1])
-        ee.record(e_streams[0])
-        return es, ee
-    e2e_run(args.warmup)
-    torch.cuda.synchronize(dev)
-    n_e = max(3, min(args.steps, 50))
-    es, ee = e2e_run(n_e)
-    torch.cuda.synchronize(dev)
-    e_ms = es.elapsed_time(ee)
+    def e2e_step(k):
+        eb = e_bufs[k % 2]
+        with torch.cuda.stream(e_streams[k % 2]):
+            eb["k"].copy_(hk, non_blocking=True)
+            tq.compress_keys_packed(eb["k"], Pi, S_mat, cb, w.mse_bits, out=eb["out"])
+            for h_, d_ in zip(eb["h"], eb["out"]):
+                h_.copy_(d_, non_blocking=True)
+    n_e = max(4, min(args.steps, 48)) // 2 * 2
+    e_ms, eager_ms = time_e2e(torch, dev, e_streams, e2e_step, n_e, args.warmup)
     cpu = None
     if not args.no_cpu_baseline:
         import oracle
@@ -704,7 +745,8 @@ def run_compress(args, w, tq, torch, dev):
             "cpu_baseline": cpu,
             "e2e": {"value": nkeys * n_e / (e_ms / 1e3), "unit": "keys/s",
                     "h2d_bytes_per_step": nkeys * key_b, "d2h_bytes_per_step": nkeys * out_b,
-                    "steps": n_e, "streams": 2},
+                    "steps": n_e, "streams": 2, "graph": True,
+                    "eager_value": nkeys * n_e / (eager_ms / 1e3)},
             "gpu_launches": steps, "clocks": clk}
     print(json.dumps(line), flush=True)
 
@@ -786,29 +828,18 @@ def run_split(args, w, tq, torch, dev):
                "Ar": copies[i]["Ar"], "out": copies[i]["out"],
                "h": torch.empty((w.P, w.B, w.S), dtype=torch.float32).pin_memory()} for i in range(2)]
 
-    def e2e_run(n):
-        es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        es.record(e_streams[0])
-        e_streams[1].wait_event(es)
-        for k in range(n):
-            eb = e_bufs[k % 2]
-            with torch.cuda.stream(e_streams[k % 2]):
-                eb["Q"].copy_(hQ, non_blocking=True)
-                for key in hc:
-                    eb["c"][key].copy_(hc[key], non_blocking=True)
-                eb["Po"].copy_(hPo, non_blocking=True)
-                eb["Pr"].copy_(hPr, non_blocking=True)
-                split_call(tq, w, eb["Q"], eb["Po"], eb["Pr"], eb["c"], eb["Ao"], eb["Ar"], eb["out"])
-                eb["h"].copy_(eb["out"], non_blocking=True)
-        e_streams[0].wait_stream(e_streams[1])
-        ee.record(e_streams[0])
-        return es, ee
-    e2e_run(args.warmup)
-    torch.cuda.synchronize(dev)
-    n_e = max(3, min(args.steps, 50))
-    es, ee = e2e_run(n_e)
-    torch.cuda.synchronize(dev)
-    e_ms = es.elapsed_time(ee)
+    def e2e_step(k):
+        eb = e_bufs[k % 2]
+        with torch.cuda.stream(e_streams[k % 2]):
+            eb["Q"].copy_(hQ, non_blocking=True)
+            for key in hc:
+                eb["c"][key].copy_(hc[key], non_blocking=True)
+            eb["Po"].copy_(hPo, non_blocking=True)
+            eb["Pr"].copy_(hPr, non_blocking=True)
+            split_call(tq, w, eb["Q"], eb["Po"], eb["Pr"], eb["c"], eb["Ao"], eb["Ar"], eb["out"])
+            eb["h"].copy_(eb["out"], non_blocking=True)
+    n_e = max(4, min(args.steps, 48)) // 2 * 2
+    e_ms, eager_ms = time_e2e(torch, dev, e_streams, e2e_step, n_e, args.warmup)
     cpu = None
     if not args.no_cpu_baseline:
         import oracle
@@ -846,7 +877,8 @@ def run_split(args, w, tq, torch, dev):
             "cpu_baseline": cpu,
             "e2e": {"value": w.P * w.B * w.S * n_e / (e_ms / 1e3), "unit": "scores/s",
                     "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": 4 * w.P * w.B * w.S,
-                    "steps": n_e, "streams": 2},
+                    "steps": n_e, "streams": 2, "graph": True,
+                    "eager_value": w.P * w.B * w.S * n_e / (eager_ms / 1e3)},
             "gpu_launches": 2 * steps, "clocks": clk}
     print(json.dumps(line), flush=True)
 
@@ -1074,25 +1106,29 @@ def main():
         d2h = int(np.prod(out_shape)) * 4
         e_streams = [stream, torch.cuda.Stream(device=dev)]
 
+        # every step's inputs (query, cache, rotation, projection, codebook) sit back to
+        # back in one pinned buffer and travel in one host-to-device copy
+        staged = {"Q": hostQ, "Pi": hPi, "cb": hcb, **{"c_" + k: v for k, v in hcache.items()}}
+        if not mse:
+            staged["S"] = hS
+
         def e2e_buffers():
-            return {"Q": torch.empty_like(Q0), "cache": {k: torch.empty_like(v) for k, v in cache0.items()},
-                    "Pi": torch.empty_like(Pi), "S": torch.empty_like(S_mat), "cb": torch.empty_like(cb),
+            hbuf, dbuf, v = staging_pair(torch, dev, staged)
+            cache = {k: v["c_" + k] for k in hcache}
+            cache.update({k: torch.empty_like(cache0[k]) for k in scratch if k in cache0})
+            return {"hbuf": hbuf, "dbuf": dbuf, "Q": v["Q"], "cache": cache, "Pi": v["Pi"],
+                    "S": v.get("S", v["Pi"]), "cb": v["cb"],
                     "out": torch.empty((w.P, w.B, w.S), device=dev),
                     "ws": torch.empty(tq.workspace_bytes(w.P, w.B, w.D), dtype=torch.uint8, device=dev),
                     "A": torch.empty((w.P, w.B, w.D), device=dev), "T": torch.empty((w.P, w.B, w.D), device=dev),
                     "hout": torch.empty(out_shape, dtype=torch.float32).pin_memory()}
         e_bufs = [e2e_buffers(), e2e_buffers()]
+        h2d = e_bufs[0]["hbuf"].numel()         # the bytes copied in each step, alignment included
 
         def e2e_step(k):
             eb = e_bufs[k % 2]
             with torch.cuda.stream(e_streams[k % 2]):
-                eb["Q"].copy_(hostQ, non_blocking=True)
-                for key in hcache:
-                    eb["cache"][key].copy_(hcache[key], non_blocking=True)
-                eb["Pi"].copy_(hPi, non_blocking=True)
-                if not mse:
-                    eb["S"].copy_(hS, non_blocking=True)
-                eb["cb"].copy_(hcb, non_blocking=True)
+                eb["dbuf"].copy_(eb["hbuf"], non_blocking=True)
                 dc, dA, dT, dout = eb["cache"], eb["A"], eb["T"], eb["out"]
                 if w.layout in ("decode", "decode_prod"):
                     tq.prepare_queries(eb["Q"], eb["Pi"], eb["Pi"] if mse else eb["S"], out=(dA, dT))
@@ -1111,26 +1147,12 @@ def main():
                                     eb["cb"], w.mse_bits, path=path, workspace=eb["ws"], out=dout)
                 eb["hout"].copy_(dout, non_blocking=True)
 
-        def e2e_run(n):
-            # both streams start after the start event and the first waits for the second
-            es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            es.record(e_streams[0])
-            e_streams[1].wait_event(es)
-            for k in range(n):
-                e2e_step(k)
-            e_streams[0].wait_stream(e_streams[1])
-            ee.record(e_streams[0])
-            return es, ee
-
-        e_steps = max(3, min(args.steps, 50))
-        e2e_run(args.warmup)
-        torch.cuda.synchronize(dev)
-        es, ee = e2e_run(e_steps)
-        torch.cuda.synchronize(dev)
-        e_ms = es.elapsed_time(ee)
+        e_steps = max(4, min(args.steps, 48)) // 2 * 2
+        e_ms, eager_ms = time_e2e(torch, dev, e_streams, e2e_step, e_steps, args.warmup)
         e2e = {"value": scores_per_step * e_steps / (e_ms / 1e3), "unit": "scores/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": e_steps,
-               "streams": 2}
+               "streams": 2, "graph": True,
+               "eager_value": scores_per_step * e_steps / (eager_ms / 1e3)}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

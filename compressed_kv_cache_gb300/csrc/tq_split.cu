@@ -127,6 +127,28 @@ __device__ __forceinline__ void mse_part(const uint32_t* __restrict__ words, int
   }
 }
 
+// The same sum from code words already in registers, for parts of at most 4 chunks.
+template <int BITS, int QB>
+__device__ __forceinline__ void mse_part_regs(const uint32_t (&wd)[4 * BITS], int chunks, const float* sA,
+                                              const float* sC, float (&m)[QB]) {
+  constexpr uint32_t kMask = (1u << BITS) - 1u;
+#pragma unroll
+  for (int ch = 0; ch < 4; ++ch) {
+    if (ch >= chunks) break;
+#pragma unroll
+    for (int u = 0; u < 32; ++u) {
+      const int pos = BITS * u;
+      const int wi = ch * BITS + (pos >> 5), sh = pos & 31;
+      const uint32_t nxt = (pos >> 5) + 1 < BITS ? wd[wi + 1] : 0u;
+      const uint32_t code = (sh + BITS <= 32) ? (wd[wi] >> sh) & kMask : __funnelshift_r(wd[wi], nxt, sh) & kMask;
+      const float c = sC[code];
+      const float* a = sA + (ch * 32 + u) * QB;
+#pragma unroll
+      for (int q = 0; q < QB; ++q) m[q] = fmaf(a[q], c, m[q]);
+    }
+  }
+}
+
 template <int BO, int BR, int QB>
 __global__ void __launch_bounds__(kSplitScoreThreads)
 split_scores_kernel(const float* __restrict__ A_out, const float* __restrict__ A_reg,
@@ -140,6 +162,24 @@ split_scores_kernel(const float* __restrict__ A_out, const float* __restrict__ A
   float* sCo = sAr + n_reg * QB;                          // [16]
   float* sCr = sCo + 16;                                  // [16]
   const int p = blockIdx.z, b0 = blockIdx.y * QB;
+  const int s = blockIdx.x * blockDim.x + threadIdx.x;
+  const size_t key = static_cast<size_t>(p) * S + (s < S ? s : 0);
+  // parts of at most 4 chunks (the printed split: 1 and 3): this thread's code words and
+  // norms are requested before the query staging below, so the two round trips overlap
+  const int co = n_out / 32, cr = n_reg / 32;
+  const bool early = co <= 4 && cr <= 4;
+  uint32_t wo[4 * BO], wr[4 * BR];
+  float no = 0.f, nr = 0.f;
+  if (early && s < S) {
+    const uint32_t* po = reinterpret_cast<const uint32_t*>(out_plane) + key * co * BO;
+    const uint32_t* pr = reinterpret_cast<const uint32_t*>(reg_plane) + key * cr * BR;
+#pragma unroll
+    for (int i = 0; i < 4 * BO; ++i) wo[i] = i < co * BO ? __ldg(po + i) : 0u;
+#pragma unroll
+    for (int i = 0; i < 4 * BR; ++i) wr[i] = i < cr * BR ? __ldg(pr + i) : 0u;
+    no = __half2float(__ushort_as_half(__ldg(out_norm + key)));
+    nr = __half2float(__ushort_as_half(__ldg(reg_norm + key)));
+  }
   for (int e = threadIdx.x; e < QB * n_out; e += blockDim.x) {
     const int q = e / n_out, d = e % n_out;
     sAo[d * QB + q] = b0 + q < B ? A_out[(static_cast<size_t>(p) * B + b0 + q) * n_out + d] : 0.f;
@@ -151,16 +191,19 @@ split_scores_kernel(const float* __restrict__ A_out, const float* __restrict__ A
   if (threadIdx.x < (1 << BO)) sCo[threadIdx.x] = cb_out[threadIdx.x];
   if (threadIdx.x < (1 << BR)) sCr[threadIdx.x] = cb_reg[threadIdx.x];
   __syncthreads();
-  const int s = blockIdx.x * blockDim.x + threadIdx.x;
   if (s >= S) return;
-  const size_t key = static_cast<size_t>(p) * S + s;
   float mo[QB], mr[QB];
 #pragma unroll
   for (int q = 0; q < QB; ++q) mo[q] = mr[q] = 0.f;
-  mse_part<BO, QB>(reinterpret_cast<const uint32_t*>(out_plane) + key * (n_out / 32) * BO, n_out / 32, sAo, sCo, mo);
-  mse_part<BR, QB>(reinterpret_cast<const uint32_t*>(reg_plane) + key * (n_reg / 32) * BR, n_reg / 32, sAr, sCr, mr);
-  const float no = __half2float(__ushort_as_half(__ldg(out_norm + key)));
-  const float nr = __half2float(__ushort_as_half(__ldg(reg_norm + key)));
+  if (early) {
+    mse_part_regs<BO, QB>(wo, co, sAo, sCo, mo);
+    mse_part_regs<BR, QB>(wr, cr, sAr, sCr, mr);
+  } else {
+    mse_part<BO, QB>(reinterpret_cast<const uint32_t*>(out_plane) + key * co * BO, co, sAo, sCo, mo);
+    mse_part<BR, QB>(reinterpret_cast<const uint32_t*>(reg_plane) + key * cr * BR, cr, sAr, sCr, mr);
+    no = __half2float(__ushort_as_half(__ldg(out_norm + key)));
+    nr = __half2float(__ushort_as_half(__ldg(reg_norm + key)));
+  }
 #pragma unroll
   for (int q = 0; q < QB; ++q)
     if (b0 + q < B) scores[(static_cast<size_t>(p) * B + b0 + q) * S + s] = fmaf(no, mo[q], nr * mr[q]);

@@ -61,7 +61,7 @@ NCU_TRAFFIC = {
     ("d1", "fp32", "584008419dc3"): 13317888,         # decode_split_kernel + decode_combine_kernel
     ("d2", "fp32", "584008419dc3"): 13324032,         # the same, product keys
     ("k1", "compress", "3cf3e4fc3955"): 16954880,     # compress_tile_kernel, packed output
-    ("s1", "split", "65e987245ff7"): 5256192,         # split_scores_kernel
+    ("s1", "split", "a002a5eeb0d2"): 5281280,         # split_scores_kernel
 }
 
 

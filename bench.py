@@ -53,10 +53,10 @@ FALLBACK_HBM_GBS = 6800.0
 # reported null.
 # Writes that were still in L2 when the kernel ended are not in the figure.
 NCU_TRAFFIC = {
-    ("c1", "bf16_mma", "c62fd8e369ee"): 8586496,      # scores_mma_kernel, unpacked, lite
+    ("c1", "bf16_mma", "d0448b366b12"): 8586496,      # scores_mma_kernel, unpacked, lite
     ("c2", "fp32", "cb02f6e173b7"): 6714368,          # solve_packed_lut_kernel, cluster of 8
     ("c3", "fp32", "cb02f6e173b7"): 255750912,        # scores_packed_lut8_kernel, stream-K, 4 queries
-    ("c4", "bf16_mma", "c62fd8e369ee"): 89109760,     # scores_mma_kernel, packed 3-bit, full
+    ("c4", "bf16_mma", "d0448b366b12"): 89109760,     # scores_mma_kernel, packed 3-bit, full
     ("m1", "fp32", "294cce443cd0"): 6573312,          # scores_mse_lut_kernel, stream-K
     ("d1", "fp32", "584008419dc3"): 13317888,         # decode_split_kernel + decode_combine_kernel
     ("d2", "fp32", "584008419dc3"): 13324032,         # the same, product keys

@@ -18,21 +18,27 @@
 // no-swizzle canonical layout: 8-row x 16-byte core matrices, row groups 128 B
 // apart (SBO), K-adjacent core matrices one row-group column apart (LBO).
 //
-// Persistent CTAs, warp-specialised (shown for the full configuration, 25 warps):
-//   warps 0-7   producers: thread = (key row, half); load the next tile's rows into
-//               registers, wait for a free shared-memory stage, dequantise into it,
-//               arrive on x_full;
-//   warps 8-23  epilogue: four warps per TMEM lane quarter (each drains a quarter of
-//               the N columns); wait for a full accumulator stage, tcgen05.ld,
-//               coalesced global stores, arrive on acc_empty;
-//   warp 24     MMA: allocates TMEM; one lane waits for x_full and acc_empty, issues
-//               the 16 MMAs of a tile and commits them to x_empty and acc_full.
-// Two shared-memory stages and up to four TMEM accumulator stages, so dequantisation,
-// the MMAs and the draining of several tiles overlap.  The epilogue reads its columns
-// 32 at a time with one tcgen05.wait::ld per batch.  Every wait
-// on an mbarrier is bounded; a wait that runs out raises a CTA-wide abort flag, every
-// role leaves its loop (the epilogue writes NaN for a tile it could not drain), and
-// TMEM is still released.
+// Persistent CTAs, warp-specialised.  Full configuration (one CTA per SM, 26 warps):
+//   warps 0-7   producers: thread = (key row, half of K); take the tile's rows from a
+//               shared-memory stage (packed rows, filled by the loader) or from registers
+//               (unpacked rows, loaded after the set-up), wait for their half of X to be
+//               free, dequantise into it, arrive on that half's x_full;
+//   warps 8-23  epilogue: four warps per TMEM lane quarter, a column group of 32 queries
+//               each; wait for a full accumulator stage, tcgen05.ld, stage the 32 x 128
+//               scores in shared memory and write them with one tensor store, arrive on
+//               acc_empty;
+//   warp 24     MMA: allocates TMEM; one lane waits for each half of X and for a free
+//               accumulator stage, issues the tile's 16 MMAs (8 a half) and commits them
+//               to the halves' x_empty and to acc_full;
+//   warp 25     loader: bulk-copies packed code and sign rows into three stages, three
+//               tiles ahead, and asks L2 for their gamma.
+// One X stage split by K into halves with their own barriers, and four TMEM accumulator
+// stages, so one half is dequantised while the MMAs read the other and the draining of
+// earlier tiles overlaps both.  The lite configuration (two CTAs per SM, at most two
+// tiles an SM) has four epilogue warps and no loader; at up to 32 queries its score tile
+// sits in the unused half of the query operand region.  Every wait on an mbarrier is
+// bounded; a wait that runs out raises a CTA-wide abort flag, every role leaves its loop
+// (the epilogue writes NaN for a tile it could not drain), and TMEM is still released.
 #include <atomic>
 
 #include <cuda.h>            // CUtensorMap (types only; the encoder comes from the runtime)
